@@ -1,0 +1,480 @@
+"""Benchmark: one step of the paged prefix-reuse hot path on synthetic data.
+
+A step is the whole path over one batch: copy-on-write block copies, slot
+indexing, append of the new tokens' K/V, prefix attention of the prefill
+chunks and decode attention of the decode batch (whichever the workload has).
+The default workload is the shared-system-prompt batch (Qwen2.5-3B-shaped
+layer: Hq=16, Hkv=2, d=128, bf16; 8 requests sharing a 1024-token prefix,
+256 new tokens each, 8192-block pool).
+
+Prints ONE JSON line.  ``value`` is the algorithmic prefix-attention
+TFLOP/s of the whole step (4*d*Hq*sum(N*P + N(N+1)/2) per step, divided by
+the device time of the step), with inputs resident in HBM and L2 flushed
+between timed steps.  ``e2e`` is the same metric measured through the C ABI
+with pinned host buffers: the step's inputs are copied host->device and its
+outputs device->host inside the timed region.
+
+    python bench.py [--steps K] [--warmup W] [--workload NAME] [--impl kvp|reference]
+
+With several GPUs (torchrun), every rank runs an independent replica (the
+path has no exchange step) and the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "paged prefix-attn TFLOP/s + decode tok/s; % of GB300 tensor/HBM roofline"
+WORKLOADS = {
+    "shared_system_prompt": 2,
+    "rag_chunk_reuse": 3,
+    "continuous_batching_step": 4,
+    "long_context_prefix": 5,
+}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work (the FLOP and byte conventions of the measurement)
+# ---------------------------------------------------------------------------
+def prefill_flops(w) -> float:
+    """4 * d * Hq * sum_s (N_s * P_s + N_s (N_s + 1) / 2) over the prefill chunks."""
+    n = w.new_lens[: w.num_prefill].astype(np.float64)
+    p = w.prefix_lens[: w.num_prefill].astype(np.float64)
+    return float(4.0 * w.head_dim * w.num_q_heads * np.sum(n * p + n * (n + 1) / 2))
+
+
+def decode_kv_bytes(w) -> float:
+    """Unique K+V bytes read by the decode batch (each sequence's context)."""
+    L = w.context_lens[w.num_prefill :].astype(np.float64)
+    return float(np.sum(L) * w.num_kv_heads * w.head_dim * 2 * 2)
+
+
+def row_flops(w, rows) -> float:
+    """Algorithmic flops of the given flat prefill rows t * Hq + h: 4 d (p + 1)."""
+    cu = w.cu_seqlens_q
+    t = np.asarray(rows) // w.num_q_heads
+    s = np.searchsorted(cu, t, side="right") - 1
+    pos = w.context_lens[s] - w.new_lens[s] + (t - cu[s])
+    return float(np.sum(4.0 * w.head_dim * (pos + 1)))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            return d, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _peak_value(peaks, *keys):
+    for k in keys:
+        v = peaks.get(k)
+        if isinstance(v, (int, float)) and v > 0:
+            return float(v)
+        if isinstance(v, dict):
+            for kk in ("value", "burst", "gbs", "tflops"):
+                if isinstance(v.get(kk), (int, float)):
+                    return float(v[kk])
+    return None
+
+
+def committed_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if that summary
+    was taken on the kernel source as it is now (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
+    src = os.path.join(ROOT, "paged_prefix_reuse_gb300", "csrc", f"kvp_{kernel}.cu")
+    if not (os.path.exists(path) and os.path.exists(src)):
+        return None
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    vals = {}
+    for line in open(path):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("source_sha256_16") != digest:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.idx = device_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.idx)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed bookkeeping (replicas only)
+# ---------------------------------------------------------------------------
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_oracle_sample(w, budget_s: float, seed: int = 0):
+    """Time the fp64 oracle on a bounded random sample of prefill rows (and
+    decode rows) of the workload; returns (tflops, seconds, rows, threads)."""
+    import oracle
+
+    rng = np.random.default_rng(seed)
+    tq = int(w.cu_seqlens_q[w.num_prefill])
+    all_rows = tq * w.num_q_heads
+    cu = w.cu_seqlens_q[: w.num_prefill + 1]
+    ctx = w.context_lens[: w.num_prefill]
+    bt = w.block_tables[: w.num_prefill]
+    n = 16
+    spent, flops, done = 0.0, 0.0, 0
+    while spent < budget_s and done < all_rows:
+        rows = rng.integers(0, all_rows, size=n)
+        t0 = time.perf_counter()
+        oracle.prefix_attn(w.dtype, w.k_pool, w.v_pool, w.q[:tq], cu, ctx, bt, w.softmax_scale, rows)
+        dt = time.perf_counter() - t0
+        spent += dt
+        flops += row_flops(w, rows)
+        done += n
+        if dt < budget_s / 8:
+            n *= 2
+    return flops / spent / 1e12, spent, done, oracle.num_threads()
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    w = wl.make_config(WORKLOADS[args.workload])
+    flops = prefill_flops(w)
+    per_step_budget = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, per_step_budget / 4)
+    vals, secs, rows_done, threads = [], 0.0, 0, 1
+    for i in range(args.steps):
+        v, s, r, threads = cpu_oracle_sample(w, per_step_budget, seed=i + 1)
+        vals.append(v)
+        secs += s
+        rows_done += r
+    value = float(np.mean(vals))
+    ms = flops / (value * 1e12) * 1e3
+    sample = (f"{rows_done} random (query token, head) rows of the prefill batch over {args.steps} steps, "
+              f"{secs:.1f} s of CPU time; value scales the sample's algorithmic flops to the whole step")
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_kvp(args):
+    import torch
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    from paged_prefix_reuse_gb300 import build as kvp_build
+
+    kvp_build.build_library()
+    import paged_prefix_reuse_gb300 as kvp
+    from paged_prefix_reuse_gb300.step import DeviceStep
+
+    kvp.load_library()
+    w = wl.make_config(WORKLOADS[args.workload])
+    st = DeviceStep(w, device=dev, prefix_splits=args.prefix_splits, decode_splits=args.decode_splits)
+    stream = torch.cuda.Stream(device=dev)
+    flops = prefill_flops(w)
+    dec_bytes = decode_kv_bytes(w)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    # kernels launched per step (ours, counted from the calls the step makes)
+    launches = 0
+    launches += 1 if st.pairs.shape[0] else 0
+    launches += 2 if st.T else 0  # slot mapping + append
+    if st.npf:
+        launches += 1 + (1 if st.prefix_splits > 1 else 0)
+    if st.ndec:
+        launches += 1 + (1 if st.decode_splits > 1 else 0)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    # ---- device-resident timing: per step events, L2 flushed between steps ----
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            st.run(stream)
+        stream.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        kev = {k: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)] for k in ("prefill", "decode", "append", "copy", "slots")}
+        clocks = ClockSampler(dev.index if world == 1 else local)
+        barrier()
+        torch.cuda.synchronize()
+        clocks.start()
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            kev["copy"][i][0].record(stream)
+            st.run_copy(stream)
+            kev["copy"][i][1].record(stream)
+            kev["slots"][i][0].record(stream)
+            st.run_slots(stream)
+            kev["slots"][i][1].record(stream)
+            kev["append"][i][0].record(stream)
+            st.run_append(stream)
+            kev["append"][i][1].record(stream)
+            kev["prefill"][i][0].record(stream)
+            st.run_prefill(stream)
+            kev["prefill"][i][1].record(stream)
+            kev["decode"][i][0].record(stream)
+            st.run_decode(stream)
+            kev["decode"][i][1].record(stream)
+            ev[i][1].record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize()
+        barrier()
+        wall = time.perf_counter() - t_wall
+        clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = {k: float(np.mean([a.elapsed_time(b) for a, b in v])) for k, v in kev.items()}
+    ms = float(np.mean(step_ms))
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end through the C ABI with pinned host buffers ----
+    host_in = {name: getattr(st, name).cpu().pin_memory() for name in ("q", "k_new", "v_new", "cu", "ctx", "bt")}
+    if st.pairs.shape[0]:
+        host_in["pairs"] = st.pairs.cpu().pin_memory()
+    outs = []
+    if st.npf:
+        outs += [st.out_pf, st.lse_pf]
+    if st.ndec:
+        outs += [st.out_dec, st.lse_dec]
+    host_out = [o.cpu().pin_memory() for o in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    e2e_ms = []
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for name, t in host_in.items():
+                getattr(st, name).copy_(t, non_blocking=True)
+            st.run(stream)
+            for o, h in zip(outs, host_out):
+                h.copy_(o, non_blocking=True)
+            b.record(stream)
+            stream.synchronize()
+            if i >= args.warmup:
+                e2e_ms.append(a.elapsed_time(b))
+    e2e = float(np.mean(e2e_ms))
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e = float(t.item())
+
+    if rank != 0:
+        return 0
+    peaks, peak_src = load_peaks()
+    value = world * flops / (ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f16",
+        "data": "synthetic",
+        "config": {
+            "workload": args.workload,
+            "B": w.B,
+            "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim,
+            "block_size": w.block_size,
+            "num_blocks": w.num_blocks,
+            "prefill_tokens": int(w.cu_seqlens_q[w.num_prefill]),
+            "decode_seqs": int(w.num_decode),
+            "prefix_splits": int(getattr(st, "prefix_splits", 0)),
+            "decode_splits": int(getattr(st, "decode_splits", 0)),
+            "l2": "flushed (512 MB write) before every timed step",
+            "parallelism": f"replicas x{world}",
+        },
+        "gpu_launches": launches * args.steps,
+        "kernel_ms": kern_ms,
+        "wall_s": wall,
+        "e2e": {"value": world * flops / (e2e * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clk,
+    }
+    if st.npf:
+        peak = _peak_value(peaks, "bf16_tflops", "bf16_tflops_burst") or FALLBACK_PEAKS["bf16_tflops"]
+        achieved = flops / (kern_ms["prefill"] * 1e-3) / 1e12
+        line["roofline"] = {
+            "kernel": "prefix_attn" + (" + lse_merge" if st.prefix_splits > 1 else ""),
+            "bound": "tensor",
+            "achieved": achieved,
+            "peak": peak,
+            "unit": "TFLOP/s",
+            "frac": achieved / peak,
+            "peak_source": f"{peak_src} bf16 dense (burst)" + (", fp16 taken equal to bf16" if w.dtype == "f16" else ""),
+            "traffic": committed_traffic("prefix", args.workload),
+        }
+    if st.ndec:
+        hbm = _peak_value(peaks, "hbm_gbs", "hbm_GBps") or FALLBACK_PEAKS["hbm_gbs"]
+        gbs = dec_bytes / (kern_ms["decode"] * 1e-3) / 1e9
+        line["decode"] = {
+            "tok_s": w.num_decode / (kern_ms["decode"] * 1e-3),
+            "achieved_gbs": gbs,
+            "peak_gbs": hbm,
+            "frac": gbs / hbm,
+            "peak_source": peak_src,
+            "traffic": committed_traffic("decode", args.workload),
+        }
+        if not st.npf:
+            line["roofline"] = {"kernel": "decode_attn", "bound": "hbm", "achieved": gbs, "peak": hbm,
+                                "unit": "GB/s", "frac": gbs / hbm, "peak_source": peak_src,
+                                "traffic": committed_traffic("decode", args.workload)}
+    if not args.no_cpu_baseline and world >= 1:
+        v, s, r, threads = cpu_oracle_sample(w, args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": v,
+            "unit": "TFLOP/s",
+            "cores": threads,
+            "kind": "oracle",
+            "sample": f"{r} random (query token, head) rows of the prefill batch, {s:.1f} s; "
+                      f"flops of the sample / CPU time",
+        }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["kvp", "reference"], default="kvp")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="shared_system_prompt")
+    ap.add_argument("--prefix-splits", type=int, default=0)
+    ap.add_argument("--decode-splits", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_kvp(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,175 @@
+/*
+ * kvp.h -- C ABI of libkvp: paged prefix-reuse attention on one GB300 GPU.
+ *
+ * The operation (kvboost 0.6.0, "How it works" step 5 and "CPU paged
+ * attention"; kvstream 0.1.0, "Request lifecycle" and "Configuration"):
+ * a request's new tokens attend causally to the K/V of a cached prefix plus
+ * their own K/V.  K/V live in a pool of fixed-size physical blocks addressed
+ * through a per-request block table; a block may be named by several tables
+ * (shared copy-on-write); new tokens' K/V are written into the pool one slot
+ * per token.  Paging changes where bytes live, not the mathematics: the
+ * result is ordinary causal softmax attention over the logical sequence.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Pool:   k_pool and v_pool are separate device arrays laid out
+ *         [num_blocks][num_kv_heads][block_size][head_dim], elements fp16 or
+ *         bf16.  One block of K plus V is block_size x heads x head_dim x 2
+ *         x dtype_bytes, the page size of the kvstream.yaml "memory" comment.
+ * Tokens: the new tokens of B sequences are packed back to back: sequence s
+ *         owns rows cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1 of q/out/k_new.
+ *         context_lens[s] = cached prefix tokens + new tokens of sequence s.
+ *         New token i of sequence s sits at absolute position
+ *         context_lens[s] - N_s + i (bottom-right causal alignment) and sees
+ *         keys 0 .. that position.
+ * Tables: block_tables is int32 [B][max_blocks]; logical token j of sequence
+ *         s lives in physical block block_tables[s][j / block_size], row
+ *         j % block_size.  Entries past ceil(context_lens[s]/block_size) are
+ *         never read.
+ * GQA:    query head h reads kv head h / (num_q_heads / num_kv_heads).
+ * Memory: every pointer argument is caller-owned; device pointers must stay
+ *         valid until the enqueued work completes.  The library allocates
+ *         nothing and keeps no per-call state.
+ * Async:  every call enqueues kernels on `stream` (a cudaStream_t, NULL =
+ *         legacy default stream) and returns after launch.  It does not
+ *         synchronise.
+ * Errors: arguments checkable on the host are validated before any launch
+ *         and reported by the return value (nothing is enqueued then).
+ *         Device-resident indices (block ids, slots, lengths) are checked in
+ *         the kernels: a bad entry is skipped and a KVP_DEVERR_* bit is
+ *         OR-ed into *pool->err_word when err_word is non-NULL.  No kernel
+ *         traps.  Every wait inside a kernel is bounded; a wait that gives
+ *         up sets KVP_DEVERR_TIMEOUT and the kernel returns.
+ */
+#ifndef KVP_H_
+#define KVP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KVP_OK = 0,
+    KVP_ERR_INVALID_ARG = 1, /* null/misaligned pointer, negative size, Hq % Hkv != 0 ... */
+    KVP_ERR_UNSUPPORTED = 2, /* head_dim not 64/96/128, dtype, block_size not 8/16/32 */
+    KVP_ERR_WORKSPACE = 3,   /* workspace missing or smaller than kvp_workspace_size() */
+    KVP_ERR_CUDA = 4,        /* a CUDA runtime/driver call or launch failed */
+    KVP_ERR_TIMEOUT = 5      /* reserved for host-side reporting of KVP_DEVERR_TIMEOUT */
+} kvp_status;
+
+typedef enum { KVP_F16 = 0, KVP_BF16 = 1 } kvp_dtype;
+
+/* Bits OR-ed into *err_word by the kernels. */
+#define KVP_DEVERR_BAD_BLOCK 0x1u /* a block-table entry outside [0, num_blocks) */
+#define KVP_DEVERR_BAD_SLOT 0x2u  /* a slot outside [0, num_blocks*block_size), not -1 */
+#define KVP_DEVERR_BAD_PAIR 0x4u  /* a copy pair naming a block outside the pool */
+#define KVP_DEVERR_BAD_LEN 0x8u   /* context_len < new tokens, or a table too short */
+#define KVP_DEVERR_TIMEOUT 0x10u  /* a bounded in-kernel wait gave up */
+
+typedef struct {
+    void *k_pool;          /* device, [num_blocks][num_kv_heads][block_size][head_dim], 16-B aligned */
+    void *v_pool;          /* device, same shape and dtype as k_pool */
+    int64_t num_blocks;    /* physical blocks in the pool, >= 1 */
+    int32_t block_size;    /* tokens per block: 8, 16 or 32 (kvstream.yaml: power of two 8/16/32) */
+    int32_t num_kv_heads;  /* >= 1 */
+    int32_t head_dim;      /* 64, 96 or 128 (kvboost "Flash Attention (CUDA)" table) */
+    int32_t dtype;         /* kvp_dtype: fp16 or bf16 (same table) */
+    uint32_t *err_word;    /* device uint32 that kernels OR KVP_DEVERR_* bits into; may be NULL */
+} kvp_pool;
+
+/* Slot of every new token (kvstream "Request lifecycle" step 2: the page
+ * table grows one slot per token).  For token i of sequence s at position
+ * p = context_lens[s] - N_s + i:
+ *     slot_mapping[cu_seqlens_q[s] + i] = block_tables[s][p / bs] * bs + p % bs.
+ * cu_seqlens_q: device int32 [B+1], non-decreasing, cu_seqlens_q[B] == total_q.
+ * context_lens: device int32 [B].  block_tables: device int32 [B][max_blocks].
+ * slot_mapping: device int64 [total_q], written.  A token whose table entry
+ * is missing or outside the pool gets slot -1 and sets KVP_DEVERR_BAD_BLOCK
+ * (or KVP_DEVERR_BAD_LEN when p / bs >= max_blocks or p < 0). */
+kvp_status kvp_slot_mapping(const kvp_pool *pool, const int32_t *cu_seqlens_q, const int32_t *context_lens,
+                            const int32_t *block_tables, int32_t max_blocks, int32_t B, int32_t total_q,
+                            int64_t *slot_mapping, void *stream);
+
+/* Append (kvstream "Request lifecycle" step 2; kvboost "How it works" step
+ * 5, write-back of newly seen chunks): for every token t with
+ * slot = slot_mapping[t] != -1 and every kv head h,
+ *     k_pool[slot / bs][h][slot % bs][:] = k_new[t][h][:]   (same for V).
+ * k_new, v_new: device [T][num_kv_heads][head_dim] in the pool dtype, 16-B
+ * aligned.  slot_mapping: device int64 [T].  Slots must be distinct (two
+ * tokens writing one slot race).  A slot outside the pool is skipped and
+ * sets KVP_DEVERR_BAD_SLOT.  T == 0 is a no-op. */
+kvp_status kvp_cache_append(const kvp_pool *pool, const void *k_new, const void *v_new,
+                            const int64_t *slot_mapping, int32_t T, void *stream);
+
+/* Copy-on-write fork (kvboost "CPU paged attention": shared prefixes share
+ * physical blocks copy-on-write; kvstream "Request lifecycle" step 3: a
+ * forked table shares pages, which are never duplicated): before a sequence
+ * writes into a block it shares, the block is copied to a private one:
+ *     k_pool[pairs[i][1]] = k_pool[pairs[i][0]]  (whole block, all heads; same for V).
+ * pairs: device int32 [n][2] = (src, dst).  Destinations must be distinct
+ * and no destination may also be a source in the same call; otherwise the
+ * result is undefined.  A pair naming a block outside the pool is skipped
+ * and sets KVP_DEVERR_BAD_PAIR.  n == 0 is a no-op. */
+kvp_status kvp_block_copy(const kvp_pool *pool, const int32_t *pairs, int32_t n, void *stream);
+
+/* Causal attention of a chunk of new tokens over the cached prefix plus the
+ * chunk itself (kvboost "How it works" step 5 and "Flash Attention (CUDA)":
+ * tiled online softmax, fp16/bf16, head_dim 64/96/128, any length, causal
+ * with future tiles skipped):
+ *     out[t][h] = sum_j softmax_j(scale * q[t][h] . K_s[j]) V_s[j],  j <= position(t)
+ *     lse[h][t] = ln(sum_j exp(scale * q[t][h] . K_s[j]))            (natural log)
+ * where K_s, V_s is sequence s's logical K/V read through block_tables and
+ * kv head h / (num_q_heads / num_kv_heads).  ALL keys are read from the
+ * pool, so the chunk's own K/V must have been appended first.
+ * q, out: device [total_q][num_q_heads][head_dim], pool dtype, 16-B aligned.
+ * lse: device float [num_q_heads][total_q], or NULL.
+ * max_q_len >= every N_s; max_context_len >= every context_lens[s] (they size
+ * the grid; larger values only waste empty blocks).
+ * num_splits: 0 = the library chooses (kvp_prefix_num_splits); >= 1 splits
+ * every query tile's key range into that many parts merged by log-sum-exp.
+ * When the resolved count is > 1 the call needs workspace_bytes >=
+ * kvp_workspace_size(0, total_q, num_q_heads, head_dim, splits) of device
+ * memory (its contents need no initialisation). */
+kvp_status kvp_prefix_attn(const kvp_pool *pool, const void *q, void *out, float *lse, const int32_t *cu_seqlens_q,
+                           const int32_t *context_lens, const int32_t *block_tables, int32_t max_blocks, int32_t B,
+                           int32_t total_q, int32_t num_q_heads, int32_t max_q_len, int32_t max_context_len,
+                           float softmax_scale, int32_t num_splits, void *workspace, size_t workspace_bytes,
+                           void *stream);
+
+/* Decode attention for a continuous batch (kvstream "Why KVStream?" and
+ * "Request lifecycle": one new token per sequence per step): prefix
+ * attention with N_s = 1 for every sequence, keys 0 .. context_lens[s]-1.
+ * q, out: device [B][num_q_heads][head_dim]; lse: device float
+ * [num_q_heads][B] or NULL.  num_q_heads / num_kv_heads must be <= 16.
+ * num_splits: 0 = the library chooses (kvp_decode_num_splits); otherwise the
+ * longest context is cut into at most that many key ranges, each processed
+ * by its own CTA and merged by log-sum-exp; the call then needs
+ * workspace_bytes >= kvp_workspace_size(1, B, num_q_heads, head_dim, splits). */
+kvp_status kvp_decode_attn(const kvp_pool *pool, const void *q, void *out, float *lse, const int32_t *context_lens,
+                           const int32_t *block_tables, int32_t max_blocks, int32_t B, int32_t num_q_heads,
+                           int32_t max_context_len, float softmax_scale, int32_t num_splits, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/* Split counts the library picks for num_splits == 0. */
+int32_t kvp_prefix_num_splits(int32_t B, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t max_q_len, int32_t max_context_len);
+int32_t kvp_decode_num_splits(int32_t B, int32_t num_kv_heads, int32_t block_size, int32_t max_context_len);
+
+/* Device workspace bytes for op 0 (prefix: rows = total_q) or op 1 (decode:
+ * rows = B) at a given split count; 0 when num_splits <= 1. */
+size_t kvp_workspace_size(int32_t op, int32_t rows, int32_t num_q_heads, int32_t head_dim, int32_t num_splits);
+
+/* Static, NUL-terminated description of a status code. */
+const char *kvp_status_string(kvp_status status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int32_t kvp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVP_H_ */

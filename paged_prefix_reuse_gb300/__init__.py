@@ -1,0 +1,296 @@
+"""paged_prefix_reuse_gb300 -- Python binding of libkvp, the sm_103a library
+for attention over a paged, prefix-sharing KV cache.
+
+This module only marshals arguments: torch tensors become device pointers
+and the current CUDA stream is passed along.  Every step of the path runs
+in libkvp's CUDA kernels; there is no CPU or PyTorch fallback.  If the
+shared library has not been built, importing works but the first call
+raises ``KvpLibraryMissing``.
+
+Functions carry the names of the C entry points declared in
+``include/kvp.h``: ``kvp_slot_mapping``, ``kvp_cache_append``,
+``kvp_block_copy``, ``kvp_prefix_attn``, ``kvp_decode_attn`` and
+``kvp_workspace_size`` (plus the split-count helpers).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "KvpError",
+    "KvpLibraryMissing",
+    "PagedKVPool",
+    "EXPORTED_SYMBOLS",
+    "lib_path",
+    "load_library",
+    "kvp_slot_mapping",
+    "kvp_cache_append",
+    "kvp_block_copy",
+    "kvp_prefix_attn",
+    "kvp_decode_attn",
+    "kvp_workspace_size",
+    "kvp_prefix_num_splits",
+    "kvp_decode_num_splits",
+    "kvp_status_string",
+    "DEVERR",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libkvp.so")
+
+KVP_F16, KVP_BF16 = 0, 1
+_DTYPES = {torch.float16: KVP_F16, torch.bfloat16: KVP_BF16}
+
+# Device error-word bits (KVP_DEVERR_* in kvp.h).
+DEVERR = {"bad_block": 0x1, "bad_slot": 0x2, "bad_pair": 0x4, "bad_len": 0x8, "timeout": 0x10}
+
+# Every extern "C" symbol declared in include/kvp.h.
+EXPORTED_SYMBOLS = (
+    "kvp_slot_mapping",
+    "kvp_cache_append",
+    "kvp_block_copy",
+    "kvp_prefix_attn",
+    "kvp_decode_attn",
+    "kvp_prefix_num_splits",
+    "kvp_decode_num_splits",
+    "kvp_workspace_size",
+    "kvp_status_string",
+    "kvp_version",
+)
+
+
+class KvpError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_status_text(status)} (kvp_status {status})")
+
+
+class KvpLibraryMissing(RuntimeError):
+    pass
+
+
+class _Pool(ctypes.Structure):
+    _fields_ = [
+        ("k_pool", ctypes.c_void_p),
+        ("v_pool", ctypes.c_void_p),
+        ("num_blocks", ctypes.c_int64),
+        ("block_size", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+        ("err_word", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libkvp.so (built by ``paged_prefix_reuse_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise KvpLibraryMissing(
+                f"{_LIB_PATH} is not built; run `python -m paged_prefix_reuse_gb300.build` first"
+            )
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, i32, i64, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+        PP = ctypes.POINTER(_Pool)
+        lib.kvp_slot_mapping.argtypes = [PP, P, P, P, i32, i32, i32, P, P]
+        lib.kvp_cache_append.argtypes = [PP, P, P, P, i32, P]
+        lib.kvp_block_copy.argtypes = [PP, P, i32, P]
+        lib.kvp_prefix_attn.argtypes = [PP, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, i32, P, sz, P]
+        lib.kvp_decode_attn.argtypes = [PP, P, P, P, P, P, i32, i32, i32, i32, f32, i32, P, sz, P]
+        for name in ("kvp_slot_mapping", "kvp_cache_append", "kvp_block_copy", "kvp_prefix_attn", "kvp_decode_attn"):
+            getattr(lib, name).restype = ctypes.c_int
+        lib.kvp_prefix_num_splits.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.kvp_prefix_num_splits.restype = i32
+        lib.kvp_decode_num_splits.argtypes = [i32, i32, i32, i32]
+        lib.kvp_decode_num_splits.restype = i32
+        lib.kvp_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        lib.kvp_workspace_size.restype = sz
+        lib.kvp_status_string.argtypes = [ctypes.c_int]
+        lib.kvp_status_string.restype = ctypes.c_char_p
+        lib.kvp_version.argtypes = []
+        lib.kvp_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def _status_text(status: int) -> str:
+    try:
+        return load_library().kvp_status_string(status).decode()
+    except Exception:  # pragma: no cover
+        return "unknown"
+
+
+def kvp_status_string(status: int) -> str:
+    return load_library().kvp_status_string(status).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise KvpError(status, where)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dev_i32(x, device) -> torch.Tensor:
+    t = torch.as_tensor(x, dtype=torch.int32)
+    return t.to(device, non_blocking=True).contiguous()
+
+
+class PagedKVPool:
+    """A pool of physical KV blocks: k/v tensors [num_blocks, Hkv, block_size, d].
+
+    The tensors are caller-owned device memory; the library keeps no state.
+    ``err_word`` is a device uint32 (int32 tensor of one element) that the
+    kernels OR ``DEVERR`` bits into.
+    """
+
+    def __init__(self, k_pool: torch.Tensor, v_pool: torch.Tensor, err_word: torch.Tensor | None = None):
+        if k_pool.shape != v_pool.shape or k_pool.dtype != v_pool.dtype or k_pool.dim() != 4:
+            raise ValueError("k_pool and v_pool must be [num_blocks, Hkv, block_size, head_dim] of one dtype")
+        if not (k_pool.is_cuda and v_pool.is_cuda and k_pool.is_contiguous() and v_pool.is_contiguous()):
+            raise ValueError("pools must be contiguous CUDA tensors")
+        if k_pool.dtype not in _DTYPES:
+            raise ValueError(f"unsupported dtype {k_pool.dtype}")
+        self.k = k_pool
+        self.v = v_pool
+        if err_word is None:
+            err_word = torch.zeros(1, dtype=torch.int32, device=k_pool.device)
+        self.err_word = err_word
+        nb, hkv, bs, d = k_pool.shape
+        self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim = int(nb), int(hkv), int(bs), int(d)
+        self.dtype = k_pool.dtype
+        self._c = _Pool(
+            k_pool.data_ptr(), v_pool.data_ptr(), nb, bs, hkv, d, _DTYPES[k_pool.dtype], err_word.data_ptr()
+        )
+
+    @classmethod
+    def allocate(cls, num_blocks, num_kv_heads, block_size, head_dim, dtype=torch.bfloat16, device="cuda"):
+        k = torch.empty((num_blocks, num_kv_heads, block_size, head_dim), dtype=dtype, device=device)
+        v = torch.empty_like(k)
+        return cls(k, v)
+
+    @property
+    def c(self):
+        return ctypes.byref(self._c)
+
+    def errors(self) -> int:
+        return int(self.err_word.item()) & 0xFFFFFFFF
+
+    def clear_errors(self) -> None:
+        self.err_word.zero_()
+
+
+def kvp_workspace_size(op: int, rows: int, num_q_heads: int, head_dim: int, num_splits: int) -> int:
+    return int(load_library().kvp_workspace_size(op, rows, num_q_heads, head_dim, num_splits))
+
+
+def kvp_prefix_num_splits(B, num_q_heads, num_kv_heads, head_dim, max_q_len, max_context_len) -> int:
+    return int(load_library().kvp_prefix_num_splits(B, num_q_heads, num_kv_heads, head_dim, max_q_len,
+                                                    max_context_len))
+
+
+def kvp_decode_num_splits(B, num_kv_heads, block_size, max_context_len) -> int:
+    return int(load_library().kvp_decode_num_splits(B, num_kv_heads, block_size, max_context_len))
+
+
+def kvp_slot_mapping(pool: PagedKVPool, cu_seqlens_q: torch.Tensor, context_lens: torch.Tensor,
+                     block_tables: torch.Tensor, total_q: int, out: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+    """Pool slot of every new token (int64 [total_q]); see kvp.h."""
+    lib = load_library()
+    if out is None:
+        out = torch.empty(total_q, dtype=torch.int64, device=pool.k.device)
+    B = int(context_lens.shape[0])
+    _check(lib.kvp_slot_mapping(pool.c, _ptr(cu_seqlens_q), _ptr(context_lens), _ptr(block_tables),
+                                int(block_tables.shape[1]), B, int(total_q), _ptr(out), _stream(stream)),
+           "kvp_slot_mapping")
+    return out
+
+
+def kvp_cache_append(pool: PagedKVPool, k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
+                     stream=None) -> None:
+    """Scatter new K/V [T, Hkv, d] into the pool slots (-1 = skip)."""
+    lib = load_library()
+    T = int(k_new.shape[0]) if k_new.dim() else 0
+    _check(lib.kvp_cache_append(pool.c, _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), T, _stream(stream)),
+           "kvp_cache_append")
+
+
+def kvp_block_copy(pool: PagedKVPool, pairs: torch.Tensor, stream=None) -> None:
+    """Copy-on-write fork: pool[dst] = pool[src] for each (src, dst) row of ``pairs``."""
+    lib = load_library()
+    n = int(pairs.shape[0]) if pairs.numel() else 0
+    _check(lib.kvp_block_copy(pool.c, _ptr(pairs) if n else None, n, _stream(stream)), "kvp_block_copy")
+
+
+def kvp_prefix_attn(pool: PagedKVPool, q: torch.Tensor, cu_seqlens_q: torch.Tensor, context_lens: torch.Tensor,
+                    block_tables: torch.Tensor, max_q_len: int, max_context_len: int, softmax_scale: float,
+                    num_splits: int = 0, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                    workspace: torch.Tensor | None = None, want_lse: bool = True, stream=None):
+    """Causal attention of the packed new tokens q [T, Hq, d] over their
+    sequences' paged K/V.  Returns (out [T, Hq, d], lse [Hq, T] float32 or None)."""
+    lib = load_library()
+    T, Hq, d = (int(x) for x in q.shape)
+    B = int(context_lens.shape[0])
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
+    splits = num_splits or kvp_prefix_num_splits(B, Hq, pool.num_kv_heads, d, max_q_len, max_context_len)
+    need = kvp_workspace_size(0, T, Hq, d, splits)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.kvp_prefix_attn(pool.c, _ptr(q), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q), _ptr(context_lens),
+                               _ptr(block_tables), int(block_tables.shape[1]), B, T, Hq, int(max_q_len),
+                               int(max_context_len), float(softmax_scale), int(splits), _ptr(workspace),
+                               ws_bytes, _stream(stream)),
+           "kvp_prefix_attn")
+    return out, lse
+
+
+def kvp_decode_attn(pool: PagedKVPool, q: torch.Tensor, context_lens: torch.Tensor, block_tables: torch.Tensor,
+                    max_context_len: int, softmax_scale: float, num_splits: int = 0,
+                    out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                    workspace: torch.Tensor | None = None, want_lse: bool = True, stream=None):
+    """One query per sequence q [B, Hq, d] over its paged context.
+    Returns (out [B, Hq, d], lse [Hq, B] float32 or None)."""
+    lib = load_library()
+    B, Hq, d = (int(x) for x in q.shape)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((Hq, B), dtype=torch.float32, device=q.device)
+    splits = num_splits or kvp_decode_num_splits(B, pool.num_kv_heads, pool.block_size, max_context_len)
+    need = kvp_workspace_size(1, B, Hq, d, splits)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.kvp_decode_attn(pool.c, _ptr(q), _ptr(out), _ptr(lse), _ptr(context_lens), _ptr(block_tables),
+                               int(block_tables.shape[1]), B, Hq, int(max_context_len), float(softmax_scale),
+                               int(splits), _ptr(workspace), ws_bytes, _stream(stream)),
+           "kvp_decode_attn")
+    return out, lse

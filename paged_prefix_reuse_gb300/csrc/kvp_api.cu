@@ -1,0 +1,299 @@
+// kvp_api.cu -- the extern "C" entry points of libkvp: host-side argument
+// validation, TMA tensor-map construction for the pools, split-count
+// heuristics, workspace carving, and kernel launches on the caller's stream.
+#include <math.h>
+#include <string.h>
+
+#include "kvp_internal.cuh"
+
+namespace kvp {
+namespace {
+
+constexpr int kNumSMs = 152;  // GB300; used only by the split heuristics
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The pool viewed as a 2-D tensor of rows (block, kv head, slot) x head_dim;
+// one TMA box is one block of one kv head, `chunk_elems` columns wide.
+kvp_status make_pool_map(CUtensorMap* map, void* base, const kvp_pool* pool) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return KVP_ERR_CUDA;
+    const int D = pool->head_dim, CW = chunk_elems(D);
+    const cuuint64_t rows = static_cast<cuuint64_t>(pool->num_blocks) * pool->num_kv_heads * pool->block_size;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), rows};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(CW), static_cast<cuuint32_t>(pool->block_size)};
+    cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType dt =
+        pool->dtype == KVP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapSwizzle swz = CW == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    CUresult r = enc(map, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? KVP_OK : KVP_ERR_CUDA;
+}
+
+kvp_status check_pool(const kvp_pool* pool) {
+    if (!pool || !pool->k_pool || !pool->v_pool) return KVP_ERR_INVALID_ARG;
+    if (!aligned16(pool->k_pool) || !aligned16(pool->v_pool)) return KVP_ERR_INVALID_ARG;
+    if (pool->num_blocks < 1 || pool->num_kv_heads < 1) return KVP_ERR_INVALID_ARG;
+    if (pool->dtype != KVP_F16 && pool->dtype != KVP_BF16) return KVP_ERR_UNSUPPORTED;
+    if (pool->head_dim != 64 && pool->head_dim != 96 && pool->head_dim != 128) return KVP_ERR_UNSUPPORTED;
+    if (pool->block_size != 8 && pool->block_size != 16 && pool->block_size != 32) return KVP_ERR_UNSUPPORTED;
+    // TMA row coordinates are int32.
+    const int64_t rows = pool->num_blocks * pool->num_kv_heads * static_cast<int64_t>(pool->block_size);
+    if (rows <= 0 || rows >= (int64_t(1) << 31)) return KVP_ERR_INVALID_ARG;
+    return KVP_OK;
+}
+
+PoolView view_of(const kvp_pool* pool) {
+    PoolView v;
+    v.num_blocks = pool->num_blocks;
+    v.block_size = pool->block_size;
+    v.num_kv_heads = pool->num_kv_heads;
+    v.head_dim = pool->head_dim;
+    v.dtype = pool->dtype;
+    v.err_word = pool->err_word;
+    return v;
+}
+
+kvp_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVP_OK : KVP_ERR_CUDA; }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int32_t ceil_div(int64_t a, int64_t b) { return static_cast<int32_t>((a + b - 1) / b); }
+
+// Decode split geometry: pages per split (a multiple of the pages in one
+// 32-key stage) and the resulting split count of the longest context.
+void decode_geometry(int32_t block_size, int32_t max_context_len, int32_t num_splits, int32_t* pages_per_split,
+                     int32_t* max_splits) {
+    const int32_t max_pages = ceil_div(max_context_len, block_size);
+    const int32_t stage_pages = 32 / block_size;
+    int32_t pps = ceil_div(max_pages, num_splits < 1 ? 1 : num_splits);
+    pps = ceil_div(pps, stage_pages) * stage_pages;
+    *pages_per_split = pps;
+    *max_splits = ceil_div(max_pages, pps);
+}
+
+}  // namespace
+}  // namespace kvp
+
+using namespace kvp;
+
+extern "C" {
+
+int32_t kvp_version(void) { return 100; }
+
+const char* kvp_status_string(kvp_status status) {
+    switch (status) {
+        case KVP_OK: return "ok";
+        case KVP_ERR_INVALID_ARG: return "invalid argument";
+        case KVP_ERR_UNSUPPORTED: return "unsupported dtype, head_dim or block_size";
+        case KVP_ERR_WORKSPACE: return "workspace missing or too small";
+        case KVP_ERR_CUDA: return "CUDA error";
+        case KVP_ERR_TIMEOUT: return "an in-kernel wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int32_t kvp_prefix_num_splits(int32_t B, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t max_q_len, int32_t max_context_len) {
+    (void)head_dim;
+    if (B <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 || max_q_len <= 0) return 1;
+    const int64_t g = num_q_heads / num_kv_heads;
+    const int64_t q_tiles = (static_cast<int64_t>(max_q_len) * g + 127) / 128;
+    const int64_t ctas = q_tiles * num_kv_heads * B;
+    const int64_t key_tiles = (static_cast<int64_t>(max_context_len) + 127) / 128;
+    const int64_t target = 2 * kNumSMs;
+    if (ctas >= target || key_tiles < 4) return 1;
+    int64_t splits = (target + ctas - 1) / ctas;
+    if (splits > key_tiles / 2) splits = key_tiles / 2;
+    if (splits > 16) splits = 16;
+    return splits < 1 ? 1 : static_cast<int32_t>(splits);
+}
+
+int32_t kvp_decode_num_splits(int32_t B, int32_t num_kv_heads, int32_t block_size, int32_t max_context_len) {
+    if (B <= 0 || num_kv_heads <= 0 || max_context_len <= 0) return 1;
+    (void)block_size;
+    int64_t splits = (static_cast<int64_t>(max_context_len) + 511) / 512;  // about 512 keys per CTA
+    const int64_t pairs = static_cast<int64_t>(B) * num_kv_heads;
+    const int64_t target = 2 * kNumSMs;
+    if (pairs * splits < target) {
+        int64_t want = (target + pairs - 1) / pairs;
+        const int64_t cap = (static_cast<int64_t>(max_context_len) + 127) / 128;  // >= 128 keys per CTA
+        splits = want < cap ? want : cap;
+    }
+    if (splits > 64) splits = 64;
+    return splits < 1 ? 1 : static_cast<int32_t>(splits);
+}
+
+size_t kvp_workspace_size(int32_t op, int32_t rows, int32_t num_q_heads, int32_t head_dim, int32_t num_splits) {
+    (void)op;
+    if (num_splits <= 1 || rows <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+    const size_t r = static_cast<size_t>(rows) * num_q_heads * num_splits;
+    return align256(r * head_dim * sizeof(float)) + align256(r * sizeof(float));
+}
+
+kvp_status kvp_slot_mapping(const kvp_pool* pool, const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                            const int32_t* block_tables, int32_t max_blocks, int32_t B, int32_t total_q,
+                            int64_t* slot_mapping, void* stream) {
+    kvp_status st = check_pool(pool);
+    if (st != KVP_OK) return st;
+    if (B < 0 || total_q < 0 || max_blocks < 0) return KVP_ERR_INVALID_ARG;
+    if (total_q == 0) return KVP_OK;
+    if (B == 0 || max_blocks == 0 || !cu_seqlens_q || !context_lens || !block_tables || !slot_mapping)
+        return KVP_ERR_INVALID_ARG;
+    return from_cuda(launch_slot_mapping(view_of(pool), cu_seqlens_q, context_lens, block_tables, max_blocks, B,
+                                         total_q, slot_mapping, static_cast<cudaStream_t>(stream)));
+}
+
+kvp_status kvp_cache_append(const kvp_pool* pool, const void* k_new, const void* v_new,
+                            const int64_t* slot_mapping, int32_t T, void* stream) {
+    kvp_status st = check_pool(pool);
+    if (st != KVP_OK) return st;
+    if (T < 0) return KVP_ERR_INVALID_ARG;
+    if (T == 0) return KVP_OK;
+    if (!k_new || !v_new || !slot_mapping || !aligned16(k_new) || !aligned16(v_new)) return KVP_ERR_INVALID_ARG;
+    return from_cuda(launch_cache_append(view_of(pool), pool->k_pool, pool->v_pool, k_new, v_new, slot_mapping, T,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+kvp_status kvp_block_copy(const kvp_pool* pool, const int32_t* pairs, int32_t n, void* stream) {
+    kvp_status st = check_pool(pool);
+    if (st != KVP_OK) return st;
+    if (n < 0) return KVP_ERR_INVALID_ARG;
+    if (n == 0) return KVP_OK;
+    if (!pairs) return KVP_ERR_INVALID_ARG;
+    return from_cuda(
+        launch_block_copy(view_of(pool), pool->k_pool, pool->v_pool, pairs, n, static_cast<cudaStream_t>(stream)));
+}
+
+kvp_status kvp_prefix_attn(const kvp_pool* pool, const void* q, void* out, float* lse, const int32_t* cu_seqlens_q,
+                           const int32_t* context_lens, const int32_t* block_tables, int32_t max_blocks, int32_t B,
+                           int32_t total_q, int32_t num_q_heads, int32_t max_q_len, int32_t max_context_len,
+                           float softmax_scale, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+    kvp_status st = check_pool(pool);
+    if (st != KVP_OK) return st;
+    if (B < 0 || total_q < 0 || max_blocks < 0 || num_splits < 0 || max_q_len < 0 || max_context_len < 0)
+        return KVP_ERR_INVALID_ARG;
+    if (B == 0 || total_q == 0) return KVP_OK;
+    if (!q || !out || !cu_seqlens_q || !context_lens || !block_tables || max_blocks == 0) return KVP_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out)) return KVP_ERR_INVALID_ARG;
+    if (num_q_heads < 1 || num_q_heads % pool->num_kv_heads != 0) return KVP_ERR_INVALID_ARG;
+    if (max_q_len < 1 || max_context_len < 1) return KVP_ERR_INVALID_ARG;
+    if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return KVP_ERR_INVALID_ARG;
+    if (pool->num_kv_heads > 65535 || B > 65535) return KVP_ERR_INVALID_ARG;
+    const int32_t g = num_q_heads / pool->num_kv_heads;
+    const int64_t q_tiles = (static_cast<int64_t>(max_q_len) * g + 127) / 128;
+    int32_t splits = num_splits > 0 ? num_splits
+                                    : kvp_prefix_num_splits(B, num_q_heads, pool->num_kv_heads, pool->head_dim,
+                                                            max_q_len, max_context_len);
+    if (q_tiles * splits >= (int64_t(1) << 31)) return KVP_ERR_INVALID_ARG;
+    PrefixParams p;
+    p.pool = view_of(pool);
+    p.q = q;
+    p.out = out;
+    p.lse = lse;
+    p.cu_seqlens_q = cu_seqlens_q;
+    p.context_lens = context_lens;
+    p.block_tables = block_tables;
+    p.max_blocks = max_blocks;
+    p.B = B;
+    p.total_q = total_q;
+    p.num_q_heads = num_q_heads;
+    p.group = g;
+    p.q_tiles = static_cast<int32_t>(q_tiles);
+    p.num_splits = splits;
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.ws_o = nullptr;
+    p.ws_lse = nullptr;
+    if (splits > 1) {
+        const size_t need = kvp_workspace_size(0, total_q, num_q_heads, pool->head_dim, splits);
+        if (!workspace || workspace_bytes < need || !aligned16(workspace)) return KVP_ERR_WORKSPACE;
+        const size_t r = static_cast<size_t>(total_q) * num_q_heads * splits;
+        p.ws_o = static_cast<float*>(workspace);
+        p.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(r * pool->head_dim * 4));
+    }
+    CUtensorMap tk, tv;
+    if ((st = make_pool_map(&tk, pool->k_pool, pool)) != KVP_OK) return st;
+    if ((st = make_pool_map(&tv, pool->v_pool, pool)) != KVP_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_prefix_attn(p, tk, tv, s);
+    if (e != cudaSuccess) return KVP_ERR_CUDA;
+    if (splits > 1)
+        e = launch_merge(p.ws_o, p.ws_lse, total_q * num_q_heads, num_q_heads, pool->head_dim, splits, pool->dtype,
+                         out, lse, total_q, nullptr, pool->block_size, 0, s);
+    return from_cuda(e);
+}
+
+kvp_status kvp_decode_attn(const kvp_pool* pool, const void* q, void* out, float* lse, const int32_t* context_lens,
+                           const int32_t* block_tables, int32_t max_blocks, int32_t B, int32_t num_q_heads,
+                           int32_t max_context_len, float softmax_scale, int32_t num_splits, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+    kvp_status st = check_pool(pool);
+    if (st != KVP_OK) return st;
+    if (B < 0 || max_blocks < 0 || num_splits < 0 || max_context_len < 0) return KVP_ERR_INVALID_ARG;
+    if (B == 0) return KVP_OK;
+    if (!q || !out || !context_lens || !block_tables || max_blocks == 0) return KVP_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out)) return KVP_ERR_INVALID_ARG;
+    if (num_q_heads < 1 || num_q_heads % pool->num_kv_heads != 0) return KVP_ERR_INVALID_ARG;
+    const int32_t g = num_q_heads / pool->num_kv_heads;
+    if (g > 16) return KVP_ERR_UNSUPPORTED;
+    if (max_context_len < 1) return KVP_ERR_INVALID_ARG;
+    if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return KVP_ERR_INVALID_ARG;
+    if (pool->num_kv_heads > 65535 || B > 65535) return KVP_ERR_INVALID_ARG;
+    const int32_t req = num_splits > 0
+                            ? num_splits
+                            : kvp_decode_num_splits(B, pool->num_kv_heads, pool->block_size, max_context_len);
+    DecodeParams p;
+    p.pool = view_of(pool);
+    p.q = q;
+    p.out = out;
+    p.lse = lse;
+    p.context_lens = context_lens;
+    p.block_tables = block_tables;
+    p.max_blocks = max_blocks;
+    p.B = B;
+    p.num_q_heads = num_q_heads;
+    p.group = g;
+    decode_geometry(pool->block_size, max_context_len, req, &p.pages_per_split, &p.max_splits);
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.ws_o = nullptr;
+    p.ws_lse = nullptr;
+    if (p.max_splits > 1) {
+        const size_t need = kvp_workspace_size(1, B, num_q_heads, pool->head_dim, p.max_splits);
+        if (!workspace || workspace_bytes < need || !aligned16(workspace)) return KVP_ERR_WORKSPACE;
+        const size_t r = static_cast<size_t>(B) * num_q_heads * p.max_splits;
+        p.ws_o = static_cast<float*>(workspace);
+        p.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(r * pool->head_dim * 4));
+    }
+    CUtensorMap tk, tv;
+    if ((st = make_pool_map(&tk, pool->k_pool, pool)) != KVP_OK) return st;
+    if ((st = make_pool_map(&tv, pool->v_pool, pool)) != KVP_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_decode_attn(p, tk, tv, s);
+    if (e != cudaSuccess) return KVP_ERR_CUDA;
+    if (p.max_splits > 1)
+        e = launch_merge(p.ws_o, p.ws_lse, B * num_q_heads, num_q_heads, pool->head_dim, p.max_splits, pool->dtype,
+                         out, lse, B, context_lens, pool->block_size, p.pages_per_split, s);
+    return from_cuda(e);
+}
+
+}  // extern "C"

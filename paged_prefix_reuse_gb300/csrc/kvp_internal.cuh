@@ -1,0 +1,298 @@
+// kvp_internal.cuh -- shared pieces of libkvp's sm_103a kernels: inline-PTX
+// wrappers (mbarrier, TMA, tcgen05/TMEM), bounded waits, swizzle addressing,
+// and the launch functions each .cu file provides to the C-ABI layer.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvp.h"
+
+namespace kvp {
+
+// ---------------------------------------------------------------------------
+// Launch parameters shared between host and device.
+// ---------------------------------------------------------------------------
+struct PoolView {
+    int64_t num_blocks;
+    int32_t block_size, num_kv_heads, head_dim, dtype;
+    uint32_t* err_word;
+};
+
+struct PrefixParams {
+    PoolView pool;
+    const void* q;
+    void* out;
+    float* lse;
+    const int32_t* cu_seqlens_q;
+    const int32_t* context_lens;
+    const int32_t* block_tables;
+    int32_t max_blocks, B, total_q, num_q_heads, group;  // group = Hq / Hkv
+    int32_t q_tiles;                                    // query tiles per (sequence, kv head)
+    int32_t num_splits;
+    float scale_log2;  // softmax_scale * log2(e)
+    float* ws_o;       // [total_q * Hq][num_splits][head_dim] fp32 (splits > 1)
+    float* ws_lse;     // [total_q * Hq][num_splits] fp32, log2 domain
+};
+
+struct DecodeParams {
+    PoolView pool;
+    const void* q;
+    void* out;
+    float* lse;
+    const int32_t* context_lens;
+    const int32_t* block_tables;
+    int32_t max_blocks, B, num_q_heads, group;
+    int32_t pages_per_split;  // multiple of the pages in one stage
+    int32_t max_splits;
+    float scale_log2;
+    float* ws_o;    // [B * Hq][max_splits][head_dim]
+    float* ws_lse;  // [B * Hq][max_splits], log2 domain
+};
+
+// Host-side launchers (defined in the kernel .cu files).
+cudaError_t launch_slot_mapping(const PoolView& pool, const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                                const int32_t* block_tables, int32_t max_blocks, int32_t B, int32_t total_q,
+                                int64_t* slot_mapping, cudaStream_t stream);
+cudaError_t launch_cache_append(const PoolView& pool, void* k_pool, void* v_pool, const void* k_new,
+                                const void* v_new, const int64_t* slot_mapping, int32_t T, cudaStream_t stream);
+cudaError_t launch_block_copy(const PoolView& pool, void* k_pool, void* v_pool, const int32_t* pairs, int32_t n,
+                              cudaStream_t stream);
+cudaError_t launch_prefix_attn(const PrefixParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                               cudaStream_t stream);
+cudaError_t launch_decode_attn(const DecodeParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                               cudaStream_t stream);
+// Merge of split partials: rows = total_q*Hq (prefix) or B*Hq (decode).
+// For decode, splits_of_row derives each row's split count from context_lens.
+cudaError_t launch_merge(const float* ws_o, const float* ws_lse, int32_t rows, int32_t num_q_heads,
+                         int32_t head_dim, int32_t max_splits, int32_t dtype, void* out, float* lse,
+                         int32_t lse_stride, const int32_t* context_lens, int32_t block_size,
+                         int32_t pages_per_split, cudaStream_t stream);
+
+// Swizzle chunk width (elements of one TMA box row) for a head dimension:
+// 64 elements (128-byte rows, 128B swizzle) when head_dim is a multiple of
+// 64, else 32 elements (64-byte rows, 64B swizzle).
+__host__ __device__ constexpr int chunk_elems(int head_dim) { return (head_dim % 64 == 0) ? 64 : 32; }
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+#if defined(__CUDACC__)
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void report(uint32_t* err_word, uint32_t bits) {
+    if (err_word) atomicOr(err_word, bits);
+}
+
+// ---- mbarrier ----
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Give up on any single wait after this long; a healthy wait lasts microseconds.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// Bounded wait for the phase with the given parity.  Returns false when the
+// wait gave up (limit reached, or another thread of the CTA already gave up
+// and raised *abort); the caller must then wind down.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint32_t* err_word) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(a, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                *abort = 1;
+                report(err_word, KVP_DEVERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// ---- proxy fences ----
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---- TMA: 2-D tiled load into shared memory, completion on an mbarrier ----
+__device__ __forceinline__ void tma_load_2d(void* dst_smem, const CUtensorMap* map, int32_t x, int32_t y,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(smem_u32(dst_smem)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---- swizzled shared-memory addressing --------------------------------------
+// Byte offset of the 16-byte chunk `c16` of row `row` in a tile whose rows are
+// `row_bytes` (128 or 64) long, written by TMA with the matching swizzle mode
+// (128B: chunk ^= row % 8; 64B: chunk ^= (row / 2) % 4).  The tile must start
+// on a 1024-byte boundary.
+__device__ __forceinline__ uint32_t swz_offset(uint32_t row, uint32_t c16, uint32_t row_bytes) {
+    if (row_bytes == 128) return row * 128u + ((c16 ^ (row & 7u)) << 4);
+    return row * 64u + ((c16 ^ ((row >> 1) & 3u)) << 4);
+}
+
+// ---- tcgen05 / TMEM ---------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (fp16/bf16 in, fp32 accumulate).
+__device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on an mbarrier once all previously issued tcgen05 ops of this thread complete.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading
+// and stride byte offsets (>> 4), version 1 at bits 46-47, swizzle mode at
+// bits 61-63 (0 none, 2 = 128B, 4 = 64B, 6 = 32B).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swz) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(swz & 7u) << 61;
+    return d;
+}
+
+// Instruction descriptor for kind::f16: fp32 accumulator, A/B fp16 or bf16,
+// A K-major, B K-major (b_mn_major = 0) or MN-major (1), shape M x N.
+__host__ __device__ constexpr uint32_t instr_desc_f16(bool bf16, int M, int N, bool b_mn_major) {
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// 32 lanes x 32 bits, 32 consecutive columns: thread i of the warp receives
+// columns [col, col+32) of TMEM lane (warp's lane quarter base + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ---- small numeric helpers ----
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <bool kBF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    if constexpr (kBF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+
+template <bool kBF16>
+__device__ __forceinline__ float2 unpack2(uint32_t u) {
+    if constexpr (kBF16) {
+        __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&u);
+        return __bfloat1622float2(v);
+    } else {
+        __half2 v = *reinterpret_cast<__half2*>(&u);
+        return __half22float2(v);
+    }
+}
+
+#endif  // __CUDACC__
+
+}  // namespace kvp

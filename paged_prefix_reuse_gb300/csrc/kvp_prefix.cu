@@ -1,0 +1,511 @@
+// kvp_prefix.cu -- causal attention of a chunk of new tokens over a paged
+// KV cache (cached prefix + the chunk's own K/V), on the 5th-generation
+// tensor cores (tcgen05, accumulators in tensor memory).
+//
+// What it computes (kvboost 0.6.0, "How it works" step 5: the live suffix
+// attends to the cached prefix in one forward; "Flash Attention (CUDA)":
+// tiled online softmax with causal masking that skips future K/V tiles,
+// fp16/bf16, head_dim 64/96/128, any length): for every new token t of
+// sequence s and query head h,
+//     out[t][h] = softmax_j(scale * q[t][h] . K[j]) . V[j],  j <= P_s + i_t,
+// K/V read through the block table (kvboost "CPU paged attention").
+//
+// Design for sm_103a (one CTA per 128-row query tile x kv head x sequence
+// [x key-range split]; 192 threads; about 224 KB of shared memory at d=128):
+//  * rows of a query tile are (token, query head of the GQA group) pairs, so
+//    all heads that share a kv head consume each loaded K/V tile once;
+//  * warp 4 gathers K and V tiles of 128 keys page by page with 2-D TMA
+//    loads (one box = one physical block of one kv head, found through the
+//    block table), swizzled to match the UMMA shared-memory descriptors,
+//    double-buffered;
+//  * warp 5 issues tcgen05.mma: S = Q K^T (M=128, N=128) into one of two
+//    TMEM S buffers, and O += P V (M=128, N=d) into a TMEM accumulator;
+//    completion is signalled with tcgen05.commit on mbarriers;
+//  * warps 0-3 (thread i owns query row i = TMEM lane i) read S from TMEM,
+//    run the online softmax in fp32 (log2 domain), write P as fp16/bf16 into
+//    a swizzled shared-memory tile (double-buffered), and rescale O in TMEM
+//    only when a row maximum grew by more than 2^8 (exact: the final
+//    normalisation uses the same reference maximum);
+//  * key tiles past the last query's position are never loaded (causal
+//    skip); the diagonal tiles are masked per row;
+//  * with num_splits > 1, each CTA handles a contiguous share of the key
+//    tiles and writes a normalised partial (O, log2 lse) for merge_kernel.
+#include "kvp_internal.cuh"
+
+namespace kvp {
+namespace {
+
+constexpr int kThreads = 192;  // warps 0-3 softmax, warp 4 TMA producer, warp 5 MMA issuer
+constexpr int kBM = 128;       // query rows per tile (TMEM lanes)
+constexpr int kBN = 128;       // keys per tile
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSCol0 = 0, kSCol1 = 128, kOCol = 256;
+
+template <int D>
+struct PrefixCfg {
+    static constexpr int CW = chunk_elems(D);
+    static constexpr int ROWB = CW * 2;
+    static constexpr int NCH = D / CW;
+    static constexpr uint32_t SWZ = ROWB == 128 ? 2u : 4u;  // descriptor swizzle code: 128B or 64B
+    static constexpr int CHUNK_BYTES = kBM * ROWB;          // one chunk column of a 128-row tile
+    static constexpr int TILE_BYTES = kBM * D * 2;
+    static constexpr int P_BYTES = kBM * kBN * 2;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + TILE_BYTES;
+    static constexpr int OFF_V = OFF_K + 2 * TILE_BYTES;
+    static constexpr int OFF_P = OFF_V + 2 * TILE_BYTES;
+    static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+    static constexpr int NBARS = 17;
+    static constexpr int SMEM_BYTES = OFF_BAR + NBARS * 8 + 16 + 1024;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+    const uint32_t a = smem_u32(p);
+    return p + (((a + 1023u) & ~1023u) - a);
+}
+
+// tcgen05.ld of 32 columns followed by its wait, in one statement so that no
+// use of the registers can be scheduled before the data has arrived.
+__device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld16_sync(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+template <bool kBF16, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefix_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                  const PrefixParams p) {
+    using C = PrefixCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* q_full = bars + 0;
+    uint64_t* k_full = bars + 1;
+    uint64_t* k_empty = bars + 3;
+    uint64_t* v_full = bars + 5;
+    uint64_t* v_empty = bars + 7;
+    uint64_t* s_full = bars + 9;
+    uint64_t* s_free = bars + 11;
+    uint64_t* p_full = bars + 13;
+    uint64_t* o_done = bars + 15;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int split = blockIdx.x % p.num_splits;
+    const int qt = p.q_tiles - 1 - static_cast<int>(blockIdx.x) / p.num_splits;  // heavy tiles first
+    const int h = blockIdx.y, s = blockIdx.z;
+    const int g = p.group, BS = p.pool.block_size, Hkv = p.pool.num_kv_heads;
+    uint32_t* err = p.pool.err_word;
+
+    const int cu0 = __ldg(p.cu_seqlens_q + s);
+    const int N = __ldg(p.cu_seqlens_q + s + 1) - cu0;
+    const int rows_total = N * g;
+    const int r0 = qt * kBM;
+    if (r0 >= rows_total) return;
+    const int L = __ldg(p.context_lens + s);
+    const int P = L - N;
+    const int npages = (L + BS - 1) / BS;
+    if (P < 0 || npages > p.max_blocks) {
+        if (tid == 0 && split == 0) report(err, KVP_DEVERR_BAD_LEN);
+        return;
+    }
+    const int r_last = min(rows_total, r0 + kBM) - 1;
+    const int qpos_max = P + r_last / g;
+    const int n_tiles = qpos_max / kBN + 1;
+    const int per = (n_tiles + p.num_splits - 1) / p.num_splits;
+    const int j_begin = min(n_tiles, split * per);
+    const int n_local = min(n_tiles, j_begin + per) - j_begin;
+
+    if (n_local <= 0) {
+        // This split's key range is empty for the whole tile: an empty partial.
+        if (tid < kBM && r0 + tid < rows_total) {
+            const int rg = r0 + tid;
+            const int64_t wrow = static_cast<int64_t>(cu0 + rg / g) * p.num_q_heads + h * g + rg % g;
+            p.ws_lse[wrow * p.num_splits + split] = -INFINITY;
+            for (int c = 0; c < D; ++c) p.ws_o[(wrow * p.num_splits + split) * D + c] = 0.f;
+        }
+        return;
+    }
+
+    if (tid == 0) {
+        mbar_init(q_full, kBM);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_free[i], 4);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&o_done[i], 1);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < 4) {
+        // =========================== softmax warps ===========================
+        const int row = tid;
+        const int rg = r0 + row;
+        const bool valid = rg < rows_total;
+        const int token = valid ? rg / g : 0;
+        const int head = h * g + (valid ? rg % g : 0);
+        const int qpos = valid ? P + token : L - 1;
+
+        {  // Q tile -> swizzled shared memory (K-major A operand)
+            constexpr int V16 = D / 8;
+            const uint4* q4 = static_cast<const uint4*>(p.q);
+            for (int e = tid; e < kBM * V16; e += kBM) {
+                const int rr = e / V16, c16 = e - (e / V16) * V16;
+                const int rgl = r0 + rr;
+                uint4 val = make_uint4(0, 0, 0, 0);
+                if (rgl < rows_total) {
+                    const int64_t qrow = static_cast<int64_t>(cu0 + rgl / g) * p.num_q_heads + h * g + rgl % g;
+                    val = __ldg(q4 + qrow * V16 + c16);
+                }
+                const int ch = c16 / (C::CW / 8), ci = c16 - ch * (C::CW / 8);
+                *reinterpret_cast<uint4*>(smem + C::OFF_Q + ch * C::CHUNK_BYTES + swz_offset(rr, ci, C::ROWB)) = val;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(q_full);
+        }
+
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const float sl2 = p.scale_log2;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int jj = 0; jj < n_local; ++jj) {
+            const int j = j_begin + jj;
+            const int b = jj & 1;
+            if (!mbar_wait(&s_full[b], (jj >> 1) & 1, abort_flag, err)) { ok = false; break; }
+            tc_fence_after();
+            float x[kBN];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t r[32];
+                tmem_ld32_sync(lane_base + (b ? kSCol1 : kSCol0) + 32 * q, r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[32 * q + i] = __uint_as_float(r[i]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[b]);
+
+            const int lim = qpos - j * kBN;  // last visible column of this tile
+            if (lim < kBN - 1) {
+#pragma unroll
+                for (int c = 0; c < kBN; ++c)
+                    if (c > lim) x[c] = -INFINITY;
+            }
+            float mx = x[0];
+#pragma unroll
+            for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, x[c]);
+            const float m_new = fmaxf(m, mx * sl2);
+            const bool need = m_new > m + 8.0f;
+            float alpha = 1.f;
+            if (need) {
+                alpha = fast_exp2(m - m_new);
+                m = m_new;
+                l *= alpha;
+            }
+            const float mref = (m == -INFINITY) ? 0.f : m;
+            float ls = 0.f;
+#pragma unroll
+            for (int c = 0; c < kBN; ++c) {
+                x[c] = fast_exp2(fmaf(x[c], sl2, -mref));
+                ls += x[c];
+            }
+            l += ls;
+
+            if (jj > 0 && __any_sync(0xffffffffu, need)) {
+                // O holds PV_0 .. PV_{jj-1} at the old reference maximum: rescale it.
+                if (!mbar_wait(&o_done[(jj - 1) & 1], ((jj - 1) >> 1) & 1, abort_flag, err)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int cb = 0; cb < D / 16; ++cb) {
+                    uint32_t r[16];
+                    tmem_ld16_sync(lane_base + kOCol + 16 * cb, r);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                    tmem_st16(lane_base + kOCol + 16 * cb, r);
+                }
+                tmem_wait_st();
+            }
+            if (jj >= 2) {  // P buffer b was last read by PV_{jj-2}
+                if (!mbar_wait(&o_done[b], ((jj - 2) >> 1) & 1, abort_flag, err)) { ok = false; break; }
+            }
+            uint8_t* pb = smem + C::OFF_P + b * C::P_BYTES;
+#pragma unroll
+            for (int c16 = 0; c16 < kBN / 8; ++c16) {
+                uint4 v;
+                v.x = pack2<kBF16>(x[8 * c16 + 0], x[8 * c16 + 1]);
+                v.y = pack2<kBF16>(x[8 * c16 + 2], x[8 * c16 + 3]);
+                v.z = pack2<kBF16>(x[8 * c16 + 4], x[8 * c16 + 5]);
+                v.w = pack2<kBF16>(x[8 * c16 + 6], x[8 * c16 + 7]);
+                *reinterpret_cast<uint4*>(pb + (c16 >> 3) * (kBM * 128) + swz_offset(row, c16 & 7, 128)) = v;
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[b]);
+        }
+
+        // ------------------------------ epilogue ------------------------------
+        if (ok) {
+            const int jl = n_local - 1;
+            ok = mbar_wait(&o_done[jl & 1], (jl >> 1) & 1, abort_flag, err);
+        }
+        if (ok) {
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float lse2 = l > 0.f ? m + __log2f(l) : -INFINITY;
+            const int64_t orow = static_cast<int64_t>(cu0 + token) * p.num_q_heads + head;
+            if (p.num_splits == 1) {
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + orow * D * 2);
+#pragma unroll
+                for (int cb = 0; cb < D / 16; ++cb) {
+                    uint32_t r[16];
+                    tmem_ld16_sync(lane_base + kOCol + 16 * cb, r);
+                    uint4 a, bq;
+                    a.x = pack2<kBF16>(__uint_as_float(r[0]) * inv, __uint_as_float(r[1]) * inv);
+                    a.y = pack2<kBF16>(__uint_as_float(r[2]) * inv, __uint_as_float(r[3]) * inv);
+                    a.z = pack2<kBF16>(__uint_as_float(r[4]) * inv, __uint_as_float(r[5]) * inv);
+                    a.w = pack2<kBF16>(__uint_as_float(r[6]) * inv, __uint_as_float(r[7]) * inv);
+                    bq.x = pack2<kBF16>(__uint_as_float(r[8]) * inv, __uint_as_float(r[9]) * inv);
+                    bq.y = pack2<kBF16>(__uint_as_float(r[10]) * inv, __uint_as_float(r[11]) * inv);
+                    bq.z = pack2<kBF16>(__uint_as_float(r[12]) * inv, __uint_as_float(r[13]) * inv);
+                    bq.w = pack2<kBF16>(__uint_as_float(r[14]) * inv, __uint_as_float(r[15]) * inv);
+                    if (valid) {
+                        dst[2 * cb] = a;
+                        dst[2 * cb + 1] = bq;
+                    }
+                }
+                if (valid && p.lse)
+                    p.lse[static_cast<int64_t>(head) * p.total_q + cu0 + token] = lse2 * 0.69314718055994531f;
+            } else {
+                float* dst = p.ws_o + (orow * p.num_splits + split) * D;
+#pragma unroll
+                for (int cb = 0; cb < D / 16; ++cb) {
+                    uint32_t r[16];
+                    tmem_ld16_sync(lane_base + kOCol + 16 * cb, r);
+                    if (valid) {
+#pragma unroll
+                        for (int i = 0; i < 16; i += 4)
+                            *reinterpret_cast<float4*>(dst + 16 * cb + i) =
+                                make_float4(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv,
+                                            __uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv);
+                    }
+                }
+                if (valid) p.ws_lse[orow * p.num_splits + split] = lse2;
+            }
+        }
+    } else if (warp == 4) {
+        // ========================= TMA producer warp =========================
+        if (lane == 0) {
+            prefetch_tmap(&tmap_k);
+            prefetch_tmap(&tmap_v);
+        }
+        const int pages_per_tile = kBN / BS;
+        int issued = 0;
+        for (int jj = 0; jj < n_local; ++jj) {
+            const int j = j_begin + jj;
+            const int b = jj & 1;
+            int my_blk = 0;
+            if (lane < pages_per_tile) {
+                const int pg = min(j * pages_per_tile + lane, npages - 1);
+                int blk = __ldg(p.block_tables + static_cast<int64_t>(s) * p.max_blocks + pg);
+                if (blk < 0 || blk >= p.pool.num_blocks) {
+                    report(err, KVP_DEVERR_BAD_BLOCK);
+                    blk = 0;
+                }
+                my_blk = blk;
+            }
+            int ok = 1;
+            if (lane == 0 && jj >= 2) ok = mbar_wait(&k_empty[b], ((jj - 2) >> 1) & 1, abort_flag, err);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            if (lane == 0) mbar_expect_tx(&k_full[b], C::TILE_BYTES);
+            uint8_t* kt = smem + C::OFF_K + b * C::TILE_BYTES;
+            for (int q = 0; q < pages_per_tile; ++q) {
+                const int blk = __shfl_sync(0xffffffffu, my_blk, q);
+                if (lane == 0) {
+                    const int32_t y = (blk * Hkv + h) * BS;
+#pragma unroll
+                    for (int c = 0; c < C::NCH; ++c)
+                        tma_load_2d(kt + c * C::CHUNK_BYTES + q * BS * C::ROWB, &tmap_k, c * C::CW, y, &k_full[b]);
+                }
+            }
+            if (lane == 0 && jj >= 2) ok = mbar_wait(&v_empty[b], ((jj - 2) >> 1) & 1, abort_flag, err);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                issued = -(jj + 1);  // K of tile jj issued, V not
+                break;
+            }
+            if (lane == 0) mbar_expect_tx(&v_full[b], C::TILE_BYTES);
+            uint8_t* vt = smem + C::OFF_V + b * C::TILE_BYTES;
+            for (int q = 0; q < pages_per_tile; ++q) {
+                const int blk = __shfl_sync(0xffffffffu, my_blk, q);
+                if (lane == 0) {
+                    const int32_t y = (blk * Hkv + h) * BS;
+#pragma unroll
+                    for (int c = 0; c < C::NCH; ++c)
+                        tma_load_2d(vt + c * C::CHUNK_BYTES + q * BS * C::ROWB, &tmap_v, c * C::CW, y, &v_full[b]);
+                }
+            }
+            issued = jj + 1;
+        }
+        // Do not leave while copies may still land in shared memory.
+        if (lane == 0) {
+            volatile int no_abort = 0;
+            const int nk = issued < 0 ? -issued : issued;
+            const int nv = issued < 0 ? -issued - 1 : issued;
+            for (int i = max(0, nk - 2); i < nk; ++i) mbar_wait(&k_full[i & 1], (i >> 1) & 1, &no_abort, err);
+            for (int i = max(0, nv - 2); i < nv; ++i) mbar_wait(&v_full[i & 1], (i >> 1) & 1, &no_abort, err);
+        }
+    } else {
+        // ========================= MMA issuer warp ==========================
+        constexpr uint32_t idesc_s = instr_desc_f16(kBF16, kBM, kBN, false);
+        constexpr uint32_t idesc_o = instr_desc_f16(kBF16, kBM, D, true);
+        const uint32_t q_base = smem_u32(smem + C::OFF_Q);
+        uint64_t* last_bar = nullptr;
+        uint32_t last_par = 0;
+        bool ok = mbar_wait(q_full, 0, abort_flag, err);
+
+        auto issue_pv = [&](int i) -> bool {
+            const int b = i & 1;
+            if (!mbar_wait(&p_full[b], (i >> 1) & 1, abort_flag, err)) return false;
+            if (!mbar_wait(&v_full[b], (i >> 1) & 1, abort_flag, err)) return false;
+            uint8_t* vt = smem + C::OFF_V + b * C::TILE_BYTES;
+            const int nvalid = L - (j_begin + i) * kBN;
+            if (nvalid < kBN) {
+                // Rows past the context may hold any bytes (even NaN); P is 0
+                // there, but 0 * NaN is NaN, so clear those V rows.
+                const int first = max(nvalid, 0);
+                const int per_row = C::ROWB / 16;
+                const int nvec = (kBN - first) * per_row * C::NCH;
+                for (int e = lane; e < nvec; e += 32) {
+                    const int c = e / ((kBN - first) * per_row);
+                    const int rem = e - c * (kBN - first) * per_row;
+                    *reinterpret_cast<uint4*>(vt + c * C::CHUNK_BYTES + (first + rem / per_row) * C::ROWB +
+                                              (rem % per_row) * 16) = make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t p_base = smem_u32(smem + C::OFF_P + b * C::P_BYTES);
+                const uint32_t v_base = smem_u32(vt);
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    const uint64_t ad = smem_desc(p_base + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024, 2);
+                    const uint64_t bd = smem_desc(v_base + kk * 16 * C::ROWB, C::CHUNK_BYTES, 8 * C::ROWB, C::SWZ);
+                    tc_mma_ss(tmem + kOCol, ad, bd, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(&o_done[b]);
+                tc_commit(&v_empty[b]);
+            }
+            __syncwarp();
+            last_bar = &o_done[b];
+            last_par = (i >> 1) & 1;
+            return true;
+        };
+
+        for (int jj = 0; ok && jj < n_local; ++jj) {
+            const int b = jj & 1;
+            if (!mbar_wait(&k_full[b], (jj >> 1) & 1, abort_flag, err)) { ok = false; break; }
+            if (jj >= 2 && !mbar_wait(&s_free[b], ((jj - 2) >> 1) & 1, abort_flag, err)) { ok = false; break; }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t k_base = smem_u32(smem + C::OFF_K + b * C::TILE_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk * 16) / C::CW) * C::CHUNK_BYTES + ((kk * 16) % C::CW) * 2;
+                    const uint64_t ad = smem_desc(q_base + off, 16, 8 * C::ROWB, C::SWZ);
+                    const uint64_t bd = smem_desc(k_base + off, 16, 8 * C::ROWB, C::SWZ);
+                    tc_mma_ss(tmem + (b ? kSCol1 : kSCol0), ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(&s_full[b]);
+                tc_commit(&k_empty[b]);
+            }
+            __syncwarp();
+            last_bar = &s_full[b];
+            last_par = (jj >> 1) & 1;
+            if (jj >= 1 && !issue_pv(jj - 1)) { ok = false; break; }
+        }
+        if (ok) issue_pv(n_local - 1);
+        // Let every issued MMA finish before tensor memory is released.
+        if (lane == 0 && last_bar) {
+            volatile int no_abort = 0;
+            mbar_wait(last_bar, last_par, &no_abort, err);
+        }
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <bool kBF16, int D>
+cudaError_t launch_prefix_t(const PrefixParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                            cudaStream_t stream) {
+    using C = PrefixCfg<D>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(prefix_kernel<kBF16, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    dim3 grid(p.q_tiles * p.num_splits, p.pool.num_kv_heads, p.B);
+    prefix_kernel<kBF16, D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(tk, tv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefix_attn(const PrefixParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                               cudaStream_t stream) {
+    const bool bf = p.pool.dtype == KVP_BF16;
+    switch (p.pool.head_dim) {
+        case 64: return bf ? launch_prefix_t<true, 64>(p, tk, tv, stream) : launch_prefix_t<false, 64>(p, tk, tv, stream);
+        case 96: return bf ? launch_prefix_t<true, 96>(p, tk, tv, stream) : launch_prefix_t<false, 96>(p, tk, tv, stream);
+        case 128: return bf ? launch_prefix_t<true, 128>(p, tk, tv, stream) : launch_prefix_t<false, 128>(p, tk, tv, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace kvp

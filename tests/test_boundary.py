@@ -1,0 +1,153 @@
+"""The C-ABI boundary without a GPU: the library loads, exports every symbol
+declared in include/kvp.h, and rejects host-checkable bad arguments with the
+documented status before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_prefix_reuse_gb300 as kvp
+from paged_prefix_reuse_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+KVP_OK, KVP_ERR_INVALID_ARG, KVP_ERR_UNSUPPORTED, KVP_ERR_WORKSPACE = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build_library()
+    return kvp.load_library()
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "kvp.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]*?\b(kvp_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declarations_match_binding_list():
+    assert declared_symbols() == sorted(kvp.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert lib.kvp_version() >= 100
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert kvp.kvp_status_string(code)
+    assert kvp.kvp_status_string(99) == "unknown status"
+
+
+def _pool(**kw):
+    fields = dict(k_pool=0x10000, v_pool=0x20000, num_blocks=8, block_size=16, num_kv_heads=2, head_dim=64,
+                  dtype=0, err_word=None)
+    fields.update(kw)
+    return kvp._Pool(**fields)
+
+
+def _prefix(lib, pool, **kw):
+    a = dict(q=0x30000, out=0x40000, lse=None, cu=0x50000, ctx=0x60000, bt=0x70000, max_blocks=4, B=1, total_q=16,
+             Hq=2, max_q=16, max_ctx=48, scale=0.125, splits=1, ws=None, ws_bytes=0)
+    a.update(kw)
+    return lib.kvp_prefix_attn(ctypes.byref(pool), a["q"], a["out"], a["lse"], a["cu"], a["ctx"], a["bt"],
+                               a["max_blocks"], a["B"], a["total_q"], a["Hq"], a["max_q"], a["max_ctx"],
+                               a["scale"], a["splits"], a["ws"], a["ws_bytes"], None)
+
+
+def _decode(lib, pool, **kw):
+    a = dict(q=0x30000, out=0x40000, lse=None, ctx=0x60000, bt=0x70000, max_blocks=4, B=1, Hq=2, max_ctx=48,
+             scale=0.125, splits=1, ws=None, ws_bytes=0)
+    a.update(kw)
+    return lib.kvp_decode_attn(ctypes.byref(pool), a["q"], a["out"], a["lse"], a["ctx"], a["bt"], a["max_blocks"],
+                               a["B"], a["Hq"], a["max_ctx"], a["scale"], a["splits"], a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize(
+    "pool_kw,status",
+    [
+        (dict(head_dim=80), KVP_ERR_UNSUPPORTED),
+        (dict(head_dim=256), KVP_ERR_UNSUPPORTED),
+        (dict(block_size=12), KVP_ERR_UNSUPPORTED),
+        (dict(block_size=64), KVP_ERR_UNSUPPORTED),
+        (dict(dtype=2), KVP_ERR_UNSUPPORTED),
+        (dict(k_pool=None), KVP_ERR_INVALID_ARG),
+        (dict(v_pool=0x20008), KVP_ERR_INVALID_ARG),  # not 16-byte aligned
+        (dict(num_blocks=0), KVP_ERR_INVALID_ARG),
+        (dict(num_kv_heads=0), KVP_ERR_INVALID_ARG),
+        (dict(num_blocks=1 << 40), KVP_ERR_INVALID_ARG),  # TMA row index overflow
+    ],
+)
+def test_pool_validation(lib, pool_kw, status):
+    pool = _pool(**pool_kw)
+    assert _prefix(lib, pool) == status
+    assert _decode(lib, pool) == status
+    assert lib.kvp_cache_append(ctypes.byref(pool), 0x30000, 0x40000, 0x50000, 4, None) == status
+    assert lib.kvp_block_copy(ctypes.byref(pool), 0x30000, 1, None) == status
+    assert lib.kvp_slot_mapping(ctypes.byref(pool), 0x30000, 0x40000, 0x50000, 4, 1, 4, 0x60000, None) == status
+
+
+@pytest.mark.parametrize(
+    "kw,status",
+    [
+        (dict(Hq=3), KVP_ERR_INVALID_ARG),  # Hq % Hkv != 0
+        (dict(q=None), KVP_ERR_INVALID_ARG),
+        (dict(out=0x40004), KVP_ERR_INVALID_ARG),
+        (dict(total_q=-1), KVP_ERR_INVALID_ARG),
+        (dict(scale=0.0), KVP_ERR_INVALID_ARG),
+        (dict(scale=float("nan")), KVP_ERR_INVALID_ARG),
+        (dict(max_q=0), KVP_ERR_INVALID_ARG),
+        (dict(max_blocks=0), KVP_ERR_INVALID_ARG),
+        (dict(splits=2), KVP_ERR_WORKSPACE),  # split partials need a workspace
+        (dict(splits=2, ws=0x80000, ws_bytes=16), KVP_ERR_WORKSPACE),
+        (dict(B=0), KVP_OK),  # empty batch: no-op
+        (dict(total_q=0), KVP_OK),
+    ],
+)
+def test_prefix_argument_validation(lib, kw, status):
+    assert _prefix(lib, _pool(), **kw) == status
+
+
+@pytest.mark.parametrize(
+    "kw,status",
+    [
+        (dict(Hq=3), KVP_ERR_INVALID_ARG),
+        (dict(Hq=34), KVP_ERR_UNSUPPORTED),  # group of 17 query heads per kv head
+        (dict(ctx=None), KVP_ERR_INVALID_ARG),
+        (dict(scale=-1.0), KVP_ERR_INVALID_ARG),
+        (dict(max_ctx=0), KVP_ERR_INVALID_ARG),
+        (dict(splits=3, max_ctx=48), KVP_ERR_WORKSPACE),
+        (dict(B=0), KVP_OK),
+    ],
+)
+def test_decode_argument_validation(lib, kw, status):
+    assert _decode(lib, _pool(), **kw) == status
+
+
+def test_append_copy_slot_validation(lib):
+    pool = _pool()
+    P = ctypes.byref(pool)
+    assert lib.kvp_cache_append(P, 0x30000, 0x40000, 0x50000, 0, None) == KVP_OK
+    assert lib.kvp_cache_append(P, 0x30000, 0x40000, 0x50000, -1, None) == KVP_ERR_INVALID_ARG
+    assert lib.kvp_cache_append(P, 0x30008, 0x40000, 0x50000, 4, None) == KVP_ERR_INVALID_ARG
+    assert lib.kvp_cache_append(P, 0x30000, 0x40000, None, 4, None) == KVP_ERR_INVALID_ARG
+    assert lib.kvp_block_copy(P, 0x30000, 0, None) == KVP_OK
+    assert lib.kvp_block_copy(P, None, 2, None) == KVP_ERR_INVALID_ARG
+    assert lib.kvp_block_copy(P, 0x30000, -2, None) == KVP_ERR_INVALID_ARG
+    assert lib.kvp_slot_mapping(P, 0x30000, 0x40000, 0x50000, 4, 1, 0, 0x60000, None) == KVP_OK
+    assert lib.kvp_slot_mapping(P, None, 0x40000, 0x50000, 4, 1, 4, 0x60000, None) == KVP_ERR_INVALID_ARG
+
+
+def test_workspace_and_split_helpers(lib):
+    assert kvp.kvp_workspace_size(0, 100, 8, 128, 1) == 0
+    ws = kvp.kvp_workspace_size(0, 100, 8, 128, 3)
+    assert ws >= 100 * 8 * 3 * (128 + 1) * 4 and ws % 256 == 0
+    # Large problems need no split; tiny ones are spread over the SMs.
+    assert kvp.kvp_prefix_num_splits(4, 64, 8, 128, 2048, 34816) == 1
+    assert kvp.kvp_prefix_num_splits(1, 2, 2, 64, 16, 48) == 1
+    assert kvp.kvp_prefix_num_splits(8, 16, 2, 128, 256, 1280) >= 2
+    assert kvp.kvp_decode_num_splits(64, 8, 16, 8193) == 17
+    assert kvp.kvp_decode_num_splits(1, 1, 16, 300) == 3
