@@ -134,7 +134,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "20",
                  "-i", str(self.idx)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -165,7 +165,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window": "untimed pre-roll steps + the timed steps"}
 
 
 # ---------------------------------------------------------------------------
@@ -301,7 +301,15 @@ def run_kvp(args):
         clocks = ClockSampler(dev.index if world == 1 else local)
         barrier()
         torch.cuda.synchronize()
+        # nvidia-smi samples every 20 ms: keep the GPU busy with untimed steps
+        # for a short pre-roll so the samples cover the load the timed steps see.
         clocks.start()
+        t_pre = time.perf_counter()
+        while time.perf_counter() - t_pre < args.preroll_s:
+            for _ in range(8):
+                flush.zero_()
+                st.run(stream)
+            stream.synchronize()
         t_wall = time.perf_counter()
         for i in range(args.steps):
             flush.zero_()
@@ -468,6 +476,7 @@ def main():
     ap.add_argument("--decode-splits", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--preroll-s", type=float, default=0.4)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -120,10 +120,12 @@ int32_t kvp_prefix_num_splits(int32_t B, int32_t num_q_heads, int32_t num_kv_hea
     const int64_t q_tiles = (static_cast<int64_t>(max_q_len) * g + 127) / 128;
     const int64_t ctas = q_tiles * num_kv_heads * B;
     const int64_t key_tiles = (static_cast<int64_t>(max_context_len) + 127) / 128;
-    const int64_t target = 2 * kNumSMs;
-    if (ctas >= target || key_tiles < 4) return 1;
-    int64_t splits = (target + ctas - 1) / ctas;
-    if (splits > key_tiles / 2) splits = key_tiles / 2;
+    // Split only when the tiles cannot fill one wave of the GPU: split partials
+    // cost an fp32 round trip and a merge launch, which measured slower than a
+    // second wave of whole tiles.
+    if (ctas >= kNumSMs || key_tiles < 8) return 1;
+    int64_t splits = (kNumSMs + ctas - 1) / ctas;
+    if (splits > key_tiles / 4) splits = key_tiles / 4;
     if (splits > 16) splits = 16;
     return splits < 1 ? 1 : static_cast<int32_t>(splits);
 }

@@ -36,7 +36,12 @@ struct DecodeCfg {
     static constexpr int REGION = kStageKeys * ROWB;  // one chunk column of a stage's K (or V)
     static constexpr int KBYTES = kStageKeys * D * 2;
     static constexpr int STAGE_BYTES = 2 * KBYTES;
-    static constexpr int NS = kRingBytes / STAGE_BYTES;
+    // Stage i sits in slot i % NS and is consumed by warp i % 4.  NS is a
+    // multiple of the consumer count, so every slot has one owner warp that
+    // consumes its phases in order: a waiter can never be two phases behind,
+    // which a parity wait could not tell apart from the phase it wants.
+    static constexpr int NS = kConsumerWarps * (kRingBytes / (kConsumerWarps * STAGE_BYTES));
+    static_assert(NS >= kConsumerWarps && NS % kConsumerWarps == 0, "ring depth");
     static constexpr int RED_BYTES = kConsumerWarps * 16 * D * 4 + 2 * kConsumerWarps * 16 * 4;
     static constexpr int SMEM_BYTES = NS * STAGE_BYTES + 2 * NS * 8 + 16 + 1024;
     static_assert(RED_BYTES <= NS * STAGE_BYTES, "reduction area reuses the ring");
@@ -149,17 +154,17 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             if (lane == 0) mbar_expect_tx(&full[slot], C::STAGE_BYTES);
+            __syncwarp();
+            // One lane per physical page of the stage issues that page's boxes.
+            const int blk = __shfl_sync(0xffffffffu, my_blk, (rel + lane) & 31);
             uint8_t* kst = smem + slot * C::STAGE_BYTES;
             uint8_t* vst = kst + C::KBYTES;
-            for (int q = 0; q < pps; ++q) {
-                const int blk = __shfl_sync(0xffffffffu, my_blk, rel + q);
-                if (lane == 0) {
-                    const int32_t y = (blk * Hkv + h) * BS;
+            if (lane < pps) {
+                const int32_t y = (blk * Hkv + h) * BS;
 #pragma unroll
-                    for (int c = 0; c < C::NCH; ++c) {
-                        tma_load_2d(kst + c * C::REGION + q * BS * C::ROWB, &tmap_k, c * C::CW, y, &full[slot]);
-                        tma_load_2d(vst + c * C::REGION + q * BS * C::ROWB, &tmap_v, c * C::CW, y, &full[slot]);
-                    }
+                for (int c = 0; c < C::NCH; ++c) {
+                    tma_load_2d(kst + c * C::REGION + lane * BS * C::ROWB, &tmap_k, c * C::CW, y, &full[slot]);
+                    tma_load_2d(vst + c * C::REGION + lane * BS * C::ROWB, &tmap_v, c * C::CW, y, &full[slot]);
                 }
             }
             issued = i + 1;
@@ -296,6 +301,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
                     mma16816<kBF16>(o[2 * nd2 + 1], pa[kk], b2, b3);
                 }
             }
+            if (nvalid < kStageKeys) fence_proxy_async_smem();  // generic zeroing before the next TMA write
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
         }

@@ -64,19 +64,14 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return p + (((a + 1023u) & ~1023u) - a);
 }
 
-// tcgen05.ld of 32 columns followed by its wait, in one statement so that no
+// tcgen05.ld of 128 columns followed by its wait, in one statement so that no
 // use of the registers can be scheduled before the data has arrived.
-__device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]) {
+__device__ __forceinline__ void tmem_ld128_sync(uint32_t taddr, uint32_t (&r)[128]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x128.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n\t"
         "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
-          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
-          "=r"(r[30]), "=r"(r[31])
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
         : "r"(taddr)
         : "memory");
 }
@@ -209,12 +204,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(&s_full[b], (jj >> 1) & 1, abort_flag, err)) { ok = false; break; }
             tc_fence_after();
             float x[kBN];
+            {
+                uint32_t r[kBN];
+                tmem_ld128_sync(lane_base + (b ? kSCol1 : kSCol0), r);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t r[32];
-                tmem_ld32_sync(lane_base + (b ? kSCol1 : kSCol0) + 32 * q, r);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) x[32 * q + i] = __uint_as_float(r[i]);
+                for (int i = 0; i < kBN; ++i) x[i] = __uint_as_float(r[i]);
             }
             tc_fence_before();
             __syncwarp();
@@ -226,9 +220,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < kBN; ++c)
                     if (c > lim) x[c] = -INFINITY;
             }
-            float mx = x[0];
+            // Tree reductions: eight independent chains instead of one serial chain.
+            float mx8[8];
 #pragma unroll
-            for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, x[c]);
+            for (int i = 0; i < 8; ++i) mx8[i] = x[i];
+#pragma unroll
+            for (int c = 8; c < kBN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             const float m_new = fmaxf(m, mx * sl2);
             const bool need = m_new > m + 8.0f;
             float alpha = 1.f;
@@ -238,13 +237,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l *= alpha;
             }
             const float mref = (m == -INFINITY) ? 0.f : m;
-            float ls = 0.f;
+            float ls8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < kBN; ++c) {
                 x[c] = fast_exp2(fmaf(x[c], sl2, -mref));
-                ls += x[c];
+                ls8[c & 7] += x[c];
             }
-            l += ls;
+            l += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
 
             if (jj > 0 && __any_sync(0xffffffffu, need)) {
                 // O holds PV_0 .. PV_{jj-1} at the old reference maximum: rescale it.
@@ -334,35 +333,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tmap_k);
             prefetch_tmap(&tmap_v);
         }
-        const int pages_per_tile = kBN / BS;
+        const int pages_per_tile = kBN / BS;  // 4, 8 or 16: a tile never straddles a 32-page batch
+        const int page_first = j_begin * pages_per_tile;
+        const int32_t* table = p.block_tables + static_cast<int64_t>(s) * p.max_blocks;
+        // Lane i holds the block id of page (batch * 32 + i); the next batch is
+        // requested 32 pages ahead so its latency hides behind the tiles in flight.
+        auto load_batch = [&](int batch) -> int {
+            const int pg = min(page_first + batch * 32 + lane, npages - 1);
+            return __ldg(table + pg);
+        };
+        int blk_cur = load_batch(0);
+        int blk_nxt = load_batch(1);
         int issued = 0;
         for (int jj = 0; jj < n_local; ++jj) {
-            const int j = j_begin + jj;
             const int b = jj & 1;
-            int my_blk = 0;
-            if (lane < pages_per_tile) {
-                const int pg = min(j * pages_per_tile + lane, npages - 1);
-                int blk = __ldg(p.block_tables + static_cast<int64_t>(s) * p.max_blocks + pg);
-                if (blk < 0 || blk >= p.pool.num_blocks) {
-                    report(err, KVP_DEVERR_BAD_BLOCK);
-                    blk = 0;
-                }
-                my_blk = blk;
+            const int rel = jj * pages_per_tile;
+            if ((rel & 31) == 0 && jj > 0) {
+                blk_cur = blk_nxt;
+                blk_nxt = load_batch((rel >> 5) + 1);
             }
+            int my_blk = blk_cur;
+            if (my_blk < 0 || my_blk >= p.pool.num_blocks) {
+                report(err, KVP_DEVERR_BAD_BLOCK);
+                my_blk = 0;
+            }
+            const int lane0 = rel & 31;
             int ok = 1;
             if (lane == 0 && jj >= 2) ok = mbar_wait(&k_empty[b], ((jj - 2) >> 1) & 1, abort_flag, err);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             if (lane == 0) mbar_expect_tx(&k_full[b], C::TILE_BYTES);
+            __syncwarp();
+            // One lane per physical page issues that page's boxes: TMA issue from
+            // a single thread is serial, so spread it over the pages of the tile.
+            const int blk_q = __shfl_sync(0xffffffffu, my_blk, (lane0 + lane) & 31);
             uint8_t* kt = smem + C::OFF_K + b * C::TILE_BYTES;
-            for (int q = 0; q < pages_per_tile; ++q) {
-                const int blk = __shfl_sync(0xffffffffu, my_blk, q);
-                if (lane == 0) {
-                    const int32_t y = (blk * Hkv + h) * BS;
+            if (lane < pages_per_tile) {
+                const int32_t y = (blk_q * Hkv + h) * BS;
 #pragma unroll
-                    for (int c = 0; c < C::NCH; ++c)
-                        tma_load_2d(kt + c * C::CHUNK_BYTES + q * BS * C::ROWB, &tmap_k, c * C::CW, y, &k_full[b]);
-                }
+                for (int c = 0; c < C::NCH; ++c)
+                    tma_load_2d(kt + c * C::CHUNK_BYTES + lane * BS * C::ROWB, &tmap_k, c * C::CW, y, &k_full[b]);
             }
             if (lane == 0 && jj >= 2) ok = mbar_wait(&v_empty[b], ((jj - 2) >> 1) & 1, abort_flag, err);
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -371,15 +381,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             if (lane == 0) mbar_expect_tx(&v_full[b], C::TILE_BYTES);
+            __syncwarp();
             uint8_t* vt = smem + C::OFF_V + b * C::TILE_BYTES;
-            for (int q = 0; q < pages_per_tile; ++q) {
-                const int blk = __shfl_sync(0xffffffffu, my_blk, q);
-                if (lane == 0) {
-                    const int32_t y = (blk * Hkv + h) * BS;
+            if (lane < pages_per_tile) {
+                const int32_t y = (blk_q * Hkv + h) * BS;
 #pragma unroll
-                    for (int c = 0; c < C::NCH; ++c)
-                        tma_load_2d(vt + c * C::CHUNK_BYTES + q * BS * C::ROWB, &tmap_v, c * C::CW, y, &v_full[b]);
-                }
+                for (int c = 0; c < C::NCH; ++c)
+                    tma_load_2d(vt + c * C::CHUNK_BYTES + lane * BS * C::ROWB, &tmap_v, c * C::CW, y, &v_full[b]);
             }
             issued = jj + 1;
         }
