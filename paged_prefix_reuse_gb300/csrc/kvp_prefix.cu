@@ -1,6 +1,6 @@
 // kvp_prefix.cu -- causal attention of a chunk of new tokens over a paged
 // KV cache (cached prefix + the chunk's own K/V), on the 5th-generation
-// tensor cores (tcgen05, accumulators in tensor memory).
+// tensor cores (tcgen05, operands and accumulators in tensor memory).
 //
 // What it computes (kvboost 0.6.0, "How it works" step 5: the live suffix
 // attends to the cached prefix in one forward; "Flash Attention (CUDA)":
@@ -10,36 +10,47 @@
 //     out[t][h] = softmax_j(scale * q[t][h] . K[j]) . V[j],  j <= P_s + i_t,
 // K/V read through the block table (kvboost "CPU paged attention").
 //
-// Design for sm_103a (one CTA per 128-row query tile x kv head x sequence
-// [x key-range split]; 192 threads; about 224 KB of shared memory at d=128):
-//  * rows of a query tile are (token, query head of the GQA group) pairs, so
-//    all heads that share a kv head consume each loaded K/V tile once;
-//  * warp 4 gathers K and V tiles of 128 keys page by page with 2-D TMA
-//    loads (one box = one physical block of one kv head, found through the
-//    block table), swizzled to match the UMMA shared-memory descriptors,
-//    double-buffered;
-//  * warp 5 issues tcgen05.mma: S = Q K^T (M=128, N=128) into one of two
-//    TMEM S buffers, and O += P V (M=128, N=d) into a TMEM accumulator;
-//    completion is signalled with tcgen05.commit on mbarriers;
-//  * warps 0-3 (thread i owns query row i = TMEM lane i) read S from TMEM,
-//    run the online softmax in fp32 (log2 domain), write P as fp16/bf16 into
-//    a swizzled shared-memory tile (double-buffered), and rescale O in TMEM
-//    only when a row maximum grew by more than 2^8 (exact: the final
-//    normalisation uses the same reference maximum);
-//  * key tiles past the last query's position are never loaded (causal
-//    skip); the diagonal tiles are masked per row;
-//  * with num_splits > 1, each CTA handles a contiguous share of the key
-//    tiles and writes a normalised partial (O, log2 lse) for merge_kernel.
+// Design for sm_103a.  One CTA handles two 128-row query tiles (256 rows) of
+// one kv head of one sequence [and one share of its key tiles when split].
+// Rows are (token, query head of the GQA group) pairs, so every query head
+// that shares a kv head consumes each K/V tile once, and the two query tiles
+// halve the K/V bytes each MMA flop needs.  320 threads:
+//  * warp 8 (producer) gathers 128-key K and V tiles into a ring of shared
+//    memory slots with 2-D TMA boxes, one box per (physical block, 64-column
+//    chunk) found through the block table, one lane per block; 128B-swizzled
+//    (64B at d=96) to match the UMMA descriptors;
+//  * warp 9 (MMA) issues tcgen05.mma from one thread: S_i = Q_i K^T (SS,
+//    M=128, N=128) into TMEM, and O_i += P_i V (TS: P_i read from TMEM,
+//    M=128, N=d).  The two query tiles alternate on the tensor core --
+//    PV_0, S_0, PV_1, S_1 -- so each softmax warpgroup works while the tensor
+//    core serves the other;
+//  * warps 0-3 and 4-7 (softmax warpgroups, one per query tile; thread i
+//    owns row i = TMEM lane i) read S with one 128-column tcgen05.ld, mask
+//    the causal diagonal, run the online softmax in fp32 (log2 domain,
+//    packed f32x2 arithmetic, ex2.approx), write P as 16-bit pairs back over
+//    S in TMEM (tcgen05.st), and rescale O in TMEM only when a row maximum
+//    grew by more than 2^8 (exact: the final 1/l uses the same reference);
+//  * the commit that signals S_i(j+1) also covers PV_i(j), so when a
+//    warpgroup sees S it may touch O_i and overwrite the P columns freely;
+//  * key tiles past the last query's position are never loaded; V rows past
+//    the context are zeroed in shared memory before P.V (0 * NaN = NaN).
+//
+// TMEM columns: S_0/P_0 [0,128), S_1/P_1 [128,256), O_0 [256,256+d),
+// O_1 [256+d, 256+2d) -- 512 columns, one CTA per SM.
 #include "kvp_internal.cuh"
 
 namespace kvp {
 namespace {
 
-constexpr int kThreads = 192;  // warps 0-3 softmax, warp 4 TMA producer, warp 5 MMA issuer
-constexpr int kBM = 128;       // query rows per tile (TMEM lanes)
-constexpr int kBN = 128;       // keys per tile
+constexpr int kSoftmaxWarps = 8;                    // two warpgroups, one per query tile
+constexpr int kProducerWarp = kSoftmaxWarps;        // warp 8
+constexpr int kMmaWarp = kSoftmaxWarps + 1;         // warp 9
+constexpr int kThreads = (kSoftmaxWarps + 2) * 32;  // 320
+constexpr int kBM = 128;                            // rows per query tile (TMEM lanes)
+constexpr int kRowsPerCta = 2 * kBM;
+constexpr int kBN = 128;  // keys per K/V tile
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSCol0 = 0, kSCol1 = 128, kOCol = 256;
+constexpr int kSmemBudget = 227 * 1024 - 2048;
 
 template <int D>
 struct PrefixCfg {
@@ -48,15 +59,19 @@ struct PrefixCfg {
     static constexpr int NCH = D / CW;
     static constexpr uint32_t SWZ = ROWB == 128 ? 2u : 4u;  // descriptor swizzle code: 128B or 64B
     static constexpr int CHUNK_BYTES = kBM * ROWB;          // one chunk column of a 128-row tile
-    static constexpr int TILE_BYTES = kBM * D * 2;
-    static constexpr int P_BYTES = kBM * kBN * 2;
+    static constexpr int TILE_BYTES = kBM * D * 2;          // a Q tile, or a K or V tile of 128 keys
+    static constexpr int NSLOT_FIT = (kSmemBudget - 2 * TILE_BYTES) / TILE_BYTES;
+    static constexpr int NSLOT = NSLOT_FIT < 8 ? NSLOT_FIT : 8;
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + TILE_BYTES;
-    static constexpr int OFF_V = OFF_K + 2 * TILE_BYTES;
-    static constexpr int OFF_P = OFF_V + 2 * TILE_BYTES;
-    static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-    static constexpr int NBARS = 17;
+    static constexpr int OFF_RING = 2 * TILE_BYTES;
+    static constexpr int OFF_BAR = OFF_RING + NSLOT * TILE_BYTES;
+    static constexpr int NBARS = 8 + 2 * NSLOT;
     static constexpr int SMEM_BYTES = OFF_BAR + NBARS * 8 + 16 + 1024;
+    static constexpr uint32_t S_COL0 = 0, S_COL1 = 128;
+    static constexpr uint32_t O_COL0 = 256, O_COL1 = 256 + D;
+    static_assert(NSLOT >= 4, "K/V ring too shallow");
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
+    static_assert(256 + 2 * D <= (int)kTmemCols, "tensor memory");
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -69,9 +84,31 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 __device__ __forceinline__ void tmem_ld128_sync(uint32_t taddr, uint32_t (&r)[128]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x128.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n\t"
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,"
+        "%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,"
+        "%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+        "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,"
+        "%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,"
+        "%126,%127}, [%128];\n\t"
         "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]),
+          "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]),
+          "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]),
+          "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]),
+          "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]),
+          "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]),
+          "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]),
+          "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]),
+          "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]),
+          "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]),
+          "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]),
+          "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]),
+          "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]),
+          "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
         : "r"(taddr)
         : "memory");
 }
@@ -94,21 +131,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-    uint64_t* q_full = bars + 0;
-    uint64_t* k_full = bars + 1;
-    uint64_t* k_empty = bars + 3;
-    uint64_t* v_full = bars + 5;
-    uint64_t* v_empty = bars + 7;
-    uint64_t* s_full = bars + 9;
-    uint64_t* s_free = bars + 11;
-    uint64_t* p_full = bars + 13;
-    uint64_t* o_done = bars + 15;
+    uint64_t* q_full = bars + 0;                 // [2] Q tile i in shared memory (128 arrivals)
+    uint64_t* s_full = bars + 2;                 // [2] S_i in TMEM (commit)
+    uint64_t* p_full = bars + 4;                 // [2] P_i in TMEM (4 warp arrivals)
+    uint64_t* o_done = bars + 6;                 // [2] last PV_i complete (commit)
+    uint64_t* slot_full = bars + 8;              // [NSLOT] ring slot loaded (TMA bytes)
+    uint64_t* slot_empty = bars + 8 + C::NSLOT;  // [NSLOT] ring slot released (commit)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x % p.num_splits;
-    const int qt = p.q_tiles - 1 - static_cast<int>(blockIdx.x) / p.num_splits;  // heavy tiles first
+    const int ct = p.q_tiles - 1 - static_cast<int>(blockIdx.x) / p.num_splits;  // heavy tiles first
     const int h = blockIdx.y, s = blockIdx.z;
     const int g = p.group, BS = p.pool.block_size, Hkv = p.pool.num_kv_heads;
     uint32_t* err = p.pool.err_word;
@@ -116,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cu0 = __ldg(p.cu_seqlens_q + s);
     const int N = __ldg(p.cu_seqlens_q + s + 1) - cu0;
     const int rows_total = N * g;
-    const int r0 = qt * kBM;
+    const int r0 = ct * kRowsPerCta;
     if (r0 >= rows_total) return;
     const int L = __ldg(p.context_lens + s);
     const int P = L - N;
@@ -125,7 +159,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0 && split == 0) report(err, KVP_DEVERR_BAD_LEN);
         return;
     }
-    const int r_last = min(rows_total, r0 + kBM) - 1;
+    const bool has1 = r0 + kBM < rows_total;  // is the second query tile non-empty?
+    const int r_last = min(rows_total, r0 + kRowsPerCta) - 1;
     const int qpos_max = P + r_last / g;
     const int n_tiles = qpos_max / kBN + 1;
     const int per = (n_tiles + p.num_splits - 1) / p.num_splits;
@@ -133,8 +168,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_local = min(n_tiles, j_begin + per) - j_begin;
 
     if (n_local <= 0) {
-        // This split's key range is empty for the whole tile: an empty partial.
-        if (tid < kBM && r0 + tid < rows_total) {
+        // This split's key range is empty for the whole CTA: empty partials.
+        if (tid < kRowsPerCta && r0 + tid < rows_total) {
             const int rg = r0 + tid;
             const int64_t wrow = static_cast<int64_t>(cu0 + rg / g) * p.num_q_heads + h * g + rg % g;
             p.ws_lse[wrow * p.num_splits + split] = -INFINITY;
@@ -144,21 +179,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (tid == 0) {
-        mbar_init(q_full, kBM);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&k_full[i], 1);
-            mbar_init(&k_empty[i], 1);
-            mbar_init(&v_full[i], 1);
-            mbar_init(&v_empty[i], 1);
+            mbar_init(&q_full[i], kBM);
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], 4);
             mbar_init(&p_full[i], 4);
             mbar_init(&o_done[i], 1);
+        }
+        for (int i = 0; i < C::NSLOT; ++i) {
+            mbar_init(&slot_full[i], 1);
+            mbar_init(&slot_empty[i], 1);
         }
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
@@ -167,168 +201,165 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp < 4) {
-        // =========================== softmax warps ===========================
-        const int row = tid;
-        const int rg = r0 + row;
-        const bool valid = rg < rows_total;
-        const int token = valid ? rg / g : 0;
-        const int head = h * g + (valid ? rg % g : 0);
-        const int qpos = valid ? P + token : L - 1;
+    if (warp < kSoftmaxWarps) {
+        // =========================== softmax warpgroups ===========================
+        const int wg = warp >> 2;
+        if (wg == 0 || has1) {
+            const int row = tid & (kBM - 1);
+            const int rg = r0 + wg * kBM + row;
+            const bool valid = rg < rows_total;
+            const int token = valid ? rg / g : 0;
+            const int head = h * g + (valid ? rg % g : 0);
+            const int qpos = valid ? P + token : L - 1;
 
-        {  // Q tile -> swizzled shared memory (K-major A operand)
-            constexpr int V16 = D / 8;
-            const uint4* q4 = static_cast<const uint4*>(p.q);
-            for (int e = tid; e < kBM * V16; e += kBM) {
-                const int rr = e / V16, c16 = e - (e / V16) * V16;
-                const int rgl = r0 + rr;
-                uint4 val = make_uint4(0, 0, 0, 0);
-                if (rgl < rows_total) {
-                    const int64_t qrow = static_cast<int64_t>(cu0 + rgl / g) * p.num_q_heads + h * g + rgl % g;
-                    val = __ldg(q4 + qrow * V16 + c16);
+            {  // Q tile wg -> swizzled shared memory (K-major A operand)
+                constexpr int V16 = D / 8;
+                const uint4* q4 = static_cast<const uint4*>(p.q);
+                uint8_t* qt = smem + C::OFF_Q + wg * C::TILE_BYTES;
+                for (int e = row; e < kBM * V16; e += kBM) {
+                    const int rr = e / V16, c16 = e - (e / V16) * V16;
+                    const int rgl = r0 + wg * kBM + rr;
+                    uint4 val = make_uint4(0, 0, 0, 0);
+                    if (rgl < rows_total) {
+                        const int64_t qrow =
+                            static_cast<int64_t>(cu0 + rgl / g) * p.num_q_heads + h * g + rgl % g;
+                        val = __ldg(q4 + qrow * V16 + c16);
+                    }
+                    const int ch = c16 / (C::CW / 8), ci = c16 - ch * (C::CW / 8);
+                    *reinterpret_cast<uint4*>(qt + ch * C::CHUNK_BYTES + swz_offset(rr, ci, C::ROWB)) = val;
                 }
-                const int ch = c16 / (C::CW / 8), ci = c16 - ch * (C::CW / 8);
-                *reinterpret_cast<uint4*>(smem + C::OFF_Q + ch * C::CHUNK_BYTES + swz_offset(rr, ci, C::ROWB)) = val;
+                fence_proxy_async_smem();
+                mbar_arrive(&q_full[wg]);
             }
-            fence_proxy_async_smem();
-            mbar_arrive(q_full);
-        }
 
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        const float sl2 = p.scale_log2;
-        float m = -INFINITY, l = 0.f;
-        bool ok = true;
-        for (int jj = 0; jj < n_local; ++jj) {
-            const int j = j_begin + jj;
-            const int b = jj & 1;
-            if (!mbar_wait(&s_full[b], (jj >> 1) & 1, abort_flag, err)) { ok = false; break; }
-            tc_fence_after();
-            float x[kBN];
-            {
-                uint32_t r[kBN];
-                tmem_ld128_sync(lane_base + (b ? kSCol1 : kSCol0), r);
-#pragma unroll
-                for (int i = 0; i < kBN; ++i) x[i] = __uint_as_float(r[i]);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_free[b]);
-
-            const int lim = qpos - j * kBN;  // last visible column of this tile
-            if (lim < kBN - 1) {
-#pragma unroll
-                for (int c = 0; c < kBN; ++c)
-                    if (c > lim) x[c] = -INFINITY;
-            }
-            // Tree reductions: eight independent chains instead of one serial chain.
-            float mx8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mx8[i] = x[i];
-#pragma unroll
-            for (int c = 8; c < kBN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-            const float m_new = fmaxf(m, mx * sl2);
-            const bool need = m_new > m + 8.0f;
-            float alpha = 1.f;
-            if (need) {
-                alpha = fast_exp2(m - m_new);
-                m = m_new;
-                l *= alpha;
-            }
-            const float mref = (m == -INFINITY) ? 0.f : m;
-            float ls8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int c = 0; c < kBN; ++c) {
-                x[c] = fast_exp2(fmaf(x[c], sl2, -mref));
-                ls8[c & 7] += x[c];
-            }
-            l += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
-
-            if (jj > 0 && __any_sync(0xffffffffu, need)) {
-                // O holds PV_0 .. PV_{jj-1} at the old reference maximum: rescale it.
-                if (!mbar_wait(&o_done[(jj - 1) & 1], ((jj - 1) >> 1) & 1, abort_flag, err)) { ok = false; break; }
+            const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+            const uint32_t scol = wg ? C::S_COL1 : C::S_COL0;
+            const uint32_t ocol = wg ? C::O_COL1 : C::O_COL0;
+            const float sl2 = p.scale_log2;
+            float m = -INFINITY, l = 0.f;
+            bool ok = true;
+            for (int jj = 0; jj < n_local; ++jj) {
+                const int j = j_begin + jj;
+                if (!mbar_wait(&s_full[wg], jj & 1, abort_flag, err)) { ok = false; break; }
                 tc_fence_after();
+                float x[kBN];
+                {
+                    uint32_t r[kBN];
+                    tmem_ld128_sync(lane_base + scol, r);
 #pragma unroll
-                for (int cb = 0; cb < D / 16; ++cb) {
-                    uint32_t r[16];
-                    tmem_ld16_sync(lane_base + kOCol + 16 * cb, r);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                    tmem_st16(lane_base + kOCol + 16 * cb, r);
+                    for (int i = 0; i < kBN; ++i) x[i] = __uint_as_float(r[i]);
                 }
-                tmem_wait_st();
-            }
-            if (jj >= 2) {  // P buffer b was last read by PV_{jj-2}
-                if (!mbar_wait(&o_done[b], ((jj - 2) >> 1) & 1, abort_flag, err)) { ok = false; break; }
-            }
-            uint8_t* pb = smem + C::OFF_P + b * C::P_BYTES;
+                const int lim = qpos - j * kBN;  // last visible column of this tile
+                if (lim < kBN - 1) {
 #pragma unroll
-            for (int c16 = 0; c16 < kBN / 8; ++c16) {
-                uint4 v;
-                v.x = pack2<kBF16>(x[8 * c16 + 0], x[8 * c16 + 1]);
-                v.y = pack2<kBF16>(x[8 * c16 + 2], x[8 * c16 + 3]);
-                v.z = pack2<kBF16>(x[8 * c16 + 4], x[8 * c16 + 5]);
-                v.w = pack2<kBF16>(x[8 * c16 + 6], x[8 * c16 + 7]);
-                *reinterpret_cast<uint4*>(pb + (c16 >> 3) * (kBM * 128) + swz_offset(row, c16 & 7, 128)) = v;
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[b]);
-        }
+                    for (int c = 0; c < kBN; ++c)
+                        if (c > lim) x[c] = -INFINITY;
+                }
+                // Row maximum: 3-input max in eight independent chains.
+                float mx8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx8[i] = x[i];
+#pragma unroll
+                for (int c = 8; c < kBN - 8; c += 16) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], x[c + i], x[c + 8 + i]);
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], x[kBN - 8 + i]);
+                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                       fmaxf(mx8[6], mx8[7]));
+                const float m_new = fmaxf(m, mx * sl2);
+                const bool need = m_new > m + 8.0f;
+                float alpha = 1.f;
+                if (need) {
+                    alpha = fast_exp2(m - m_new);
+                    m = m_new;
+                    l *= alpha;
+                }
+                const float mref = (m == -INFINITY) ? 0.f : m;
+                // p = 2^(x * scale * log2 e - m), pairs on the packed fp32 pipe.
+                const float2 sc = make_float2(sl2, sl2), nb = make_float2(-mref, -mref);
+                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f)};
+                uint32_t pk[kBN / 2];
+#pragma unroll
+                for (int c = 0; c < kBN; c += 2) {
+                    const float2 t = ffma2(make_float2(x[c], x[c + 1]), sc, nb);
+                    const float2 e = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+                    acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], e);
+                    pk[c >> 1] = pack2<kBF16>(e.x, e.y);
+                }
+                const float2 a = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+                l += a.x + a.y;
 
-        // ------------------------------ epilogue ------------------------------
-        if (ok) {
-            const int jl = n_local - 1;
-            ok = mbar_wait(&o_done[jl & 1], (jl >> 1) & 1, abort_flag, err);
-        }
-        if (ok) {
-            tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            const float lse2 = l > 0.f ? m + __log2f(l) : -INFINITY;
-            const int64_t orow = static_cast<int64_t>(cu0 + token) * p.num_q_heads + head;
-            if (p.num_splits == 1) {
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + orow * D * 2);
+                if (jj > 0 && __any_sync(0xffffffffu, need)) {
+                    // O_wg holds PV_0 .. PV_{jj-1} (the commit that signalled S
+                    // covered them) at the old reference maximum: rescale it.
 #pragma unroll
-                for (int cb = 0; cb < D / 16; ++cb) {
-                    uint32_t r[16];
-                    tmem_ld16_sync(lane_base + kOCol + 16 * cb, r);
-                    uint4 a, bq;
-                    a.x = pack2<kBF16>(__uint_as_float(r[0]) * inv, __uint_as_float(r[1]) * inv);
-                    a.y = pack2<kBF16>(__uint_as_float(r[2]) * inv, __uint_as_float(r[3]) * inv);
-                    a.z = pack2<kBF16>(__uint_as_float(r[4]) * inv, __uint_as_float(r[5]) * inv);
-                    a.w = pack2<kBF16>(__uint_as_float(r[6]) * inv, __uint_as_float(r[7]) * inv);
-                    bq.x = pack2<kBF16>(__uint_as_float(r[8]) * inv, __uint_as_float(r[9]) * inv);
-                    bq.y = pack2<kBF16>(__uint_as_float(r[10]) * inv, __uint_as_float(r[11]) * inv);
-                    bq.z = pack2<kBF16>(__uint_as_float(r[12]) * inv, __uint_as_float(r[13]) * inv);
-                    bq.w = pack2<kBF16>(__uint_as_float(r[14]) * inv, __uint_as_float(r[15]) * inv);
-                    if (valid) {
-                        dst[2 * cb] = a;
-                        dst[2 * cb + 1] = bq;
+                    for (int cb = 0; cb < D / 16; ++cb) {
+                        uint32_t r[16];
+                        tmem_ld16_sync(lane_base + ocol + 16 * cb, r);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        tmem_st16(lane_base + ocol + 16 * cb, r);
                     }
                 }
-                if (valid && p.lse)
-                    p.lse[static_cast<int64_t>(head) * p.total_q + cu0 + token] = lse2 * 0.69314718055994531f;
-            } else {
-                float* dst = p.ws_o + (orow * p.num_splits + split) * D;
+                tmem_st64(lane_base + scol, pk);  // P over the first 64 columns of S
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[wg]);
+            }
+
+            // ------------------------------ epilogue ------------------------------
+            if (ok) ok = mbar_wait(&o_done[wg], 0, abort_flag, err);
+            if (ok) {
+                tc_fence_after();
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const float lse2 = l > 0.f ? m + __log2f(l) : -INFINITY;
+                const int64_t orow = static_cast<int64_t>(cu0 + token) * p.num_q_heads + head;
+                if (p.num_splits == 1) {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + orow * D * 2);
 #pragma unroll
-                for (int cb = 0; cb < D / 16; ++cb) {
-                    uint32_t r[16];
-                    tmem_ld16_sync(lane_base + kOCol + 16 * cb, r);
-                    if (valid) {
-#pragma unroll
-                        for (int i = 0; i < 16; i += 4)
-                            *reinterpret_cast<float4*>(dst + 16 * cb + i) =
-                                make_float4(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv,
-                                            __uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv);
+                    for (int cb = 0; cb < D / 16; ++cb) {
+                        uint32_t r[16];
+                        tmem_ld16_sync(lane_base + ocol + 16 * cb, r);
+                        uint4 a0, a1;
+                        a0.x = pack2<kBF16>(__uint_as_float(r[0]) * inv, __uint_as_float(r[1]) * inv);
+                        a0.y = pack2<kBF16>(__uint_as_float(r[2]) * inv, __uint_as_float(r[3]) * inv);
+                        a0.z = pack2<kBF16>(__uint_as_float(r[4]) * inv, __uint_as_float(r[5]) * inv);
+                        a0.w = pack2<kBF16>(__uint_as_float(r[6]) * inv, __uint_as_float(r[7]) * inv);
+                        a1.x = pack2<kBF16>(__uint_as_float(r[8]) * inv, __uint_as_float(r[9]) * inv);
+                        a1.y = pack2<kBF16>(__uint_as_float(r[10]) * inv, __uint_as_float(r[11]) * inv);
+                        a1.z = pack2<kBF16>(__uint_as_float(r[12]) * inv, __uint_as_float(r[13]) * inv);
+                        a1.w = pack2<kBF16>(__uint_as_float(r[14]) * inv, __uint_as_float(r[15]) * inv);
+                        if (valid) {
+                            dst[2 * cb] = a0;
+                            dst[2 * cb + 1] = a1;
+                        }
                     }
+                    if (valid && p.lse)
+                        p.lse[static_cast<int64_t>(head) * p.total_q + cu0 + token] = lse2 * 0.69314718055994531f;
+                } else {
+                    float* dst = p.ws_o + (orow * p.num_splits + split) * D;
+#pragma unroll
+                    for (int cb = 0; cb < D / 16; ++cb) {
+                        uint32_t r[16];
+                        tmem_ld16_sync(lane_base + ocol + 16 * cb, r);
+                        if (valid) {
+#pragma unroll
+                            for (int i = 0; i < 16; i += 4)
+                                *reinterpret_cast<float4*>(dst + 16 * cb + i) =
+                                    make_float4(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv,
+                                                __uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv);
+                        }
+                    }
+                    if (valid) p.ws_lse[orow * p.num_splits + split] = lse2;
                 }
-                if (valid) p.ws_lse[orow * p.num_splits + split] = lse2;
             }
         }
-    } else if (warp == 4) {
-        // ========================= TMA producer warp =========================
+    } else if (warp == kProducerWarp) {
+        // ============================ TMA producer warp ============================
         if (lane == 0) {
             prefetch_tmap(&tmap_k);
             prefetch_tmap(&tmap_v);
@@ -344,9 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         int blk_cur = load_batch(0);
         int blk_nxt = load_batch(1);
-        int issued = 0;
-        for (int jj = 0; jj < n_local; ++jj) {
-            const int b = jj & 1;
+        int loads = 0;  // ring loads issued: K_j is load 2j, V_j is load 2j+1
+        bool stop = false;
+        for (int jj = 0; jj < n_local && !stop; ++jj) {
             const int rel = jj * pages_per_tile;
             if ((rel & 31) == 0 && jj > 0) {
                 blk_cur = blk_nxt;
@@ -357,66 +388,100 @@ __global__ void __launch_bounds__(kThreads, 1)
                 report(err, KVP_DEVERR_BAD_BLOCK);
                 my_blk = 0;
             }
-            const int lane0 = rel & 31;
-            int ok = 1;
-            if (lane == 0 && jj >= 2) ok = mbar_wait(&k_empty[b], ((jj - 2) >> 1) & 1, abort_flag, err);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            if (lane == 0) mbar_expect_tx(&k_full[b], C::TILE_BYTES);
-            __syncwarp();
             // One lane per physical page issues that page's boxes: TMA issue from
             // a single thread is serial, so spread it over the pages of the tile.
-            const int blk_q = __shfl_sync(0xffffffffu, my_blk, (lane0 + lane) & 31);
-            uint8_t* kt = smem + C::OFF_K + b * C::TILE_BYTES;
-            if (lane < pages_per_tile) {
-                const int32_t y = (blk_q * Hkv + h) * BS;
+            const int blk_q = __shfl_sync(0xffffffffu, my_blk, ((rel & 31) + lane) & 31);
+            const int32_t y = (blk_q * Hkv + h) * BS;
+            for (int kv = 0; kv < 2; ++kv) {
+                const int gl = 2 * jj + kv;
+                const int slot = gl % C::NSLOT;
+                int ok = 1;
+                if (lane == 0 && gl >= C::NSLOT)
+                    ok = mbar_wait(&slot_empty[slot], ((gl / C::NSLOT) - 1) & 1, abort_flag, err);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) {
+                    stop = true;
+                    break;
+                }
+                if (lane == 0) mbar_expect_tx(&slot_full[slot], C::TILE_BYTES);
+                __syncwarp();
+                uint8_t* dst = smem + C::OFF_RING + slot * C::TILE_BYTES;
+                if (lane < pages_per_tile) {
 #pragma unroll
-                for (int c = 0; c < C::NCH; ++c)
-                    tma_load_2d(kt + c * C::CHUNK_BYTES + lane * BS * C::ROWB, &tmap_k, c * C::CW, y, &k_full[b]);
+                    for (int c = 0; c < C::NCH; ++c)
+                        tma_load_2d(dst + c * C::CHUNK_BYTES + lane * BS * C::ROWB, kv ? &tmap_v : &tmap_k,
+                                    c * C::CW, y, &slot_full[slot]);
+                }
+                loads = gl + 1;
             }
-            if (lane == 0 && jj >= 2) ok = mbar_wait(&v_empty[b], ((jj - 2) >> 1) & 1, abort_flag, err);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) {
-                issued = -(jj + 1);  // K of tile jj issued, V not
-                break;
-            }
-            if (lane == 0) mbar_expect_tx(&v_full[b], C::TILE_BYTES);
-            __syncwarp();
-            uint8_t* vt = smem + C::OFF_V + b * C::TILE_BYTES;
-            if (lane < pages_per_tile) {
-                const int32_t y = (blk_q * Hkv + h) * BS;
-#pragma unroll
-                for (int c = 0; c < C::NCH; ++c)
-                    tma_load_2d(vt + c * C::CHUNK_BYTES + lane * BS * C::ROWB, &tmap_v, c * C::CW, y, &v_full[b]);
-            }
-            issued = jj + 1;
         }
         // Do not leave while copies may still land in shared memory.
         if (lane == 0) {
             volatile int no_abort = 0;
-            const int nk = issued < 0 ? -issued : issued;
-            const int nv = issued < 0 ? -issued - 1 : issued;
-            for (int i = max(0, nk - 2); i < nk; ++i) mbar_wait(&k_full[i & 1], (i >> 1) & 1, &no_abort, err);
-            for (int i = max(0, nv - 2); i < nv; ++i) mbar_wait(&v_full[i & 1], (i >> 1) & 1, &no_abort, err);
+            for (int gl = max(0, loads - C::NSLOT); gl < loads; ++gl)
+                mbar_wait(&slot_full[gl % C::NSLOT], (gl / C::NSLOT) & 1, &no_abort, err);
         }
     } else {
-        // ========================= MMA issuer warp ==========================
+        // ============================ MMA issuer warp ============================
         constexpr uint32_t idesc_s = instr_desc_f16(kBF16, kBM, kBN, false);
         constexpr uint32_t idesc_o = instr_desc_f16(kBF16, kBM, D, true);
-        const uint32_t q_base = smem_u32(smem + C::OFF_Q);
+        const uint32_t ring = smem_u32(smem + C::OFF_RING);
+        const uint32_t qb0 = smem_u32(smem + C::OFF_Q), qb1 = qb0 + C::TILE_BYTES;
         uint64_t* last_bar = nullptr;
         uint32_t last_par = 0;
-        bool ok = mbar_wait(q_full, 0, abort_flag, err);
+        auto slot_addr = [&](int gl) -> uint32_t { return ring + (gl % C::NSLOT) * C::TILE_BYTES; };
+        auto wait_slot = [&](int gl) -> bool {
+            return mbar_wait(&slot_full[gl % C::NSLOT], (gl / C::NSLOT) & 1, abort_flag, err);
+        };
+        auto release = [&](int gl) {
+            if (lane == 0) tc_commit(&slot_empty[gl % C::NSLOT]);
+            last_bar = &slot_empty[gl % C::NSLOT];
+            last_par = (gl / C::NSLOT) & 1;
+        };
+        auto issue_s = [&](int i, uint32_t kbase) {
+            if (lane == 0) {
+                const uint32_t qb = i ? qb1 : qb0;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk * 16) / C::CW) * C::CHUNK_BYTES + ((kk * 16) % C::CW) * 2;
+                    const uint64_t ad = smem_desc(qb + off, 16, 8 * C::ROWB, C::SWZ);
+                    const uint64_t bd = smem_desc(kbase + off, 16, 8 * C::ROWB, C::SWZ);
+                    tc_mma_ss(tmem + (i ? C::S_COL1 : C::S_COL0), ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(&s_full[i]);
+            }
+        };
+        auto issue_pv = [&](int i, uint32_t vbase, bool accumulate) {
+            if (lane == 0) {
+                const uint32_t scol = i ? C::S_COL1 : C::S_COL0;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    const uint64_t bd = smem_desc(vbase + kk * 16 * C::ROWB, C::CHUNK_BYTES, 8 * C::ROWB, C::SWZ);
+                    tc_mma_ts(tmem + (i ? C::O_COL1 : C::O_COL0), tmem + scol + kk * 8, bd, idesc_o,
+                              (accumulate || kk > 0) ? 1u : 0u);
+                }
+            }
+        };
 
-        auto issue_pv = [&](int i) -> bool {
-            const int b = i & 1;
-            if (!mbar_wait(&p_full[b], (i >> 1) & 1, abort_flag, err)) return false;
-            if (!mbar_wait(&v_full[b], (i >> 1) & 1, abort_flag, err)) return false;
-            uint8_t* vt = smem + C::OFF_V + b * C::TILE_BYTES;
-            const int nvalid = L - (j_begin + i) * kBN;
+        bool ok = mbar_wait(&q_full[0], 0, abort_flag, err);
+        if (ok && has1) ok = mbar_wait(&q_full[1], 0, abort_flag, err);
+        if (ok) ok = wait_slot(0);
+        if (ok) {
+            tc_fence_after();
+            issue_s(0, slot_addr(0));
+            if (has1) issue_s(1, slot_addr(0));
+            release(0);
+            __syncwarp();
+        }
+        for (int jj = 0; ok && jj < n_local; ++jj) {
+            const int gv = 2 * jj + 1, gk = 2 * jj + 2;
+            const bool more = jj + 1 < n_local;
+            if (!wait_slot(gv)) { ok = false; break; }
+            const int nvalid = L - (j_begin + jj) * kBN;
             if (nvalid < kBN) {
                 // Rows past the context may hold any bytes (even NaN); P is 0
                 // there, but 0 * NaN is NaN, so clear those V rows.
+                uint8_t* vt = smem + C::OFF_RING + (gv % C::NSLOT) * C::TILE_BYTES;
                 const int first = max(nvalid, 0);
                 const int per_row = C::ROWB / 16;
                 const int nvec = (kBN - first) * per_row * C::NCH;
@@ -429,48 +494,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
             }
+            // ---- query tile 0: PV_0(jj), then S_0(jj+1)
+            if (!mbar_wait(&p_full[0], jj & 1, abort_flag, err)) { ok = false; break; }
             tc_fence_after();
-            if (lane == 0) {
-                const uint32_t p_base = smem_u32(smem + C::OFF_P + b * C::P_BYTES);
-                const uint32_t v_base = smem_u32(vt);
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint64_t ad = smem_desc(p_base + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024, 2);
-                    const uint64_t bd = smem_desc(v_base + kk * 16 * C::ROWB, C::CHUNK_BYTES, 8 * C::ROWB, C::SWZ);
-                    tc_mma_ss(tmem + kOCol, ad, bd, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
-                }
-                tc_commit(&o_done[b]);
-                tc_commit(&v_empty[b]);
+            issue_pv(0, slot_addr(gv), jj > 0);
+            if (!more && lane == 0) tc_commit(&o_done[0]);
+            if (more) {
+                if (!wait_slot(gk)) { ok = false; break; }
+                tc_fence_after();
+                issue_s(0, slot_addr(gk));
+            }
+            // ---- query tile 1: PV_1(jj), then S_1(jj+1)
+            if (has1) {
+                if (!mbar_wait(&p_full[1], jj & 1, abort_flag, err)) { ok = false; break; }
+                tc_fence_after();
+                issue_pv(1, slot_addr(gv), jj > 0);
+                if (!more && lane == 0) tc_commit(&o_done[1]);
+            }
+            release(gv);
+            if (more) {
+                if (has1) issue_s(1, slot_addr(gk));
+                release(gk);
             }
             __syncwarp();
-            last_bar = &o_done[b];
-            last_par = (i >> 1) & 1;
-            return true;
-        };
-
-        for (int jj = 0; ok && jj < n_local; ++jj) {
-            const int b = jj & 1;
-            if (!mbar_wait(&k_full[b], (jj >> 1) & 1, abort_flag, err)) { ok = false; break; }
-            if (jj >= 2 && !mbar_wait(&s_free[b], ((jj - 2) >> 1) & 1, abort_flag, err)) { ok = false; break; }
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t k_base = smem_u32(smem + C::OFF_K + b * C::TILE_BYTES);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = ((kk * 16) / C::CW) * C::CHUNK_BYTES + ((kk * 16) % C::CW) * 2;
-                    const uint64_t ad = smem_desc(q_base + off, 16, 8 * C::ROWB, C::SWZ);
-                    const uint64_t bd = smem_desc(k_base + off, 16, 8 * C::ROWB, C::SWZ);
-                    tc_mma_ss(tmem + (b ? kSCol1 : kSCol0), ad, bd, idesc_s, kk > 0 ? 1u : 0u);
-                }
-                tc_commit(&s_full[b]);
-                tc_commit(&k_empty[b]);
-            }
-            __syncwarp();
-            last_bar = &s_full[b];
-            last_par = (jj >> 1) & 1;
-            if (jj >= 1 && !issue_pv(jj - 1)) { ok = false; break; }
         }
-        if (ok) issue_pv(n_local - 1);
         // Let every issued MMA finish before tensor memory is released.
         if (lane == 0 && last_bar) {
             volatile int no_abort = 0;
@@ -481,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -504,6 +551,8 @@ cudaError_t launch_prefix_t(const PrefixParams& p, const CUtensorMap& tk, const 
 }
 
 }  // namespace
+
+int prefix_rows_per_cta() { return kRowsPerCta; }
 
 cudaError_t launch_prefix_attn(const PrefixParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                cudaStream_t stream) {

@@ -148,7 +148,7 @@ def test_workspace_and_split_helpers(lib):
     # Large problems need no split; tiny ones are spread over the SMs.
     assert kvp.kvp_prefix_num_splits(4, 64, 8, 128, 2048, 34816) == 1
     assert kvp.kvp_prefix_num_splits(1, 2, 2, 64, 16, 48) == 1
-    assert kvp.kvp_prefix_num_splits(8, 16, 2, 128, 256, 1280) == 1  # 256 tiles fill a wave
-    assert kvp.kvp_prefix_num_splits(1, 8, 8, 128, 128, 32768) >= 2  # 8 long tiles: split
+    assert kvp.kvp_prefix_num_splits(8, 16, 2, 128, 256, 1280) == 1  # 128 CTAs: no split
+    assert kvp.kvp_prefix_num_splits(1, 8, 8, 128, 128, 32768) >= 2  # 8 CTAs over 256 key tiles: split
     assert kvp.kvp_decode_num_splits(64, 8, 16, 8193) == 17
     assert kvp.kvp_decode_num_splits(1, 1, 16, 300) == 3
