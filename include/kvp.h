@@ -153,6 +153,36 @@ kvp_status kvp_decode_attn(const kvp_pool *pool, const void *q, void *out, float
                            int32_t max_context_len, float softmax_scale, int32_t num_splits, void *workspace,
                            size_t workspace_bytes, void *stream);
 
+/* Bytes of split partials that kvp_decode_attn_noalloc can hold (32 MiB). */
+#define KVP_DECODE_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/* Decode attention that allocates nothing and takes no workspace.  The pages
+ * have no counterpart of this call: it exists for callers that cannot hand
+ * the library device memory at the point of the call -- a runtime that owns
+ * a fixed memory budget through its own allocator, a plug-in that has no
+ * access to the host application's allocator, or a serving loop that bans
+ * cudaMalloc/cudaFree because they can synchronise the device.
+ * Arguments, results and errors are those of kvp_decode_attn without
+ * `workspace` and `workspace_bytes`.  The split partials go to one fixed
+ * array of KVP_DECODE_NOALLOC_SCRATCH_BYTES in the library's device image,
+ * which every GPU that loads the library holds until the process exits.
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.  Every call uses the same array and
+ * it keeps the last call's contents; nothing in it needs to start at zero,
+ * because each call writes every partial it reads.  Calls whose kernels
+ * overlap on the GPU (e.g. on two streams without ordering) race on the
+ * array: order them on one stream or with events.
+ * Returns KVP_ERR_WORKSPACE, launching nothing, when the resolved split
+ * count needs more than the array holds, i.e. when
+ * kvp_workspace_size(1, B, num_q_heads, head_dim, splits) exceeds
+ * KVP_DECODE_NOALLOC_SCRATCH_BYTES; pass a smaller num_splits or batch.
+ * It calls no cudaMalloc, cudaFree or other allocating routine. */
+kvp_status kvp_decode_attn_noalloc(const kvp_pool *pool, const void *q, void *out, float *lse,
+                                   const int32_t *context_lens, const int32_t *block_tables, int32_t max_blocks,
+                                   int32_t B, int32_t num_q_heads, int32_t max_context_len, float softmax_scale,
+                                   int32_t num_splits, void *stream);
+
 /* Split counts the library picks for num_splits == 0. */
 int32_t kvp_prefix_num_splits(int32_t B, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                               int32_t max_q_len, int32_t max_context_len);

@@ -32,6 +32,7 @@ __all__ = [
     "kvp_block_copy",
     "kvp_prefix_attn",
     "kvp_decode_attn",
+    "kvp_decode_attn_noalloc",
     "kvp_workspace_size",
     "kvp_prefix_num_splits",
     "kvp_decode_num_splits",
@@ -55,6 +56,7 @@ EXPORTED_SYMBOLS = (
     "kvp_block_copy",
     "kvp_prefix_attn",
     "kvp_decode_attn",
+    "kvp_decode_attn_noalloc",
     "kvp_prefix_num_splits",
     "kvp_decode_num_splits",
     "kvp_workspace_size",
@@ -112,7 +114,9 @@ def load_library():
         lib.kvp_block_copy.argtypes = [PP, P, i32, P]
         lib.kvp_prefix_attn.argtypes = [PP, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, i32, P, sz, P]
         lib.kvp_decode_attn.argtypes = [PP, P, P, P, P, P, i32, i32, i32, i32, f32, i32, P, sz, P]
-        for name in ("kvp_slot_mapping", "kvp_cache_append", "kvp_block_copy", "kvp_prefix_attn", "kvp_decode_attn"):
+        lib.kvp_decode_attn_noalloc.argtypes = [PP, P, P, P, P, P, i32, i32, i32, i32, f32, i32, P]
+        for name in ("kvp_slot_mapping", "kvp_cache_append", "kvp_block_copy", "kvp_prefix_attn", "kvp_decode_attn",
+                     "kvp_decode_attn_noalloc"):
             getattr(lib, name).restype = ctypes.c_int
         lib.kvp_prefix_num_splits.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.kvp_prefix_num_splits.restype = i32
@@ -293,4 +297,29 @@ def kvp_decode_attn(pool: PagedKVPool, q: torch.Tensor, context_lens: torch.Tens
                                int(block_tables.shape[1]), B, Hq, int(max_context_len), float(softmax_scale),
                                int(splits), _ptr(workspace), ws_bytes, _stream(stream)),
            "kvp_decode_attn")
+    return out, lse
+
+
+# Bytes of split partials the no-allocation decode entry point can hold.
+DECODE_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def kvp_decode_attn_noalloc(pool: PagedKVPool, q: torch.Tensor, context_lens: torch.Tensor,
+                            block_tables: torch.Tensor, max_context_len: int, softmax_scale: float,
+                            num_splits: int = 0, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                            want_lse: bool = True, stream=None):
+    """Decode attention without a workspace: the split partials use the
+    library's fixed device array (see kvp.h).  The caller still provides
+    ``out`` and ``lse`` (allocated here only when omitted)."""
+    lib = load_library()
+    B, Hq, d = (int(x) for x in q.shape)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((Hq, B), dtype=torch.float32, device=q.device)
+    _check(lib.kvp_decode_attn_noalloc(pool.c, _ptr(q), _ptr(out), _ptr(lse), _ptr(context_lens),
+                                       _ptr(block_tables), int(block_tables.shape[1]), B, Hq,
+                                       int(max_context_len), float(softmax_scale), int(num_splits),
+                                       _stream(stream)),
+           "kvp_decode_attn_noalloc")
     return out, lse
