@@ -44,7 +44,11 @@ WORKLOADS = {
     "rag_chunk_reuse": 3,
     "continuous_batching_step": 4,
     "long_context_prefix": 5,
+    # one request of the long-context shape in a 4096-block pool: a small case
+    # for detailed profiler captures of the same kernel
+    "long_context_prefix_b1": 5,
 }
+WORKLOAD_ARGS = {"long_context_prefix_b1": {"B": 1, "num_blocks": 4096}}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 512 << 20
 
@@ -211,7 +215,7 @@ def run_reference(args):
     world, rank, _ = dist_setup()
     if rank != 0:
         return 0
-    w = wl.make_config(WORKLOADS[args.workload])
+    w = wl.make_config(WORKLOADS[args.workload], **WORKLOAD_ARGS.get(args.workload, {}))
     flops = prefill_flops(w)
     per_step_budget = max(1.0, 60.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
@@ -268,7 +272,7 @@ def run_kvp(args):
     from paged_prefix_reuse_gb300.step import DeviceStep
 
     kvp.load_library()
-    w = wl.make_config(WORKLOADS[args.workload])
+    w = wl.make_config(WORKLOADS[args.workload], **WORKLOAD_ARGS.get(args.workload, {}))
     st = DeviceStep(w, device=dev, prefix_splits=args.prefix_splits, decode_splits=args.decode_splits)
     stream = torch.cuda.Stream(device=dev)
     flops = prefill_flops(w)
