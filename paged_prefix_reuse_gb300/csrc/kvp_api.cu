@@ -148,9 +148,9 @@ int32_t kvp_decode_num_splits(int32_t B, int32_t num_kv_heads, int32_t block_siz
 }
 
 size_t kvp_workspace_size(int32_t op, int32_t rows, int32_t num_q_heads, int32_t head_dim, int32_t num_splits) {
-    (void)op;
     if (num_splits <= 1 || rows <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
-    const size_t r = static_cast<size_t>(rows) * num_q_heads * num_splits;
+    const size_t parts = op == 1 ? static_cast<size_t>(decode_parts_per_split()) : 1;
+    const size_t r = static_cast<size_t>(rows) * num_q_heads * num_splits * parts;
     return align256(r * head_dim * sizeof(float)) + align256(r * sizeof(float));
 }
 
@@ -244,7 +244,7 @@ kvp_status kvp_prefix_attn(const kvp_pool* pool, const void* q, void* out, float
     if (e != cudaSuccess) return KVP_ERR_CUDA;
     if (splits > 1)
         e = launch_merge(p.ws_o, p.ws_lse, total_q * num_q_heads, num_q_heads, pool->head_dim, splits, pool->dtype,
-                         out, lse, total_q, nullptr, pool->block_size, 0, s);
+                         out, lse, total_q, nullptr, pool->block_size, 0, 1, s);
     return from_cuda(e);
 }
 
@@ -285,7 +285,7 @@ kvp_status kvp_decode_attn(const kvp_pool* pool, const void* q, void* out, float
     if (p.max_splits > 1) {
         const size_t need = kvp_workspace_size(1, B, num_q_heads, pool->head_dim, p.max_splits);
         if (!workspace || workspace_bytes < need || !aligned16(workspace)) return KVP_ERR_WORKSPACE;
-        const size_t r = static_cast<size_t>(B) * num_q_heads * p.max_splits;
+        const size_t r = static_cast<size_t>(B) * num_q_heads * p.max_splits * decode_parts_per_split();
         p.ws_o = static_cast<float*>(workspace);
         p.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(r * pool->head_dim * 4));
     }
@@ -297,7 +297,7 @@ kvp_status kvp_decode_attn(const kvp_pool* pool, const void* q, void* out, float
     if (e != cudaSuccess) return KVP_ERR_CUDA;
     if (p.max_splits > 1)
         e = launch_merge(p.ws_o, p.ws_lse, B * num_q_heads, num_q_heads, pool->head_dim, p.max_splits, pool->dtype,
-                         out, lse, B, context_lens, pool->block_size, p.pages_per_split, s);
+                         out, lse, B, context_lens, pool->block_size, p.pages_per_split, decode_parts_per_split(), s);
     return from_cuda(e);
 }
 

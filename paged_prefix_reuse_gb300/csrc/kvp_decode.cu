@@ -23,28 +23,29 @@
 namespace kvp {
 namespace {
 
-constexpr int kStageKeys = 32;
-constexpr int kConsumerWarps = 4;
+constexpr int kConsumerWarps = 2;
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
-constexpr int kRingBytes = 96 * 1024;
+constexpr int kRingSlots = 2 * kConsumerWarps;  // two slots per consumer warp: one computing, one loading
 
-template <int D>
+// SK keys per stage: 16 (one 16-token block) when blocks hold <= 16 tokens,
+// else 32 (one 32-token block).
+template <int D, int SK>
 struct DecodeCfg {
     static constexpr int CW = chunk_elems(D);
     static constexpr int ROWB = CW * 2;
     static constexpr int NCH = D / CW;
-    static constexpr int REGION = kStageKeys * ROWB;  // one chunk column of a stage's K (or V)
-    static constexpr int KBYTES = kStageKeys * D * 2;
+    static constexpr int REGION = SK * ROWB;  // one chunk column of a stage's K (or V)
+    static constexpr int KBYTES = SK * D * 2;
     static constexpr int STAGE_BYTES = 2 * KBYTES;
     // Stage i sits in slot i % NS and is consumed by warp i % 4.  NS is a
     // multiple of the consumer count, so every slot has one owner warp that
     // consumes its phases in order: a waiter can never be two phases behind,
     // which a parity wait could not tell apart from the phase it wants.
-    static constexpr int NS = kConsumerWarps * (kRingBytes / (kConsumerWarps * STAGE_BYTES));
-    static_assert(NS >= kConsumerWarps && NS % kConsumerWarps == 0, "ring depth");
-    static constexpr int RED_BYTES = kConsumerWarps * 16 * D * 4 + 2 * kConsumerWarps * 16 * 4;
-    static constexpr int SMEM_BYTES = NS * STAGE_BYTES + 2 * NS * 8 + 16 + 1024;
-    static_assert(RED_BYTES <= NS * STAGE_BYTES, "reduction area reuses the ring");
+    static constexpr int NS = kRingSlots;
+    static_assert(NS % kConsumerWarps == 0, "ring depth");
+    static constexpr int RED_BYTES = (D / 8) * 32 * 16 + 32 * 8;  // one warp's fragments + row stats
+    static constexpr int RING_BYTES = NS * STAGE_BYTES > RED_BYTES ? NS * STAGE_BYTES : RED_BYTES;
+    static constexpr int SMEM_BYTES = RING_BYTES + 2 * NS * 8 + 16 + 1024;
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -80,14 +81,15 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return p + (((a + 1023u) & ~1023u) - a);
 }
 
-template <bool kBF16, int D>
-__global__ void __launch_bounds__(kDecodeThreads, 2)
+template <bool kBF16, int D, int SK>
+__global__ void __launch_bounds__(kDecodeThreads, 4)
     decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                   const DecodeParams p) {
-    using C = DecodeCfg<D>;
+    using C = DecodeCfg<D, SK>;
+    constexpr int kStageKeys = SK;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::NS * C::STAGE_BYTES);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::RING_BYTES);
     uint64_t* empty = full + C::NS;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + C::NS);
 
@@ -217,14 +219,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
             }
             const uint32_t kbase = smem_u32(kst), vbase = smem_u32(vst);
 
-            // S = q K^T for 32 keys: 4 n-tiles of 8 keys.
-            float s[4][4];
+            // S = q K^T for SK keys: SK/8 n-tiles of 8 keys.
+            constexpr int NT = SK / 8;
+            float s[NT][4];
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+            for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
 #pragma unroll
-                for (int np = 0; np < 2; ++np) {
+                for (int np = 0; np < NT / 2; ++np) {
                     const uint32_t key = np * 16 + (lane & 7) + ((lane >> 4) << 3);
                     const uint32_t c16 = ks * 2 + ((lane >> 3) & 1);
                     const uint32_t addr = kbase + (c16 / (C::CW / 8)) * C::REGION +
@@ -237,7 +240,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
             }
             if (nvalid < kStageKeys) {
 #pragma unroll
-                for (int nt = 0; nt < 4; ++nt)
+                for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
                         if (nt * 8 + cq + (e & 1) >= nvalid) s[nt][e] = -INFINITY;
@@ -245,7 +248,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
             // Online softmax (log2 domain; the scale is folded into the exponent).
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
+            for (int nt = 0; nt < NT; ++nt) {
                 mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
                 mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
             }
@@ -261,7 +264,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
             m_run[1] = mn1;
             float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
+            for (int nt = 0; nt < NT; ++nt) {
                 s[nt][0] = fast_exp2(fmaf(s[nt][0], sl2, -mn0));
                 s[nt][1] = fast_exp2(fmaf(s[nt][1], sl2, -mn0));
                 s[nt][2] = fast_exp2(fmaf(s[nt][2], sl2, -mn1));
@@ -278,9 +281,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
                 o[nd][2] *= a1;
                 o[nd][3] *= a1;
             }
-            uint32_t pa[2][4];
+            uint32_t pa[SK / 16][4];
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
+            for (int kk = 0; kk < SK / 16; ++kk) {
                 pa[kk][0] = pack2<kBF16>(s[2 * kk][0], s[2 * kk][1]);
                 pa[kk][1] = pack2<kBF16>(s[2 * kk][2], s[2 * kk][3]);
                 pa[kk][2] = pack2<kBF16>(s[2 * kk + 1][0], s[2 * kk + 1][1]);
@@ -288,7 +291,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
             }
             // O += P V: V is [key][dim] in shared memory, loaded transposed.
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
+            for (int kk = 0; kk < SK / 16; ++kk) {
 #pragma unroll
                 for (int nd2 = 0; nd2 < D / 16; ++nd2) {
                     const uint32_t key = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
@@ -312,118 +315,186 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
         l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], 2);
     }
 
-    // ------------------- merge the four warps' states -------------------------
-    __syncthreads();  // every stage consumed and every copy landed: the ring is free
-    float* red_o = reinterpret_cast<float*>(smem);                   // [4][16][D]
-    float* red_m = red_o + kConsumerWarps * 16 * D;                  // [4][16]
-    float* red_l = red_m + kConsumerWarps * 16;                      // [4][16]
-    if (warp < kConsumerWarps) {
-        const int r0 = lane >> 2, r1 = r0 + 8, cq = 2 * (lane & 3);
-        float* wo = red_o + warp * 16 * D;
+    if (warp == kConsumerWarps) return;
+
+    // ------------------------------ epilogue ------------------------------
+    const int r0 = lane >> 2, r1 = r0 + 8, cq = 2 * (lane & 3);
+    if (p.max_splits > 1) {
+        if (*abort_flag) return;
+        // Each consumer warp writes its own partial (normalised O, log2 lse):
+        // part = split * kConsumerWarps + warp; merge_kernel combines them.
+        const int parts = p.max_splits * kConsumerWarps;
+        const int part = sp * kConsumerWarps + warp;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int r = half ? r1 : r0;
+            if (r >= g) continue;
+            const float lsum = l_run[half];
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            const int64_t row = static_cast<int64_t>(b) * p.num_q_heads + h * g + r;
+            float* dst = p.ws_o + (row * parts + part) * D;
+#pragma unroll
+            for (int nd = 0; nd < D / 8; ++nd)
+                *reinterpret_cast<float2*>(dst + nd * 8 + cq) =
+                    make_float2(o[nd][2 * half] * inv, o[nd][2 * half + 1] * inv);
+            if ((lane & 3) == 0)
+                p.ws_lse[row * parts + part] = lsum > 0.f ? m_run[half] + __log2f(lsum) : -INFINITY;
+        }
+        return;
+    }
+    // One split: combine the consumer warps through shared memory (all stages
+    // are consumed once both warps pass the barrier, so the ring is free).
+    float4* red = reinterpret_cast<float4*>(smem);                       // [D/8][32 lanes]
+    float2* stat = reinterpret_cast<float2*>(smem + (D / 8) * 32 * 16);  // [32 lanes] (m, l) x 2 rows
+    asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+    if (warp == 1) {
+#pragma unroll
+        for (int nd = 0; nd < D / 8; ++nd) red[nd * 32 + lane] = make_float4(o[nd][0], o[nd][1], o[nd][2], o[nd][3]);
+        stat[2 * lane] = make_float2(m_run[0], l_run[0]);
+        stat[2 * lane + 1] = make_float2(m_run[1], l_run[1]);
+    }
+    // Both consumer warps always reach both barriers (even after a timed-out
+    // wait), so neither can be left waiting for the other.
+    asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+    if (warp != 0 || *abort_flag) return;
+    float f0[2], f1[2], inv[2], lse2[2];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const float2 st1 = stat[2 * lane + half];
+        const float M = fmaxf(m_run[half], st1.x);
+        f0[half] = m_run[half] == -INFINITY ? 0.f : fast_exp2(m_run[half] - M);
+        f1[half] = st1.x == -INFINITY ? 0.f : fast_exp2(st1.x - M);
+        const float lsum = l_run[half] * f0[half] + st1.y * f1[half];
+        inv[half] = lsum > 0.f ? 1.f / lsum : 0.f;
+        lse2[half] = lsum > 0.f ? M + __log2f(lsum) : -INFINITY;
+    }
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int r = half ? r1 : r0;
+        if (r >= g) continue;
+        const int64_t row = static_cast<int64_t>(b) * p.num_q_heads + h * g + r;
+        uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(p.out) + row * D * 2);
 #pragma unroll
         for (int nd = 0; nd < D / 8; ++nd) {
-            wo[r0 * D + nd * 8 + cq] = o[nd][0];
-            wo[r0 * D + nd * 8 + cq + 1] = o[nd][1];
-            wo[r1 * D + nd * 8 + cq] = o[nd][2];
-            wo[r1 * D + nd * 8 + cq + 1] = o[nd][3];
+            const float4 w1 = red[nd * 32 + lane];
+            const float a0 = (o[nd][2 * half] * f0[half] + (half ? w1.z : w1.x) * f1[half]) * inv[half];
+            const float a1 = (o[nd][2 * half + 1] * f0[half] + (half ? w1.w : w1.y) * f1[half]) * inv[half];
+            dst[(nd * 8 + cq) / 2] = pack2<kBF16>(a0, a1);
         }
-        if ((lane & 3) == 0) {
-            red_m[warp * 16 + r0] = m_run[0];
-            red_m[warp * 16 + r1] = m_run[1];
-            red_l[warp * 16 + r0] = l_run[0];
-            red_l[warp * 16 + r1] = l_run[1];
-        }
-    }
-    __syncthreads();
-    if (warp < kConsumerWarps && !*abort_flag) {
-        for (int e = tid; e < g * D; e += kConsumerWarps * 32) {
-            const int r = e / D, c = e - (e / D) * D;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_m[w * 16 + r]);
-            float lsum = 0.f, acc = 0.f;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float mw = red_m[w * 16 + r];
-                const float f = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
-                lsum += red_l[w * 16 + r] * f;
-                acc += red_o[(w * 16 + r) * D + c] * f;
-            }
-            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-            const float lse2 = lsum > 0.f ? M + __log2f(lsum) : -INFINITY;
-            const int64_t row = static_cast<int64_t>(b) * p.num_q_heads + h * g + r;
-            if (p.max_splits == 1) {
-                if constexpr (kBF16)
-                    static_cast<__nv_bfloat16*>(p.out)[row * D + c] = __float2bfloat16_rn(acc * inv);
-                else
-                    static_cast<__half*>(p.out)[row * D + c] = __float2half_rn(acc * inv);
-                if (c == 0 && p.lse) p.lse[static_cast<int64_t>(h * g + r) * p.B + b] = lse2 * 0.69314718055994531f;
-            } else {
-                p.ws_o[(row * p.max_splits + sp) * D + c] = acc * inv;
-                if (c == 0) p.ws_lse[row * p.max_splits + sp] = lse2;
-            }
-        }
+        if ((lane & 3) == 0 && p.lse)
+            p.lse[static_cast<int64_t>(h * g + r) * p.B + b] = lse2[half] * 0.69314718055994531f;
     }
 }
 
-// One warp per output row: merge `splits` partials (normalised O, log2 lse).
-template <bool kBF16>
-__global__ void merge_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse, int32_t rows,
-                             int32_t Hq, int32_t D, int32_t max_splits, void* __restrict__ out,
-                             float* __restrict__ lse, int32_t lse_stride, const int32_t* __restrict__ ctx,
-                             int32_t block_size, int32_t pages_per_split) {
+// One warp per output row: merge `splits` partials (normalised O, log2 lse):
+//   lse = log2 sum_i 2^lse_i,  O = sum_i 2^(lse_i - lse) O_i.
+// Lane i computes the weight of split i (32 at a time); the weights are
+// broadcast by shuffle while each lane accumulates four adjacent columns with
+// 16-byte loads, so one split's partial is one coalesced 4*D-byte read.
+template <bool kBF16, int D>
+__global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
+                                                    int32_t rows, int32_t Hq, int32_t max_splits,
+                                                    void* __restrict__ out, float* __restrict__ lse,
+                                                    int32_t lse_stride, const int32_t* __restrict__ ctx,
+                                                    int32_t block_size, int32_t pages_per_split,
+                                                    int32_t parts_per_split) {
+    constexpr int V4 = D / 4;  // float4 columns per row: 16, 24 or 32
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (warp >= rows) return;
     const int64_t row = warp;
+    // max_splits * parts_per_split partials per row; a decode row has only
+    // its own sequence's splits.
     int splits = max_splits;
-    if (ctx) {  // decode: the sequence's own split count
+    if (ctx) {
         const int L = __ldg(ctx + row / Hq);
         const int np = (L + block_size - 1) / block_size;
         splits = max(0, min(max_splits, (np + pages_per_split - 1) / pages_per_split));
     }
+    splits *= parts_per_split;
+    max_splits *= parts_per_split;
+    const float* lrow = ws_lse + row * max_splits;
     float M = -INFINITY;
-    for (int i = lane; i < splits; i += 32) M = fmaxf(M, ws_lse[row * max_splits + i]);
+    for (int i = lane; i < splits; i += 32) M = fmaxf(M, __ldg(lrow + i));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float sum = 0.f;
     for (int i = lane; i < splits; i += 32) {
-        const float li = ws_lse[row * max_splits + i];
+        const float li = __ldg(lrow + i);
         sum += (li == -INFINITY) ? 0.f : fast_exp2(li - M);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     const float tot = (M == -INFINITY || sum <= 0.f) ? -INFINITY : M + __log2f(sum);
-    for (int c = lane; c < D; c += 32) {
-        float acc = 0.f;
-        if (tot != -INFINITY) {
-            for (int i = 0; i < splits; ++i) {
-                const float li = ws_lse[row * max_splits + i];
-                if (li != -INFINITY) acc += fast_exp2(li - tot) * ws_o[(row * max_splits + i) * D + c];
+
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4* orow = reinterpret_cast<const float4*>(ws_o + row * max_splits * D);
+    if (tot != -INFINITY) {
+        for (int base = 0; base < splits; base += 32) {
+            const int i = base + lane;
+            const float li = i < splits ? __ldg(lrow + i) : -INFINITY;
+            const float wi = (li == -INFINITY) ? 0.f : fast_exp2(li - tot);
+            const int n = min(32, splits - base);
+            int k = 0;
+            for (; k + 4 <= n; k += 4) {
+                float w[4];
+                float4 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    w[u] = __shfl_sync(0xffffffffu, wi, k + u);
+                    v[u] = lane < V4 ? __ldg(orow + static_cast<int64_t>(base + k + u) * V4 + lane)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    acc.x = fmaf(w[u], v[u].x, acc.x);
+                    acc.y = fmaf(w[u], v[u].y, acc.y);
+                    acc.z = fmaf(w[u], v[u].z, acc.z);
+                    acc.w = fmaf(w[u], v[u].w, acc.w);
+                }
+            }
+            for (; k < n; ++k) {
+                const float w0 = __shfl_sync(0xffffffffu, wi, k);
+                if (lane < V4) {
+                    const float4 v0 = __ldg(orow + static_cast<int64_t>(base + k) * V4 + lane);
+                    acc.x = fmaf(w0, v0.x, acc.x);
+                    acc.y = fmaf(w0, v0.y, acc.y);
+                    acc.z = fmaf(w0, v0.z, acc.z);
+                    acc.w = fmaf(w0, v0.w, acc.w);
+                }
             }
         }
-        if constexpr (kBF16)
-            static_cast<__nv_bfloat16*>(out)[row * D + c] = __float2bfloat16_rn(acc);
-        else
-            static_cast<__half*>(out)[row * D + c] = __float2half_rn(acc);
+    }
+    if (lane < V4) {
+        uint2 pk;
+        pk.x = pack2<kBF16>(acc.x, acc.y);
+        pk.y = pack2<kBF16>(acc.z, acc.w);
+        reinterpret_cast<uint2*>(static_cast<uint8_t*>(out) + row * D * 2)[lane] = pk;
     }
     if (lane == 0 && lse) lse[(row % Hq) * lse_stride + row / Hq] = tot * 0.69314718055994531f;
 }
 
-template <bool kBF16, int D>
+template <bool kBF16, int D, int SK>
 cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                             cudaStream_t stream) {
-    using C = DecodeCfg<D>;
+    using C = DecodeCfg<D, SK>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<kBF16, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::SMEM_BYTES);
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<kBF16, D, SK>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     dim3 grid(p.max_splits, p.pool.num_kv_heads, p.B);
-    decode_kernel<kBF16, D><<<grid, kDecodeThreads, C::SMEM_BYTES, stream>>>(tk, tv, p);
+    decode_kernel<kBF16, D, SK><<<grid, kDecodeThreads, C::SMEM_BYTES, stream>>>(tk, tv, p);
     return cudaGetLastError();
+}
+
+template <bool kBF16, int D>
+cudaError_t launch_decode_d(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                            cudaStream_t stream) {
+    return p.pool.block_size <= 16 ? launch_decode_t<kBF16, D, 16>(p, tk, tv, stream)
+                                   : launch_decode_t<kBF16, D, 32>(p, tk, tv, stream);
 }
 
 }  // namespace
@@ -432,28 +503,34 @@ cudaError_t launch_decode_attn(const DecodeParams& p, const CUtensorMap& tk, con
                                cudaStream_t stream) {
     const bool bf = p.pool.dtype == KVP_BF16;
     switch (p.pool.head_dim) {
-        case 64: return bf ? launch_decode_t<true, 64>(p, tk, tv, stream) : launch_decode_t<false, 64>(p, tk, tv, stream);
-        case 96: return bf ? launch_decode_t<true, 96>(p, tk, tv, stream) : launch_decode_t<false, 96>(p, tk, tv, stream);
-        case 128: return bf ? launch_decode_t<true, 128>(p, tk, tv, stream) : launch_decode_t<false, 128>(p, tk, tv, stream);
+        case 64: return bf ? launch_decode_d<true, 64>(p, tk, tv, stream) : launch_decode_d<false, 64>(p, tk, tv, stream);
+        case 96: return bf ? launch_decode_d<true, 96>(p, tk, tv, stream) : launch_decode_d<false, 96>(p, tk, tv, stream);
+        case 128: return bf ? launch_decode_d<true, 128>(p, tk, tv, stream) : launch_decode_d<false, 128>(p, tk, tv, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
+int decode_parts_per_split() { return kConsumerWarps; }
+
 cudaError_t launch_merge(const float* ws_o, const float* ws_lse, int32_t rows, int32_t num_q_heads,
                          int32_t head_dim, int32_t max_splits, int32_t dtype, void* out, float* lse,
                          int32_t lse_stride, const int32_t* context_lens, int32_t block_size,
-                         int32_t pages_per_split, cudaStream_t stream) {
+                         int32_t pages_per_split, int32_t parts_per_split, cudaStream_t stream) {
     if (rows <= 0) return cudaSuccess;
     const int threads = 256;
     const int blocks = (rows * 32 + threads - 1) / threads;
-    if (dtype == KVP_BF16)
-        merge_kernel<true><<<blocks, threads, 0, stream>>>(ws_o, ws_lse, rows, num_q_heads, head_dim, max_splits,
-                                                           out, lse, lse_stride, context_lens, block_size,
-                                                           pages_per_split);
-    else
-        merge_kernel<false><<<blocks, threads, 0, stream>>>(ws_o, ws_lse, rows, num_q_heads, head_dim,
-                                                            max_splits, out, lse, lse_stride, context_lens,
-                                                            block_size, pages_per_split);
+    const bool bf = dtype == KVP_BF16;
+#define KVP_MERGE(BF, DD)                                                                                      \
+    merge_kernel<BF, DD><<<blocks, threads, 0, stream>>>(ws_o, ws_lse, rows, num_q_heads, max_splits, out, lse, \
+                                                        lse_stride, context_lens, block_size, pages_per_split,     \
+                                                        parts_per_split)
+    switch (head_dim) {
+        case 64: if (bf) KVP_MERGE(true, 64); else KVP_MERGE(false, 64); break;
+        case 96: if (bf) KVP_MERGE(true, 96); else KVP_MERGE(false, 96); break;
+        case 128: if (bf) KVP_MERGE(true, 128); else KVP_MERGE(false, 128); break;
+        default: return cudaErrorInvalidValue;
+    }
+#undef KVP_MERGE
     return cudaGetLastError();
 }
 

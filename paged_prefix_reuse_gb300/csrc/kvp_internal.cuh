@@ -49,8 +49,8 @@ struct DecodeParams {
     int32_t pages_per_split;  // multiple of the pages in one stage
     int32_t max_splits;
     float scale_log2;
-    float* ws_o;    // [B * Hq][max_splits][head_dim]
-    float* ws_lse;  // [B * Hq][max_splits], log2 domain
+    float* ws_o;    // [B * Hq][max_splits * parts][head_dim]
+    float* ws_lse;  // [B * Hq][max_splits * parts], log2 domain
 };
 
 // Host-side launchers (defined in the kernel .cu files).
@@ -67,12 +67,15 @@ cudaError_t launch_prefix_attn(const PrefixParams& p, const CUtensorMap& tmap_k,
 int prefix_rows_per_cta();
 cudaError_t launch_decode_attn(const DecodeParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                cudaStream_t stream);
-// Merge of split partials: rows = total_q*Hq (prefix) or B*Hq (decode).
-// For decode, splits_of_row derives each row's split count from context_lens.
+// Merge of split partials: rows = total_q*Hq (prefix) or B*Hq (decode), with
+// max_splits * parts_per_split partials per row.  For decode, each row's
+// split count derives from its sequence's context length.
 cudaError_t launch_merge(const float* ws_o, const float* ws_lse, int32_t rows, int32_t num_q_heads,
                          int32_t head_dim, int32_t max_splits, int32_t dtype, void* out, float* lse,
                          int32_t lse_stride, const int32_t* context_lens, int32_t block_size,
-                         int32_t pages_per_split, cudaStream_t stream);
+                         int32_t pages_per_split, int32_t parts_per_split, cudaStream_t stream);
+// Partials one decode split writes (one per consumer warp).
+int decode_parts_per_split();
 
 // Swizzle chunk width (elements of one TMA box row) for a head dimension:
 // 64 elements (128-byte rows, 128B swizzle) when head_dim is a multiple of
