@@ -213,20 +213,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int qpos = valid ? P + token : L - 1;
 
             {  // Q tile wg -> swizzled shared memory (K-major A operand)
+                // All of this thread's 16-byte loads are issued before any store,
+                // so their latencies overlap instead of adding up.
                 constexpr int V16 = D / 8;
                 const uint4* q4 = static_cast<const uint4*>(p.q);
                 uint8_t* qt = smem + C::OFF_Q + wg * C::TILE_BYTES;
-                for (int e = row; e < kBM * V16; e += kBM) {
-                    const int rr = e / V16, c16 = e - (e / V16) * V16;
+                uint4 qv[V16];
+#pragma unroll
+                for (int k = 0; k < V16; ++k) {
+                    const int e = row + k * kBM;
+                    const int rr = e / V16, c16 = e % V16;
                     const int rgl = r0 + wg * kBM + rr;
-                    uint4 val = make_uint4(0, 0, 0, 0);
+                    qv[k] = make_uint4(0, 0, 0, 0);
                     if (rgl < rows_total) {
                         const int64_t qrow =
                             static_cast<int64_t>(cu0 + rgl / g) * p.num_q_heads + h * g + rgl % g;
-                        val = __ldg(q4 + qrow * V16 + c16);
+                        qv[k] = __ldg(q4 + qrow * V16 + c16);
                     }
-                    const int ch = c16 / (C::CW / 8), ci = c16 - ch * (C::CW / 8);
-                    *reinterpret_cast<uint4*>(qt + ch * C::CHUNK_BYTES + swz_offset(rr, ci, C::ROWB)) = val;
+                }
+#pragma unroll
+                for (int k = 0; k < V16; ++k) {
+                    const int e = row + k * kBM;
+                    const int rr = e / V16, c16 = e % V16;
+                    const int ch = c16 / (C::CW / 8), ci = c16 % (C::CW / 8);
+                    *reinterpret_cast<uint4*>(qt + ch * C::CHUNK_BYTES + swz_offset(rr, ci, C::ROWB)) = qv[k];
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&q_full[wg]);
@@ -319,8 +329,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float lse2 = l > 0.f ? m + __log2f(l) : -INFINITY;
                 const int64_t orow = static_cast<int64_t>(cu0 + token) * p.num_q_heads + head;
                 if (p.num_splits == 1) {
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + orow * D * 2);
-#pragma unroll
+                    // Stage the bf16/fp16 O tile in this warpgroup's Q region (the
+                    // last S_wg that read it has completed), then write whole rows
+                    // with coalesced 16-byte stores.  Row rr's 16-byte chunk c
+                    // sits at chunk position (c + rr) % (d/8) to spread banks.
+                    constexpr int V16 = D / 8;
+                    uint4* stg = reinterpret_cast<uint4*>(smem + C::OFF_Q + wg * C::TILE_BYTES);
+#pragma unroll 1
                     for (int cb = 0; cb < D / 16; ++cb) {
                         uint32_t r[16];
                         tmem_ld16_sync(lane_base + ocol + 16 * cb, r);
@@ -333,13 +348,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                         a1.y = pack2<kBF16>(__uint_as_float(r[10]) * inv, __uint_as_float(r[11]) * inv);
                         a1.z = pack2<kBF16>(__uint_as_float(r[12]) * inv, __uint_as_float(r[13]) * inv);
                         a1.w = pack2<kBF16>(__uint_as_float(r[14]) * inv, __uint_as_float(r[15]) * inv);
-                        if (valid) {
-                            dst[2 * cb] = a0;
-                            dst[2 * cb + 1] = a1;
-                        }
+                        stg[row * V16 + (2 * cb + row) % V16] = a0;
+                        stg[row * V16 + (2 * cb + 1 + row) % V16] = a1;
                     }
                     if (valid && p.lse)
                         p.lse[static_cast<int64_t>(head) * p.total_q + cu0 + token] = lse2 * 0.69314718055994531f;
+                    // Named barrier over this warpgroup's 128 threads (ids 1 and 2).
+                    if (wg == 0)
+                        asm volatile("bar.sync 1, 128;" ::: "memory");
+                    else
+                        asm volatile("bar.sync 2, 128;" ::: "memory");
+                    uint8_t* out_b = static_cast<uint8_t*>(p.out);
+#pragma unroll 1
+                    for (int e = row; e < kBM * V16; e += kBM) {
+                        const int rr = e / V16, c = e % V16;
+                        const int rgl = r0 + wg * kBM + rr;
+                        if (rgl < rows_total) {
+                            const int64_t grow =
+                                static_cast<int64_t>(cu0 + rgl / g) * p.num_q_heads + h * g + rgl % g;
+                            reinterpret_cast<uint4*>(out_b + grow * D * 2)[c] = stg[rr * V16 + (c + rr) % V16];
+                        }
+                    }
                 } else {
                     float* dst = p.ws_o + (orow * p.num_splits + split) * D;
 #pragma unroll
