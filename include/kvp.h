@@ -112,7 +112,7 @@ kvp_status kvp_cache_append(const kvp_pool *pool, const void *k_new, const void 
  * pairs: device int32 [n][2] = (src, dst).  Destinations must be distinct
  * and no destination may also be a source in the same call; otherwise the
  * result is undefined.  A pair naming a block outside the pool is skipped
- * and sets KVP_DEVERR_BAD_PAIR.  n == 0 is a no-op. */
+ * and sets KVP_DEVERR_BAD_PAIR.  n == 0 is a no-op; n <= 65535 per call. */
 kvp_status kvp_block_copy(const kvp_pool *pool, const int32_t *pairs, int32_t n, void *stream);
 
 /* Causal attention of a chunk of new tokens over the cached prefix plus the

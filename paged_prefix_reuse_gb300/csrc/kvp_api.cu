@@ -181,7 +181,7 @@ kvp_status kvp_cache_append(const kvp_pool* pool, const void* k_new, const void*
 kvp_status kvp_block_copy(const kvp_pool* pool, const int32_t* pairs, int32_t n, void* stream) {
     kvp_status st = check_pool(pool);
     if (st != KVP_OK) return st;
-    if (n < 0) return KVP_ERR_INVALID_ARG;
+    if (n < 0 || n > 65535) return KVP_ERR_INVALID_ARG;
     if (n == 0) return KVP_OK;
     if (!pairs) return KVP_ERR_INVALID_ARG;
     return from_cuda(

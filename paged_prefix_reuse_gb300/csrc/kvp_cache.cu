@@ -60,56 +60,92 @@ __global__ void slot_mapping_kernel(PoolView pool, const int32_t* __restrict__ c
     }
 }
 
-// One thread per 16-byte vector of a (token, kv head) row, K and V together.
-__global__ void append_kernel(PoolView pool, uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
-                              const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
-                              const int64_t* __restrict__ slots, int32_t T) {
-    const int vec_per_head = pool.head_dim / 8;  // 16-byte vectors of 8 x 16-bit
-    const int64_t vec_per_tok = static_cast<int64_t>(pool.num_kv_heads) * vec_per_head;
-    const int64_t total = vec_per_tok * T;
+// Append.  A token's K (and V) rows for all kv heads are vpt = Hkv * d / 8
+// 16-byte vectors.  A 256-thread block covers tpb = max(1, 256 / vpt) tokens
+// per step; thread i owns vector i % vpt of token i / vpt (computed once, in
+// 32-bit arithmetic) and walks tokens with a grid stride, keeping kUnroll
+// tokens' loads in flight before their stores.
+constexpr int kUnroll = 4;
+
+__global__ void __launch_bounds__(kThreads) append_kernel(PoolView pool, uint4* __restrict__ k_pool,
+                                                          uint4* __restrict__ v_pool, const uint4* __restrict__ k_new,
+                                                          const uint4* __restrict__ v_new,
+                                                          const int64_t* __restrict__ slots, int32_t T, int32_t vpt,
+                                                          int32_t tpb) {
+    const int vph = pool.head_dim / 8;  // vectors per (token, head)
     const int64_t num_slots = pool.num_blocks * pool.block_size;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < total; v += stride) {
-        const int64_t t = v / vec_per_tok;
-        const int64_t rem = v - t * vec_per_tok;
-        const int64_t slot = __ldg(slots + t);
-        if (slot == -1) continue;
-        if (slot < 0 || slot >= num_slots) {
-            if (rem == 0) report(pool.err_word, KVP_DEVERR_BAD_SLOT);
-            continue;
+    const bool wide = vpt >= kThreads;          // one token per step, several vectors per thread
+    const int span = wide ? vpt : tpb * vpt;    // vector positions a block covers per step (<= 256 if !wide)
+    for (int j0 = threadIdx.x; j0 < span; j0 += kThreads) {
+        const int tok_local = wide ? 0 : j0 / vpt;
+        const int j = j0 - tok_local * vpt;
+        const int h = j / vph, c = j - h * vph;
+        const int64_t step = static_cast<int64_t>(gridDim.x) * tpb;
+        for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * tpb + tok_local; t0 < T; t0 += step * kUnroll) {
+            uint4 kv[kUnroll], vv[kUnroll];
+            int64_t dst[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int64_t t = t0 + u * step;
+                dst[u] = -1;
+                if (t < T) {
+                    const int64_t slot = __ldg(slots + t);
+                    if (slot >= 0 && slot < num_slots) {
+                        const int64_t blk = slot / pool.block_size;
+                        const int64_t row = slot - blk * pool.block_size;
+                        dst[u] = ((blk * pool.num_kv_heads + h) * pool.block_size + row) * vph + c;
+                        kv[u] = __ldcs(k_new + t * vpt + j);
+                        vv[u] = __ldcs(v_new + t * vpt + j);
+                    } else if (slot != -1 && j == 0) {
+                        report(pool.err_word, KVP_DEVERR_BAD_SLOT);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                if (dst[u] >= 0) {
+                    k_pool[dst[u]] = kv[u];
+                    v_pool[dst[u]] = vv[u];
+                }
+            }
         }
-        const int64_t h = rem / vec_per_head;
-        const int64_t c = rem - h * vec_per_head;
-        const int64_t blk = slot / pool.block_size;
-        const int64_t row = slot - blk * pool.block_size;
-        const int64_t dst = ((blk * pool.num_kv_heads + h) * pool.block_size + row) * vec_per_head + c;
-        const uint4 kv = __ldcs(k_new + v);
-        const uint4 vv = __ldcs(v_new + v);
-        k_pool[dst] = kv;
-        v_pool[dst] = vv;
     }
 }
 
-// One thread per 16-byte vector of a whole block (all heads), K and V together.
-__global__ void block_copy_kernel(PoolView pool, uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
-                                  const int32_t* __restrict__ pairs, int32_t n) {
-    const int64_t vec_per_block =
-        static_cast<int64_t>(pool.num_kv_heads) * pool.block_size * (pool.head_dim / 8);
-    const int64_t total = vec_per_block * n;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < total; v += stride) {
-        const int64_t i = v / vec_per_block;
-        const int64_t e = v - i * vec_per_block;
-        const int64_t src = __ldg(pairs + 2 * i);
-        const int64_t dst = __ldg(pairs + 2 * i + 1);
-        if (src < 0 || src >= pool.num_blocks || dst < 0 || dst >= pool.num_blocks) {
-            if (e == 0) report(pool.err_word, KVP_DEVERR_BAD_PAIR);
-            continue;
-        }
-        const uint4 kv = k_pool[src * vec_per_block + e];
-        const uint4 vv = v_pool[src * vec_per_block + e];
-        k_pool[dst * vec_per_block + e] = kv;
-        v_pool[dst * vec_per_block + e] = vv;
+// Copy-on-write copy.  A block of one pool is vpb = Hkv * bs * d / 8 16-byte
+// vectors; blockIdx.y picks the pair and blockIdx.x a 512-vector chunk of
+// it, each thread copying two vectors of K and two of V.
+__global__ void __launch_bounds__(kThreads) block_copy_kernel(PoolView pool, uint4* __restrict__ k_pool,
+                                                              uint4* __restrict__ v_pool,
+                                                              const int32_t* __restrict__ pairs, int32_t vpb) {
+    const int i = blockIdx.y;
+    const int64_t src = __ldg(pairs + 2 * i);
+    const int64_t dst = __ldg(pairs + 2 * i + 1);
+    if (src < 0 || src >= pool.num_blocks || dst < 0 || dst >= pool.num_blocks) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) report(pool.err_word, KVP_DEVERR_BAD_PAIR);
+        return;
+    }
+    const int e0 = blockIdx.x * 2 * kThreads + threadIdx.x, e1 = e0 + kThreads;
+    const uint4* ks = k_pool + src * vpb;
+    const uint4* vs = v_pool + src * vpb;
+    uint4* kd = k_pool + dst * vpb;
+    uint4* vd = v_pool + dst * vpb;
+    uint4 k0, v0, k1, v1;
+    if (e0 < vpb) {
+        k0 = ks[e0];
+        v0 = vs[e0];
+    }
+    if (e1 < vpb) {
+        k1 = ks[e1];
+        v1 = vs[e1];
+    }
+    if (e0 < vpb) {
+        kd[e0] = k0;
+        vd[e0] = v0;
+    }
+    if (e1 < vpb) {
+        kd[e1] = k1;
+        vd[e1] = v1;
     }
 }
 
@@ -127,20 +163,25 @@ cudaError_t launch_slot_mapping(const PoolView& pool, const int32_t* cu_seqlens_
 cudaError_t launch_cache_append(const PoolView& pool, void* k_pool, void* v_pool, const void* k_new,
                                 const void* v_new, const int64_t* slot_mapping, int32_t T, cudaStream_t stream) {
     if (T <= 0) return cudaSuccess;
-    const int64_t total = static_cast<int64_t>(T) * pool.num_kv_heads * (pool.head_dim / 8);
-    append_kernel<<<grid_for(total, kThreads), kThreads, 0, stream>>>(
+    const int32_t vpt = pool.num_kv_heads * (pool.head_dim / 8);
+    const int32_t tpb = vpt >= kThreads ? 1 : kThreads / vpt;
+    const int64_t steps = (static_cast<int64_t>(T) + tpb - 1) / tpb;
+    // One step per block when there are few; a block loops (kUnroll steps per
+    // pass) only once the steps outnumber the blocks the GPU holds.
+    append_kernel<<<grid_for(steps, 1), kThreads, 0, stream>>>(
         pool, static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), static_cast<const uint4*>(k_new),
-        static_cast<const uint4*>(v_new), slot_mapping, T);
+        static_cast<const uint4*>(v_new), slot_mapping, T, vpt, tpb);
     return cudaGetLastError();
 }
 
 cudaError_t launch_block_copy(const PoolView& pool, void* k_pool, void* v_pool, const int32_t* pairs, int32_t n,
                               cudaStream_t stream) {
     if (n <= 0) return cudaSuccess;
-    const int64_t total =
-        static_cast<int64_t>(n) * pool.num_kv_heads * pool.block_size * (pool.head_dim / 8);
-    block_copy_kernel<<<grid_for(total, kThreads), kThreads, 0, stream>>>(
-        pool, static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), pairs, n);
+    const int32_t vpb = pool.num_kv_heads * pool.block_size * (pool.head_dim / 8);
+    if (n > 65535) return cudaErrorInvalidValue;
+    const dim3 grid((vpb + 2 * kThreads - 1) / (2 * kThreads), n);
+    block_copy_kernel<<<grid, kThreads, 0, stream>>>(pool, static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool),
+                                                     pairs, vpb);
     return cudaGetLastError();
 }
 
