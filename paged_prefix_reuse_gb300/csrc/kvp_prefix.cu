@@ -463,32 +463,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             return mbar_wait(&slot_full[gl % C::NSLOT], (gl / C::NSLOT) & 1, abort_flag, err);
         };
         auto release = [&](int gl) {
-            if (lane == 0) tc_commit(&slot_empty[gl % C::NSLOT]);
+            tc_commit(&slot_empty[gl % C::NSLOT]);
             last_bar = &slot_empty[gl % C::NSLOT];
             last_par = (gl / C::NSLOT) & 1;
         };
+        // The whole warp runs these (the MMA and commit wrappers elect one lane).
         auto issue_s = [&](int i, uint32_t kbase) {
-            if (lane == 0) {
-                const uint32_t qb = i ? qb1 : qb0;
+            const uint32_t qb = i ? qb1 : qb0;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = ((kk * 16) / C::CW) * C::CHUNK_BYTES + ((kk * 16) % C::CW) * 2;
-                    const uint64_t ad = smem_desc(qb + off, 16, 8 * C::ROWB, C::SWZ);
-                    const uint64_t bd = smem_desc(kbase + off, 16, 8 * C::ROWB, C::SWZ);
-                    tc_mma_ss(tmem + (i ? C::S_COL1 : C::S_COL0), ad, bd, idesc_s, kk > 0 ? 1u : 0u);
-                }
-                tc_commit(&s_full[i]);
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = ((kk * 16) / C::CW) * C::CHUNK_BYTES + ((kk * 16) % C::CW) * 2;
+                const uint64_t ad = smem_desc(qb + off, 16, 8 * C::ROWB, C::SWZ);
+                const uint64_t bd = smem_desc(kbase + off, 16, 8 * C::ROWB, C::SWZ);
+                tc_mma_ss(tmem + (i ? C::S_COL1 : C::S_COL0), ad, bd, idesc_s, kk > 0 ? 1u : 0u);
             }
+            tc_commit(&s_full[i]);
         };
         auto issue_pv = [&](int i, uint32_t vbase, bool accumulate) {
-            if (lane == 0) {
-                const uint32_t scol = i ? C::S_COL1 : C::S_COL0;
+            const uint32_t scol = i ? C::S_COL1 : C::S_COL0;
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint64_t bd = smem_desc(vbase + kk * 16 * C::ROWB, C::CHUNK_BYTES, 8 * C::ROWB, C::SWZ);
-                    tc_mma_ts(tmem + (i ? C::O_COL1 : C::O_COL0), tmem + scol + kk * 8, bd, idesc_o,
-                              (accumulate || kk > 0) ? 1u : 0u);
-                }
+            for (int kk = 0; kk < kBN / 16; ++kk) {
+                const uint64_t bd = smem_desc(vbase + kk * 16 * C::ROWB, C::CHUNK_BYTES, 8 * C::ROWB, C::SWZ);
+                tc_mma_ts(tmem + (i ? C::O_COL1 : C::O_COL0), tmem + scol + kk * 8, bd, idesc_o,
+                          (accumulate || kk > 0) ? 1u : 0u);
             }
         };
 
@@ -527,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(&p_full[0], jj & 1, abort_flag, err)) { ok = false; break; }
             tc_fence_after();
             issue_pv(0, slot_addr(gv), jj > 0);
-            if (!more && lane == 0) tc_commit(&o_done[0]);
+            if (!more) tc_commit(&o_done[0]);
             if (more) {
                 if (!wait_slot(gk)) { ok = false; break; }
                 tc_fence_after();
@@ -538,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(&p_full[1], jj & 1, abort_flag, err)) { ok = false; break; }
                 tc_fence_after();
                 issue_pv(1, slot_addr(gv), jj > 0);
-                if (!more && lane == 0) tc_commit(&o_done[1]);
+                if (!more) tc_commit(&o_done[1]);
             }
             release(gv);
             if (more) {
