@@ -147,12 +147,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = p.group, BS = p.pool.block_size, Hkv = p.pool.num_kv_heads;
     uint32_t* err = p.pool.err_word;
 
+    // All three metadata loads before the first branch: one memory round trip.
     const int cu0 = __ldg(p.cu_seqlens_q + s);
-    const int N = __ldg(p.cu_seqlens_q + s + 1) - cu0;
+    const int cu1 = __ldg(p.cu_seqlens_q + s + 1);
+    const int L = __ldg(p.context_lens + s);
+    const int N = cu1 - cu0;
     const int rows_total = N * g;
     const int r0 = ct * kRowsPerCta;
     if (r0 >= rows_total) return;
-    const int L = __ldg(p.context_lens + s);
     const int P = L - N;
     const int npages = (L + BS - 1) / BS;
     if (P < 0 || npages > p.max_blocks) {

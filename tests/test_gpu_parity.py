@@ -95,6 +95,12 @@ SMALL = {
     "block32_d96_bf16": lambda: wl.make_random(43, [300, 5], [40, 100], Hq=6, Hkv=3, d=96, dtype="bf16", bs=32),
     "zero_new_tokens": lambda: wl.make_random(44, [50, 20, 70], [30, 0, 17], Hq=2, Hkv=1, d=64, dtype="f16"),
     "gqa16_d128": lambda: wl.make_random(45, [260], [20], Hq=16, Hkv=1, d=128, dtype="bf16"),
+    # logits with std ~6: row maxima jump by more than 2^8 between tiles and
+    # between the two 64-key halves of a tile (the rescaling paths)
+    "large_logits_bf16": lambda: wl.make_random(46, [300, 0], [200, 150], Hq=4, Hkv=2, d=128, dtype="bf16",
+                                                q_std=6.0),
+    "large_logits_f16_d64": lambda: wl.make_random(47, [520, 33], [90, 260], Hq=6, Hkv=3, d=64, dtype="f16",
+                                                   q_std=6.0),
 }
 
 
