@@ -102,14 +102,31 @@ def _peak_value(peaks, *keys):
     return None
 
 
+# Workloads too large for a full ncu capture under the size rule take their
+# DRAM traffic from a smaller capture of the same kernel, scaled by the units
+# processed: long_context_prefix is four independent copies of the B=1 case
+# (own block tables, Q and O), so its traffic is four times B=1's.
+TRAFFIC_PROXY = {"long_context_prefix": ("long_context_prefix_b1", 4.0)}
+
+
 def committed_traffic(kernel: str, workload: str):
+    if workload in TRAFFIC_PROXY:
+        proxy, factor = TRAFFIC_PROXY[workload]
+        t = _committed_traffic(kernel, proxy)
+        return None if t is None else t * factor
+    return _committed_traffic(kernel, workload)
+
+
+def _committed_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if that summary
-    was taken on the kernel source as it is now (else None)."""
+    was taken on the kernel source as it is now -- the kernel's .cu file and
+    the shared kvp_internal.cuh, hashed together -- else None."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
-    src = os.path.join(ROOT, "paged_prefix_reuse_gb300", "csrc", f"kvp_{kernel}.cu")
-    if not (os.path.exists(path) and os.path.exists(src)):
+    csrc = os.path.join(ROOT, "paged_prefix_reuse_gb300", "csrc")
+    srcs = [os.path.join(csrc, f"kvp_{kernel}.cu"), os.path.join(csrc, "kvp_internal.cuh")]
+    if not (os.path.exists(path) and all(os.path.exists(f) for f in srcs)):
         return None
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    digest = hashlib.sha256(b"".join(open(f, "rb").read() for f in srcs)).hexdigest()[:16]
     vals = {}
     for line in open(path):
         if ":" in line:
