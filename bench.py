@@ -516,6 +516,77 @@ def run_kvp(args):
     return 0
 
 
+def run_swap(args):
+    """Host <-> device block swap: move N scattered pages (K and V) of the
+    mixed-batch pool to a pinned host page pool and back, through the C ABI.
+    The denominator is one contiguous pinned copy of the same bytes
+    (cudaMemcpyAsync through torch), measured in the same run: the host
+    link's practical rate."""
+    import numpy as np
+    import torch
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    from paged_prefix_reuse_gb300 import build as kvp_build
+
+    kvp_build.build_library()
+    import paged_prefix_reuse_gb300 as kvp
+    from paged_prefix_reuse_gb300.step import DeviceStep
+
+    kvp.load_library()
+    w = wl.make_config(4)
+    st = DeviceStep(w, device=dev)
+    pool = st.pool
+    n = min(1024, pool.num_blocks)
+    host = kvp.HostKVPool.like(pool, n)
+    rng = np.random.default_rng(0)
+    src = rng.choice(pool.num_blocks, size=n, replace=False)
+    out_pairs = torch.from_numpy(np.stack([src, np.arange(n)], 1).astype(np.int32)).to(dev)
+    in_pairs = torch.from_numpy(np.stack([np.arange(n), src], 1).astype(np.int32)).to(dev)
+    page_bytes = 2 * pool.num_kv_heads * pool.block_size * pool.head_dim * pool.k.element_size()
+    moved = n * page_bytes
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    dbuf = torch.empty(moved, dtype=torch.uint8, device=dev)
+    hbuf = torch.empty(moved, dtype=torch.uint8, pin_memory=True)
+
+    def timed(fn):
+        ts = []
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup + args.steps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                e1.synchronize()
+                if i >= args.warmup:
+                    ts.append(e0.elapsed_time(e1) / 1e3)
+        return sorted(ts)[len(ts) // 2]
+
+    t_out = timed(lambda: kvp.kvp_block_swap(pool, host, out_pairs, kvp.HostKVPool.SWAP_OUT, stream=stream))
+    t_in = timed(lambda: kvp.kvp_block_swap(pool, host, in_pairs, kvp.HostKVPool.SWAP_IN, stream=stream))
+    t_d2h = timed(lambda: hbuf.copy_(dbuf, non_blocking=True))
+    t_h2d = timed(lambda: dbuf.copy_(hbuf, non_blocking=True))
+    gbs = lambda t: moved / t / 1e9
+    value = 2 * moved / (t_out + t_in) / 1e9
+    peak = 2 * moved / (t_d2h + t_h2d) / 1e9
+    line = {
+        "metric": "block swap GB/s (scattered K+V pages, GPU pool to pinned host pool and back)",
+        "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": (t_out + t_in) * 1e3, "higher_is_better": True, "op": "block_swap",
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "continuous_batching_step pool", "pages": n, "page_bytes": page_bytes,
+                   "bytes_each_way": moved, "l2": "flushed before every timed call"},
+        "out_gbs": gbs(t_out), "in_gbs": gbs(t_in), "gpu_launches": 2,
+        "roofline": {"bound": "host link", "achieved": value, "peak": peak, "unit": "GB/s", "frac": value / peak,
+                     "peak_source": "one contiguous pinned cudaMemcpyAsync of the same bytes each way, this run",
+                     "memcpy_d2h_gbs": gbs(t_d2h), "memcpy_h2d_gbs": gbs(t_h2d), "traffic": None},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -528,9 +599,13 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--preroll-s", type=float, default=0.4)
+    ap.add_argument("--op", choices=["step", "block_swap"], default="step",
+                    help="step: the prefill/decode step (default); block_swap: host <-> device page swap")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.op == "block_swap":
+        return run_swap(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_kvp(args)

@@ -115,6 +115,40 @@ kvp_status kvp_cache_append(const kvp_pool *pool, const void *k_new, const void 
  * and sets KVP_DEVERR_BAD_PAIR.  n == 0 is a no-op; n <= 65535 per call. */
 kvp_status kvp_block_copy(const kvp_pool *pool, const int32_t *pairs, int32_t n, void *stream);
 
+/* A pool of blocks in host memory with the same block geometry (num_kv_heads,
+ * block_size, head_dim, dtype) as a device pool: the swap buffer of
+ * preempted sequences.  k_pool, v_pool: host [num_blocks][Hkv][bs][d],
+ * 16-byte aligned, page-locked and mapped into the device's address space
+ * (cudaHostAlloc / cudaMallocHost memory on a unified-address system, or
+ * cudaHostRegister'ed memory).  Caller-owned; the library keeps no state. */
+typedef struct kvp_host_pool {
+    void *k_pool;
+    void *v_pool;
+    int64_t num_blocks;
+} kvp_host_pool;
+
+enum { KVP_SWAP_OUT = 0, KVP_SWAP_IN = 1 };
+
+/* Swap whole blocks between the device pool and the host pool (kvstream
+ * "Features": low-priority sequences are spilled to a CPU page pool rather
+ * than dropped, and its configuration sizes that pool in num_cpu_blocks with
+ * preemption_policy "swap"; the kvboost post on CPU paging: KV blocks that
+ * do not fit on the GPU move to system RAM by asynchronous DMA).
+ *     direction KVP_SWAP_OUT: host.k_pool[pairs[i][1]] = pool.k_pool[pairs[i][0]]
+ *     direction KVP_SWAP_IN:  pool.k_pool[pairs[i][1]] = host.k_pool[pairs[i][0]]
+ * (whole block, all heads; same for V).  One kernel moves every pair, reading
+ * or writing the host pool directly over the host link, so a list of
+ * scattered blocks costs one launch, asynchronous on `stream` (a copy stream
+ * lets it overlap compute on another).  pairs: device int32 [n][2] =
+ * (src, dst), block ids of the source and destination pool.  Destinations
+ * must be distinct; otherwise the result is undefined.  A pair naming a block
+ * outside its pool is skipped and sets KVP_DEVERR_BAD_PAIR in the device
+ * pool's err_word.  n == 0 is a no-op; n <= 65535 per call.  Errors:
+ * KVP_ERR_INVALID_ARG for a null or misaligned pointer, a negative block
+ * count or an unknown direction; no device work is queued then. */
+kvp_status kvp_block_swap(const kvp_pool *pool, const kvp_host_pool *host, const int32_t *pairs, int32_t n,
+                          int32_t direction, void *stream);
+
 /* Causal attention of a chunk of new tokens over the cached prefix plus the
  * chunk itself (kvboost "How it works" step 5 and "Flash Attention (CUDA)":
  * tiled online softmax, fp16/bf16, head_dim 64/96/128, any length, causal

@@ -129,6 +129,26 @@ def block_copy(k_pool, v_pool, pairs):
     return kp, vp, int(bad)
 
 
+def block_swap(src_k, src_v, dst_k, dst_v, pairs):
+    """Swap between a device pool and a host page pool (kvstream "Features":
+    low-priority sequences spill to a CPU page pool; kvboost's CPU paging:
+    blocks that do not fit on the GPU move to system RAM).  For each
+    (src, dst) pair in order, dst_pool[dst] = src_pool[src], whole block, K
+    and V; a pair naming a block outside its pool is skipped and counted.
+    Returns (dst_k', dst_v', n_invalid)."""
+    dk = np.array(dst_k, copy=True)
+    dv = np.array(dst_v, copy=True)
+    pr = np.asarray(pairs, dtype=np.int64).reshape(-1, 2)
+    bad = 0
+    for src, dst in pr:
+        if not (0 <= src < src_k.shape[0] and 0 <= dst < dk.shape[0]):
+            bad += 1
+            continue
+        dk[dst] = src_k[src]
+        dv[dst] = src_v[src]
+    return dk, dv, bad
+
+
 def prefix_attn(dtype, k_pool, v_pool, q, cu_seqlens_q, context_lens, block_tables, scale, rows=None):
     """Causal attention of every new token over its sequence's logical K/V.
 

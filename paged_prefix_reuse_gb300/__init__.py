@@ -9,7 +9,7 @@ raises ``KvpLibraryMissing``.
 
 Functions carry the names of the C entry points declared in
 ``include/kvp.h``: ``kvp_slot_mapping``, ``kvp_cache_append``,
-``kvp_block_copy``, ``kvp_prefix_attn``, ``kvp_decode_attn`` and
+``kvp_block_copy``, ``kvp_block_swap``, ``kvp_prefix_attn``, ``kvp_decode_attn`` and
 ``kvp_workspace_size`` (plus the split-count helpers).
 """
 from __future__ import annotations
@@ -24,12 +24,14 @@ __all__ = [
     "KvpError",
     "KvpLibraryMissing",
     "PagedKVPool",
+    "HostKVPool",
     "EXPORTED_SYMBOLS",
     "lib_path",
     "load_library",
     "kvp_slot_mapping",
     "kvp_cache_append",
     "kvp_block_copy",
+    "kvp_block_swap",
     "kvp_prefix_attn",
     "kvp_decode_attn",
     "kvp_decode_attn_noalloc",
@@ -54,6 +56,7 @@ EXPORTED_SYMBOLS = (
     "kvp_slot_mapping",
     "kvp_cache_append",
     "kvp_block_copy",
+    "kvp_block_swap",
     "kvp_prefix_attn",
     "kvp_decode_attn",
     "kvp_decode_attn_noalloc",
@@ -73,6 +76,10 @@ class KvpError(RuntimeError):
 
 class KvpLibraryMissing(RuntimeError):
     pass
+
+
+class _HostPool(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("num_blocks", ctypes.c_int64)]
 
 
 class _Pool(ctypes.Structure):
@@ -112,11 +119,12 @@ def load_library():
         lib.kvp_slot_mapping.argtypes = [PP, P, P, P, i32, i32, i32, P, P]
         lib.kvp_cache_append.argtypes = [PP, P, P, P, i32, P]
         lib.kvp_block_copy.argtypes = [PP, P, i32, P]
+        lib.kvp_block_swap.argtypes = [PP, ctypes.POINTER(_HostPool), P, i32, i32, P]
         lib.kvp_prefix_attn.argtypes = [PP, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, i32, P, sz, P]
         lib.kvp_decode_attn.argtypes = [PP, P, P, P, P, P, i32, i32, i32, i32, f32, i32, P, sz, P]
         lib.kvp_decode_attn_noalloc.argtypes = [PP, P, P, P, P, P, i32, i32, i32, i32, f32, i32, P]
-        for name in ("kvp_slot_mapping", "kvp_cache_append", "kvp_block_copy", "kvp_prefix_attn", "kvp_decode_attn",
-                     "kvp_decode_attn_noalloc"):
+        for name in ("kvp_slot_mapping", "kvp_cache_append", "kvp_block_copy", "kvp_block_swap", "kvp_prefix_attn",
+                     "kvp_decode_attn", "kvp_decode_attn_noalloc"):
             getattr(lib, name).restype = ctypes.c_int
         lib.kvp_prefix_num_splits.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.kvp_prefix_num_splits.restype = i32
@@ -205,6 +213,53 @@ class PagedKVPool:
 
     def clear_errors(self) -> None:
         self.err_word.zero_()
+
+
+class HostKVPool:
+    """The swap buffer: k/v tensors [num_blocks, Hkv, block_size, d] in pinned
+    host memory, with the block geometry and dtype of a device pool.
+
+    Pinned (page-locked) host memory is mapped into the device's address
+    space on a unified-address system, which is what ``kvp_block_swap``
+    reads and writes.
+    """
+
+    SWAP_OUT, SWAP_IN = 0, 1
+
+    def __init__(self, k_pool: torch.Tensor, v_pool: torch.Tensor):
+        if k_pool.shape != v_pool.shape or k_pool.dtype != v_pool.dtype or k_pool.dim() != 4:
+            raise ValueError("k_pool and v_pool must be [num_blocks, Hkv, block_size, head_dim] of one dtype")
+        if k_pool.is_cuda or v_pool.is_cuda or not (k_pool.is_pinned() and v_pool.is_pinned()):
+            raise ValueError("a host pool must be pinned host memory")
+        if not (k_pool.is_contiguous() and v_pool.is_contiguous()):
+            raise ValueError("host pool tensors must be contiguous")
+        self.k, self.v = k_pool, v_pool
+        self.num_blocks = int(k_pool.shape[0])
+        self._c = _HostPool(k_pool.data_ptr(), v_pool.data_ptr(), self.num_blocks)
+
+    @classmethod
+    def like(cls, pool: "PagedKVPool", num_blocks: int):
+        shape = (num_blocks, pool.num_kv_heads, pool.block_size, pool.head_dim)
+        k = torch.empty(shape, dtype=pool.dtype, pin_memory=True)
+        v = torch.empty(shape, dtype=pool.dtype, pin_memory=True)
+        return cls(k, v)
+
+    @property
+    def c(self):
+        return ctypes.byref(self._c)
+
+
+def kvp_block_swap(pool: PagedKVPool, host: HostKVPool, pairs: torch.Tensor, direction: int, stream=None) -> None:
+    """Move whole blocks between the device pool and the host pool:
+    ``direction`` HostKVPool.SWAP_OUT copies pool[src] -> host[dst],
+    HostKVPool.SWAP_IN copies host[src] -> pool[dst], per (src, dst) row of
+    ``pairs`` (device int32 [n, 2])."""
+    if tuple(host.k.shape[1:]) != (pool.num_kv_heads, pool.block_size, pool.head_dim) or host.k.dtype != pool.dtype:
+        raise ValueError("host pool geometry or dtype differs from the device pool")
+    lib = load_library()
+    n = int(pairs.shape[0]) if pairs.numel() else 0
+    _check(lib.kvp_block_swap(pool.c, host.c, _ptr(pairs) if n else None, n, int(direction), _stream(stream)),
+           "kvp_block_swap")
 
 
 def kvp_workspace_size(op: int, rows: int, num_q_heads: int, head_dim: int, num_splits: int) -> int:

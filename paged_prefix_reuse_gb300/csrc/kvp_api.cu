@@ -188,6 +188,21 @@ kvp_status kvp_block_copy(const kvp_pool* pool, const int32_t* pairs, int32_t n,
         launch_block_copy(view_of(pool), pool->k_pool, pool->v_pool, pairs, n, static_cast<cudaStream_t>(stream)));
 }
 
+kvp_status kvp_block_swap(const kvp_pool* pool, const kvp_host_pool* host, const int32_t* pairs, int32_t n,
+                          int32_t direction, void* stream) {
+    kvp_status st = check_pool(pool);
+    if (st != KVP_OK) return st;
+    if (!host || n < 0 || n > 65535) return KVP_ERR_INVALID_ARG;
+    if (direction != KVP_SWAP_OUT && direction != KVP_SWAP_IN) return KVP_ERR_INVALID_ARG;
+    if (!host->k_pool || !host->v_pool || host->num_blocks < 1) return KVP_ERR_INVALID_ARG;
+    if (!aligned16(host->k_pool) || !aligned16(host->v_pool)) return KVP_ERR_INVALID_ARG;
+    if (n == 0) return KVP_OK;
+    if (!pairs) return KVP_ERR_INVALID_ARG;
+    return from_cuda(launch_block_swap(view_of(pool), pool->k_pool, pool->v_pool, host->k_pool, host->v_pool,
+                                       host->num_blocks, pairs, n, direction == KVP_SWAP_OUT,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 kvp_status kvp_prefix_attn(const kvp_pool* pool, const void* q, void* out, float* lse, const int32_t* cu_seqlens_q,
                            const int32_t* context_lens, const int32_t* block_tables, int32_t max_blocks, int32_t B,
                            int32_t total_q, int32_t num_q_heads, int32_t max_q_len, int32_t max_context_len,

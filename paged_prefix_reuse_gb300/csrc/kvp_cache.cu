@@ -3,7 +3,8 @@
 // and stores, grid-stride loops sized to the SM count.
 //
 // Pages: kvstream 0.1.0, "Request lifecycle" steps 2-3 (one slot per new
-// token; a forked block table shares pages copy-on-write); kvboost 0.6.0,
+// token; a forked block table shares pages copy-on-write) and "Features"
+// (swap and preemption to a CPU page pool); kvboost 0.6.0,
 // "CPU paged attention" (fixed block pool, shared prefixes share physical
 // blocks copy-on-write) and "How it works" step 5 (newly seen K/V written
 // back to the cache).
@@ -112,40 +113,45 @@ __global__ void __launch_bounds__(kThreads) append_kernel(PoolView pool, uint4* 
     }
 }
 
-// Copy-on-write copy.  A block of one pool is vpb = Hkv * bs * d / 8 16-byte
-// vectors; blockIdx.y picks the pair and blockIdx.x a 512-vector chunk of
-// it, each thread copying two vectors of K and two of V.
-__global__ void __launch_bounds__(kThreads) block_copy_kernel(PoolView pool, uint4* __restrict__ k_pool,
-                                                              uint4* __restrict__ v_pool,
-                                                              const int32_t* __restrict__ pairs, int32_t vpb) {
+// Block moves: copy-on-write within the device pool, and swap between the
+// device pool and a host pool (read or written over the host link through
+// the host memory's device mapping).  A block of either pool is vpb =
+// Hkv * bs * d / 8 16-byte vectors; blockIdx.y picks the pair and blockIdx.x
+// a 512-vector chunk of it, each thread moving two vectors of K and two of V
+// with all four loads issued before the stores.
+__global__ void __launch_bounds__(kThreads) block_move_kernel(const uint4* __restrict__ ks,
+                                                              const uint4* __restrict__ vs, int64_t src_blocks,
+                                                              uint4* __restrict__ kd, uint4* __restrict__ vd,
+                                                              int64_t dst_blocks, const int32_t* __restrict__ pairs,
+                                                              int32_t vpb, uint32_t* err_word) {
     const int i = blockIdx.y;
     const int64_t src = __ldg(pairs + 2 * i);
     const int64_t dst = __ldg(pairs + 2 * i + 1);
-    if (src < 0 || src >= pool.num_blocks || dst < 0 || dst >= pool.num_blocks) {
-        if (threadIdx.x == 0 && blockIdx.x == 0) report(pool.err_word, KVP_DEVERR_BAD_PAIR);
+    if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) report(err_word, KVP_DEVERR_BAD_PAIR);
         return;
     }
     const int e0 = blockIdx.x * 2 * kThreads + threadIdx.x, e1 = e0 + kThreads;
-    const uint4* ks = k_pool + src * vpb;
-    const uint4* vs = v_pool + src * vpb;
-    uint4* kd = k_pool + dst * vpb;
-    uint4* vd = v_pool + dst * vpb;
+    const uint4* kss = ks + src * vpb;
+    const uint4* vss = vs + src * vpb;
+    uint4* kdd = kd + dst * vpb;
+    uint4* vdd = vd + dst * vpb;
     uint4 k0, v0, k1, v1;
     if (e0 < vpb) {
-        k0 = ks[e0];
-        v0 = vs[e0];
+        k0 = kss[e0];
+        v0 = vss[e0];
     }
     if (e1 < vpb) {
-        k1 = ks[e1];
-        v1 = vs[e1];
+        k1 = kss[e1];
+        v1 = vss[e1];
     }
     if (e0 < vpb) {
-        kd[e0] = k0;
-        vd[e0] = v0;
+        kdd[e0] = k0;
+        vdd[e0] = v0;
     }
     if (e1 < vpb) {
-        kd[e1] = k1;
-        vd[e1] = v1;
+        kdd[e1] = k1;
+        vdd[e1] = v1;
     }
 }
 
@@ -180,8 +186,28 @@ cudaError_t launch_block_copy(const PoolView& pool, void* k_pool, void* v_pool, 
     const int32_t vpb = pool.num_kv_heads * pool.block_size * (pool.head_dim / 8);
     if (n > 65535) return cudaErrorInvalidValue;
     const dim3 grid((vpb + 2 * kThreads - 1) / (2 * kThreads), n);
-    block_copy_kernel<<<grid, kThreads, 0, stream>>>(pool, static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool),
-                                                     pairs, vpb);
+    block_move_kernel<<<grid, kThreads, 0, stream>>>(static_cast<const uint4*>(k_pool), static_cast<const uint4*>(v_pool),
+                                                     pool.num_blocks, static_cast<uint4*>(k_pool),
+                                                     static_cast<uint4*>(v_pool), pool.num_blocks, pairs, vpb,
+                                                     pool.err_word);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_block_swap(const PoolView& pool, void* k_pool, void* v_pool, void* host_k, void* host_v,
+                              int64_t host_blocks, const int32_t* pairs, int32_t n, bool to_host,
+                              cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    const int32_t vpb = pool.num_kv_heads * pool.block_size * (pool.head_dim / 8);
+    if (n > 65535) return cudaErrorInvalidValue;
+    const dim3 grid((vpb + 2 * kThreads - 1) / (2 * kThreads), n);
+    if (to_host)
+        block_move_kernel<<<grid, kThreads, 0, stream>>>(
+            static_cast<const uint4*>(k_pool), static_cast<const uint4*>(v_pool), pool.num_blocks,
+            static_cast<uint4*>(host_k), static_cast<uint4*>(host_v), host_blocks, pairs, vpb, pool.err_word);
+    else
+        block_move_kernel<<<grid, kThreads, 0, stream>>>(
+            static_cast<const uint4*>(host_k), static_cast<const uint4*>(host_v), host_blocks,
+            static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), pool.num_blocks, pairs, vpb, pool.err_word);
     return cudaGetLastError();
 }
 

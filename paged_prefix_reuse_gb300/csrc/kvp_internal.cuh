@@ -61,6 +61,9 @@ cudaError_t launch_cache_append(const PoolView& pool, void* k_pool, void* v_pool
                                 const void* v_new, const int64_t* slot_mapping, int32_t T, cudaStream_t stream);
 cudaError_t launch_block_copy(const PoolView& pool, void* k_pool, void* v_pool, const int32_t* pairs, int32_t n,
                               cudaStream_t stream);
+cudaError_t launch_block_swap(const PoolView& pool, void* k_pool, void* v_pool, void* host_k, void* host_v,
+                              int64_t host_blocks, const int32_t* pairs, int32_t n, bool to_host,
+                              cudaStream_t stream);
 cudaError_t launch_prefix_attn(const PrefixParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                cudaStream_t stream);
 // Query rows (token, head-of-group pairs) one prefix CTA covers.

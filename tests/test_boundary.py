@@ -141,6 +141,26 @@ def test_append_copy_slot_validation(lib):
     assert lib.kvp_slot_mapping(P, None, 0x40000, 0x50000, 4, 1, 4, 0x60000, None) == KVP_ERR_INVALID_ARG
 
 
+def test_swap_validation(lib):
+    """kvp_block_swap rejects bad host pools, directions and counts before any device work."""
+    pool = _pool()
+    P = ctypes.byref(pool)
+    H = kvp._HostPool(0x70000, 0x80000, 64)
+    assert lib.kvp_block_swap(P, ctypes.byref(H), 0x30000, 0, 0, None) == KVP_OK
+    assert lib.kvp_block_swap(P, ctypes.byref(H), 0x30000, 0, 1, None) == KVP_OK
+    assert lib.kvp_block_swap(P, None, 0x30000, 1, 0, None) == KVP_ERR_INVALID_ARG
+    assert lib.kvp_block_swap(P, ctypes.byref(H), 0x30000, 1, 2, None) == KVP_ERR_INVALID_ARG
+    assert lib.kvp_block_swap(P, ctypes.byref(H), 0x30000, -1, 0, None) == KVP_ERR_INVALID_ARG
+    assert lib.kvp_block_swap(P, ctypes.byref(H), None, 3, 0, None) == KVP_ERR_INVALID_ARG
+    assert lib.kvp_block_swap(P, ctypes.byref(H), 0x30000, 65536, 0, None) == KVP_ERR_INVALID_ARG
+    bad = kvp._HostPool(0x70008, 0x80000, 64)  # misaligned
+    assert lib.kvp_block_swap(P, ctypes.byref(bad), 0x30000, 1, 0, None) == KVP_ERR_INVALID_ARG
+    empty = kvp._HostPool(0x70000, 0x80000, 0)
+    assert lib.kvp_block_swap(P, ctypes.byref(empty), 0x30000, 1, 0, None) == KVP_ERR_INVALID_ARG
+    nullk = kvp._HostPool(None, 0x80000, 64)
+    assert lib.kvp_block_swap(P, ctypes.byref(nullk), 0x30000, 1, 0, None) == KVP_ERR_INVALID_ARG
+
+
 def test_workspace_and_split_helpers(lib):
     assert kvp.kvp_workspace_size(0, 100, 8, 128, 1) == 0
     ws = kvp.kvp_workspace_size(0, 100, 8, 128, 3)

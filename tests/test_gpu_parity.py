@@ -270,3 +270,75 @@ def test_full_size_configs_sampled_rows(cfg):
     if drows is not None:
         _compare_attn(w.dtype, st.out_dec, st.lse_dec, ref["decode_out"], ref["decode_lse"], drows, f"cfg{cfg}-dec")
         assert torch.isfinite(st.out_dec.float()).all()
+
+
+# --------------------------------------------------------------------------
+# host <-> device block swap (the CPU page pool of preempted sequences)
+# --------------------------------------------------------------------------
+def _bits_host(t: torch.Tensor) -> np.ndarray:
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("dtype,d,bs", [("bf16", 128, 16), ("f16", 96, 32), ("bf16", 64, 8)])
+def test_block_swap_out_and_in_is_bit_exact(dtype, d, bs):
+    import paged_prefix_reuse_gb300 as kvp
+
+    nb = 128
+    w = wl.make_random(60 + d, [500, 300], [20, 7], Hq=8, Hkv=4, d=d, dtype=dtype, bs=bs, num_blocks=nb,
+                       fill_all_blocks=True)
+    st = _step(w)
+    host = kvp.HostKVPool.like(st.pool, 40)
+    rng = np.random.default_rng(d)
+    host.k.view(torch.int16).copy_(torch.from_numpy(rng.integers(-32768, 32767, size=host.k.shape, dtype=np.int16)))
+    host.v.view(torch.int16).copy_(torch.from_numpy(rng.integers(-32768, 32767, size=host.v.shape, dtype=np.int16)))
+    hk0, hv0 = _bits_host(host.k).copy(), _bits_host(host.v).copy()
+    dev_k0, dev_v0 = _bits(st.pool.k), _bits(st.pool.v)
+
+    # swap out 23 scattered device blocks to scattered host blocks, on a side stream
+    src = rng.choice(nb, size=23, replace=False)
+    dst = rng.choice(40, size=23, replace=False)
+    out_pairs = np.stack([src, dst], 1).astype(np.int32)
+    side = torch.cuda.Stream()
+    pairs_d = torch.from_numpy(out_pairs).cuda()
+    side.wait_stream(torch.cuda.current_stream())
+    kvp.kvp_block_swap(st.pool, host, pairs_d, kvp.HostKVPool.SWAP_OUT, stream=side)
+    side.synchronize()
+    assert st.pool.errors() == 0
+    want_k, want_v, bad = oracle.block_swap(dev_k0, dev_v0, hk0, hv0, out_pairs)
+    assert bad == 0
+    np.testing.assert_array_equal(_bits_host(host.k), want_k)
+    np.testing.assert_array_equal(_bits_host(host.v), want_v)
+
+    # swap those host blocks back in to other (free) device blocks
+    free = np.setdiff1d(np.arange(nb), src)
+    back = np.stack([dst, rng.choice(free, size=23, replace=False)], 1).astype(np.int32)
+    kvp.kvp_block_swap(st.pool, host, torch.from_numpy(back).cuda(), kvp.HostKVPool.SWAP_IN)
+    torch.cuda.synchronize()
+    assert st.pool.errors() == 0
+    want_dk, want_dv, bad = oracle.block_swap(want_k, want_v, dev_k0, dev_v0, back)
+    assert bad == 0
+    np.testing.assert_array_equal(_bits(st.pool.k), want_dk)
+    np.testing.assert_array_equal(_bits(st.pool.v), want_dv)
+    np.testing.assert_array_equal(want_dk[back[:, 1]], dev_k0[src])  # the round trip
+
+
+def test_block_swap_bad_pairs_are_flagged_not_faulted():
+    import paged_prefix_reuse_gb300 as kvp
+
+    w = wl.make_random(70, [100], [4], Hq=4, Hkv=2, d=64, dtype="f16", num_blocks=16, fill_all_blocks=True)
+    st = _step(w)
+    host = kvp.HostKVPool.like(st.pool, 8)
+    host.k.zero_()
+    host.v.zero_()
+    dev_k0 = _bits(st.pool.k)
+    pairs = torch.tensor([[3, 8], [16, 0], [2, 1], [-1, 2]], dtype=torch.int32, device="cuda")
+    kvp.kvp_block_swap(st.pool, host, pairs, kvp.HostKVPool.SWAP_OUT)
+    torch.cuda.synchronize()
+    assert st.pool.errors() & kvp.DEVERR["bad_pair"]
+    np.testing.assert_array_equal(_bits_host(host.k)[1], dev_k0[2])  # the valid pair still moved
+    assert not _bits_host(host.k)[[0, 2, 3]].any()
+    st.pool.clear_errors()
+    kvp.kvp_block_swap(st.pool, host, pairs[:0], kvp.HostKVPool.SWAP_IN)  # n == 0
+    torch.cuda.synchronize()
+    assert st.pool.errors() == 0
+    np.testing.assert_array_equal(_bits(st.pool.k), dev_k0)

@@ -442,6 +442,32 @@ def test_block_copy_copies_exactly_the_pairs():
     assert bad == 1
 
 
+def test_block_swap_moves_blocks_between_pools_and_round_trips():
+    """Swap out then back in to other blocks: the device blocks come back
+    byte-identical, untouched blocks of both pools are unchanged, and a pair
+    outside either pool is skipped and counted."""
+    w = wl.make_random(32, [70], [9], Hq=4, Hkv=2, d=64, dtype="bf16", bs=16, num_blocks=12, fill_all_blocks=True)
+    rng = np.random.default_rng(5)
+    host_k = rng.integers(0, 1 << 16, size=(6,) + w.k_pool.shape[1:], dtype=np.uint16)
+    host_v = rng.integers(0, 1 << 16, size=host_k.shape, dtype=np.uint16)
+    out = np.array([[3, 0], [7, 4], [11, 5]], dtype=np.int32)
+    hk, hv, bad = oracle.block_swap(w.k_pool, w.v_pool, host_k, host_v, out)
+    assert bad == 0
+    for src, dst in out:
+        np.testing.assert_array_equal(hk[dst], w.k_pool[src])
+        np.testing.assert_array_equal(hv[dst], w.v_pool[src])
+    np.testing.assert_array_equal(hk[[1, 2, 3]], host_k[[1, 2, 3]])
+    back = np.array([[0, 1], [4, 2], [5, 9]], dtype=np.int32)
+    dk, dv, bad = oracle.block_swap(hk, hv, w.k_pool, w.v_pool, back)
+    assert bad == 0
+    np.testing.assert_array_equal(dk[[1, 2, 9]], w.k_pool[[3, 7, 11]])
+    np.testing.assert_array_equal(dv[[1, 2, 9]], w.v_pool[[3, 7, 11]])
+    keep = [b for b in range(12) if b not in (1, 2, 9)]
+    np.testing.assert_array_equal(dk[keep], w.k_pool[keep])
+    _, _, bad = oracle.block_swap(w.k_pool, w.v_pool, host_k, host_v, np.array([[12, 0], [0, 6], [-1, 1]]))
+    assert bad == 3
+
+
 def test_pool_page_size_matches_the_pages_formula():
     """kvstream.yaml: one page = block_size x heads x head_dim x 2 x dtype_bytes."""
     vals = {}
