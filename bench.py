@@ -587,6 +587,93 @@ def run_swap(args):
     return 0
 
 
+def run_decode_q(args):
+    """Decode over a quantized cached prefix: the mixed batch's decode
+    sequences with every complete page moved to an 8- or 4-bit pool (the
+    trailing partial page stays 16-bit), timed against the 16-bit decode of
+    the same batch.  Bytes are the pages each kernel reads: quantized pages at
+    their packed size (codes and fp16 scales), 16-bit pages whole."""
+    import numpy as np
+    import torch
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    from paged_prefix_reuse_gb300 import build as kvp_build
+
+    kvp_build.build_library()
+    import paged_prefix_reuse_gb300 as kvp
+    from paged_prefix_reuse_gb300.step import DeviceStep
+
+    kvp.load_library()
+    w = wl.make_config(4)
+    st = DeviceStep(w, device=dev)
+    st.run_slots()
+    st.run_append()
+    torch.cuda.synchronize()
+    pool = st.pool
+    bs, hkv, d = pool.block_size, pool.num_kv_heads, pool.head_dim
+    ctx = st.ctx[st.npf:].cpu().numpy()
+    bt = st.bt[st.npf:].cpu().numpy().copy()
+    qpages = (ctx // bs).astype(np.int32)
+    pairs = []
+    for b in range(len(ctx)):
+        for pg in range(int(qpages[b])):
+            pairs.append((int(bt[b, pg]), len(pairs)))
+            bt[b, pg] = len(pairs) - 1
+    qp = kvp.QuantKVPool.like(pool, len(pairs), args.bits)
+    kvp.kvp_quantize_blocks(pool, qp, torch.tensor(pairs, dtype=torch.int32, device=dev))
+    torch.cuda.synchronize()
+    tq = torch.from_numpy(qpages).to(dev)
+    tbt = torch.from_numpy(bt).to(dev)
+    q = st.q[st.tq:]
+    ctx_d = st.ctx[st.npf:]
+    bt16 = st.bt[st.npf:]
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def timed(fn):
+        ts = []
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup + args.steps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                e1.synchronize()
+                if i >= args.warmup:
+                    ts.append(e0.elapsed_time(e1) / 1e3)
+        return sorted(ts)[len(ts) // 2]
+
+    mctx = int(ctx.max())
+    t16 = timed(lambda: kvp.kvp_decode_attn(pool, q, ctx_d, bt16, mctx, w.softmax_scale, stream=stream))
+    tqz = timed(lambda: kvp.kvp_decode_attn_q(pool, qp, tq, q, ctx_d, tbt, mctx, w.softmax_scale, stream=stream))
+    npages = (ctx + bs - 1) // bs
+    page16 = hkv * bs * d * 2 * 2
+    pageq = hkv * (2 * bs * d * args.bits // 8 + 4 * d + 4 * bs)
+    bytes16 = float(npages.sum() * page16)
+    bytesq = float(qpages.sum() * pageq + (npages - qpages).sum() * page16)
+    peaks, peak_src = load_peaks()
+    hbm = _peak_value(peaks, "hbm_gbs") or FALLBACK_PEAKS["hbm_gbs"]
+    gbs = bytesq / tqz / 1e9
+    line = {
+        "metric": f"decode over an int{args.bits} cached prefix: sequences/s (GB/s of quantized pages read)",
+        "value": len(ctx) / tqz, "unit": "seq/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tqz * 1e3, "higher_is_better": True, "op": "decode_q", "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": "continuous_batching_step decode batch", "B": int(len(ctx)), "bits": args.bits,
+                   "quantized_pages": int(qpages.sum()), "pages_16bit": int((npages - qpages).sum()),
+                   "l2": "flushed before every timed call"},
+        "decode_16bit_ms": t16 * 1e3, "speedup_vs_16bit": t16 / tqz, "bytes_read": bytesq,
+        "bytes_read_16bit": bytes16, "gpu_launches": 1 + (1 if kvp.kvp_decode_num_splits(
+            len(ctx), hkv, bs, mctx) > 1 else 0),
+        "roofline": {"kernel": "decode_attn_q", "bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": gbs / hbm, "peak_source": f"{peak_src} HBM copy",
+                     "traffic": None},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -599,13 +686,17 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--preroll-s", type=float, default=0.4)
-    ap.add_argument("--op", choices=["step", "block_swap"], default="step",
-                    help="step: the prefill/decode step (default); block_swap: host <-> device page swap")
+    ap.add_argument("--op", choices=["step", "block_swap", "decode_q"], default="step",
+                    help="step: the prefill/decode step (default); block_swap: host <-> device page swap; "
+                         "decode_q: decode over a quantized cached prefix")
+    ap.add_argument("--bits", type=int, choices=[8, 4], default=8, help="quantized pool width for --op decode_q")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.op == "block_swap":
         return run_swap(args)
+    if args.op == "decode_q":
+        return run_decode_q(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_kvp(args)

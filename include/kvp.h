@@ -68,6 +68,7 @@ typedef enum { KVP_F16 = 0, KVP_BF16 = 1 } kvp_dtype;
 #define KVP_DEVERR_BAD_PAIR 0x4u  /* a copy pair naming a block outside the pool */
 #define KVP_DEVERR_BAD_LEN 0x8u   /* context_len < new tokens, or a table too short */
 #define KVP_DEVERR_TIMEOUT 0x10u  /* a bounded in-kernel wait gave up */
+#define KVP_DEVERR_QRANGE 0x20u   /* a quantization group's scale or min is not a finite fp16 */
 
 typedef struct {
     void *k_pool;          /* device, [num_blocks][num_kv_heads][block_size][head_dim], 16-B aligned */
@@ -114,6 +115,61 @@ kvp_status kvp_cache_append(const kvp_pool *pool, const void *k_new, const void 
  * result is undefined.  A pair naming a block outside the pool is skipped
  * and sets KVP_DEVERR_BAD_PAIR.  n == 0 is a no-op; n <= 65535 per call. */
 kvp_status kvp_block_copy(const kvp_pool *pool, const int32_t *pairs, int32_t n, void *stream);
+
+/* A quantized block pool (kvboost "Optional: KV quantization": cached K/V
+ * stored in 8 or 4 bits, K quantized per channel and V per token, the
+ * asymmetry of the KIVI paper).  The pages give nothing more; the format
+ * taken here: the quantization group is one page of one kv head, K per
+ * (block, head, channel) over the block's tokens and V per (block, head,
+ * token) over the channels; asymmetric min/max codes, levels = 2^bits - 1,
+ *     s = fp16_round_up((max - min) / levels),  z = fp16_round_down(min),
+ *     code = clamp(round_half_even((x - z) / s), 0, levels)   (fp32 steps),
+ *     x' = code * s + z;
+ * a group with max == min has s = 0 and codes 0.
+ *   k_codes, v_codes: device uint8 [num_blocks][Hkv][bs][head_dim*bits/8],
+ *       channels in order; at 4 bits two codes per byte, the even channel in
+ *       the low nibble.
+ *   k_meta: device fp16 [num_blocks][Hkv][2][head_dim] (scale row, min row).
+ *   v_meta: device fp16 [num_blocks][Hkv][bs][2] (scale, min) per token.
+ * All four 16-byte aligned, caller-owned.  num_kv_heads, block_size and
+ * head_dim must equal those of the 16-bit pool it is used with. */
+typedef struct kvp_qpool {
+    void *k_codes;
+    void *v_codes;
+    void *k_meta;
+    void *v_meta;
+    int64_t num_blocks;
+    int32_t block_size;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t bits; /* 8 or 4 */
+} kvp_qpool;
+
+/* Quantize whole blocks of the 16-bit pool into the quantized pool (the
+ * write-back of cached chunks in quantized form): for each pair,
+ *     qpool[pairs[i][1]] = quantize(pool[pairs[i][0]])   (K and V, all heads).
+ * pairs: device int32 [n][2] = (src block of pool, dst block of qpool);
+ * destinations must be distinct.  A pair outside either pool is skipped and
+ * sets KVP_DEVERR_BAD_PAIR; a group whose scale or min overflows fp16 sets
+ * KVP_DEVERR_QRANGE (in pool.err_word).  n == 0 is a no-op; n <= 65535.
+ * Errors: KVP_ERR_INVALID_ARG (null/misaligned pointer, n < 0, geometry of
+ * the two pools differs), KVP_ERR_UNSUPPORTED (bits not 8 or 4). */
+kvp_status kvp_quantize_blocks(const kvp_pool *pool, const kvp_qpool *qpool, const int32_t *pairs, int32_t n,
+                               void *stream);
+
+/* Decode attention over a context whose cached prefix is quantized: as
+ * kvp_decode_attn, except that for sequence s the first qpages[s] entries of
+ * its block table name blocks of qpool (dequantized on the fly inside the
+ * kernel, code * s + z, then rounded to the pool dtype for the tensor-core
+ * product) and the remaining entries name blocks of the 16-bit pool (the live
+ * suffix).  qpages: device int32 [B], 0 <= qpages[s] <= pages of s (a larger
+ * value is clamped).  block_size must be 16 or 32.  Workspace, splits,
+ * outputs and errors as kvp_decode_attn (kvp_workspace_size op 1). */
+kvp_status kvp_decode_attn_q(const kvp_pool *pool, const kvp_qpool *qpool, const int32_t *qpages, const void *q,
+                             void *out, float *lse, const int32_t *context_lens, const int32_t *block_tables,
+                             int32_t max_blocks, int32_t B, int32_t num_q_heads, int32_t max_context_len,
+                             float softmax_scale, int32_t num_splits, void *workspace, size_t workspace_bytes,
+                             void *stream);
 
 /* A pool of blocks in host memory with the same block geometry (num_kv_heads,
  * block_size, head_dim, dtype) as a device pool: the swap buffer of

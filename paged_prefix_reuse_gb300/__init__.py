@@ -9,7 +9,8 @@ raises ``KvpLibraryMissing``.
 
 Functions carry the names of the C entry points declared in
 ``include/kvp.h``: ``kvp_slot_mapping``, ``kvp_cache_append``,
-``kvp_block_copy``, ``kvp_block_swap``, ``kvp_prefix_attn``, ``kvp_decode_attn`` and
+``kvp_block_copy``, ``kvp_block_swap``, ``kvp_quantize_blocks``,
+``kvp_prefix_attn``, ``kvp_decode_attn``, ``kvp_decode_attn_q`` and
 ``kvp_workspace_size`` (plus the split-count helpers).
 """
 from __future__ import annotations
@@ -25,6 +26,7 @@ __all__ = [
     "KvpLibraryMissing",
     "PagedKVPool",
     "HostKVPool",
+    "QuantKVPool",
     "EXPORTED_SYMBOLS",
     "lib_path",
     "load_library",
@@ -32,8 +34,10 @@ __all__ = [
     "kvp_cache_append",
     "kvp_block_copy",
     "kvp_block_swap",
+    "kvp_quantize_blocks",
     "kvp_prefix_attn",
     "kvp_decode_attn",
+    "kvp_decode_attn_q",
     "kvp_decode_attn_noalloc",
     "kvp_workspace_size",
     "kvp_prefix_num_splits",
@@ -49,7 +53,7 @@ KVP_F16, KVP_BF16 = 0, 1
 _DTYPES = {torch.float16: KVP_F16, torch.bfloat16: KVP_BF16}
 
 # Device error-word bits (KVP_DEVERR_* in kvp.h).
-DEVERR = {"bad_block": 0x1, "bad_slot": 0x2, "bad_pair": 0x4, "bad_len": 0x8, "timeout": 0x10}
+DEVERR = {"bad_block": 0x1, "bad_slot": 0x2, "bad_pair": 0x4, "bad_len": 0x8, "timeout": 0x10, "qrange": 0x20}
 
 # Every extern "C" symbol declared in include/kvp.h.
 EXPORTED_SYMBOLS = (
@@ -57,8 +61,10 @@ EXPORTED_SYMBOLS = (
     "kvp_cache_append",
     "kvp_block_copy",
     "kvp_block_swap",
+    "kvp_quantize_blocks",
     "kvp_prefix_attn",
     "kvp_decode_attn",
+    "kvp_decode_attn_q",
     "kvp_decode_attn_noalloc",
     "kvp_prefix_num_splits",
     "kvp_decode_num_splits",
@@ -76,6 +82,20 @@ class KvpError(RuntimeError):
 
 class KvpLibraryMissing(RuntimeError):
     pass
+
+
+class _QPool(ctypes.Structure):
+    _fields_ = [
+        ("k_codes", ctypes.c_void_p),
+        ("v_codes", ctypes.c_void_p),
+        ("k_meta", ctypes.c_void_p),
+        ("v_meta", ctypes.c_void_p),
+        ("num_blocks", ctypes.c_int64),
+        ("block_size", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("bits", ctypes.c_int32),
+    ]
 
 
 class _HostPool(ctypes.Structure):
@@ -120,11 +140,15 @@ def load_library():
         lib.kvp_cache_append.argtypes = [PP, P, P, P, i32, P]
         lib.kvp_block_copy.argtypes = [PP, P, i32, P]
         lib.kvp_block_swap.argtypes = [PP, ctypes.POINTER(_HostPool), P, i32, i32, P]
+        QP = ctypes.POINTER(_QPool)
+        lib.kvp_quantize_blocks.argtypes = [PP, QP, P, i32, P]
+        lib.kvp_decode_attn_q.argtypes = [PP, QP, P, P, P, P, P, P, i32, i32, i32, i32, f32, i32, P, sz, P]
         lib.kvp_prefix_attn.argtypes = [PP, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, i32, P, sz, P]
         lib.kvp_decode_attn.argtypes = [PP, P, P, P, P, P, i32, i32, i32, i32, f32, i32, P, sz, P]
         lib.kvp_decode_attn_noalloc.argtypes = [PP, P, P, P, P, P, i32, i32, i32, i32, f32, i32, P]
-        for name in ("kvp_slot_mapping", "kvp_cache_append", "kvp_block_copy", "kvp_block_swap", "kvp_prefix_attn",
-                     "kvp_decode_attn", "kvp_decode_attn_noalloc"):
+        for name in ("kvp_slot_mapping", "kvp_cache_append", "kvp_block_copy", "kvp_block_swap",
+                     "kvp_quantize_blocks", "kvp_prefix_attn", "kvp_decode_attn", "kvp_decode_attn_q",
+                     "kvp_decode_attn_noalloc"):
             getattr(lib, name).restype = ctypes.c_int
         lib.kvp_prefix_num_splits.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.kvp_prefix_num_splits.restype = i32
@@ -213,6 +237,76 @@ class PagedKVPool:
 
     def clear_errors(self) -> None:
         self.err_word.zero_()
+
+
+class QuantKVPool:
+    """A quantized block pool (8 or 4 bits; K per channel, V per token; see
+    ``kvp_qpool`` in kvp.h): device tensors k_codes/v_codes uint8
+    [num_blocks, Hkv, bs, d*bits/8], k_meta float16 [num_blocks, Hkv, 2, d]
+    (scale row, min row), v_meta float16 [num_blocks, Hkv, bs, 2]."""
+
+    def __init__(self, k_codes, v_codes, k_meta, v_meta, bits: int):
+        nb, hkv, bs, cb = (int(x) for x in k_codes.shape)
+        d = cb * 8 // bits
+        if bits not in (8, 4) or tuple(v_codes.shape) != (nb, hkv, bs, cb):
+            raise ValueError("bad code tensors")
+        if tuple(k_meta.shape) != (nb, hkv, 2, d) or tuple(v_meta.shape) != (nb, hkv, bs, 2):
+            raise ValueError("bad meta tensors")
+        for t in (k_codes, v_codes, k_meta, v_meta):
+            if not (t.is_cuda and t.is_contiguous()):
+                raise ValueError("quantized pool tensors must be contiguous CUDA tensors")
+        self.k_codes, self.v_codes, self.k_meta, self.v_meta = k_codes, v_codes, k_meta, v_meta
+        self.bits, self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim = bits, nb, hkv, bs, d
+        self._c = _QPool(k_codes.data_ptr(), v_codes.data_ptr(), k_meta.data_ptr(), v_meta.data_ptr(), nb, bs, hkv,
+                         d, bits)
+
+    @classmethod
+    def like(cls, pool: "PagedKVPool", num_blocks: int, bits: int):
+        dev = pool.k.device
+        cb = pool.head_dim * bits // 8
+        shape = (num_blocks, pool.num_kv_heads, pool.block_size, cb)
+        return cls(torch.zeros(shape, dtype=torch.uint8, device=dev), torch.zeros(shape, dtype=torch.uint8, device=dev),
+                   torch.zeros((num_blocks, pool.num_kv_heads, 2, pool.head_dim), dtype=torch.float16, device=dev),
+                   torch.zeros((num_blocks, pool.num_kv_heads, pool.block_size, 2), dtype=torch.float16, device=dev),
+                   bits)
+
+    @property
+    def c(self):
+        return ctypes.byref(self._c)
+
+
+def kvp_quantize_blocks(pool: PagedKVPool, qpool: QuantKVPool, pairs: torch.Tensor, stream=None) -> None:
+    """qpool[dst] = quantize(pool[src]) per (src, dst) row of ``pairs`` (device int32 [n, 2])."""
+    lib = load_library()
+    n = int(pairs.shape[0]) if pairs.numel() else 0
+    _check(lib.kvp_quantize_blocks(pool.c, qpool.c, _ptr(pairs) if n else None, n, _stream(stream)),
+           "kvp_quantize_blocks")
+
+
+def kvp_decode_attn_q(pool: PagedKVPool, qpool: QuantKVPool, qpages: torch.Tensor, q: torch.Tensor,
+                      context_lens: torch.Tensor, block_tables: torch.Tensor, max_context_len: int,
+                      softmax_scale: float, num_splits: int = 0, out: torch.Tensor | None = None,
+                      lse: torch.Tensor | None = None, workspace: torch.Tensor | None = None, want_lse: bool = True,
+                      stream=None):
+    """Decode attention where the first ``qpages[s]`` table entries of each
+    sequence name blocks of the quantized pool and the rest blocks of the
+    16-bit pool.  Returns (out [B, Hq, d], lse [Hq, B] float32 or None)."""
+    lib = load_library()
+    B, Hq, d = (int(x) for x in q.shape)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((Hq, B), dtype=torch.float32, device=q.device)
+    splits = num_splits or kvp_decode_num_splits(B, pool.num_kv_heads, pool.block_size, max_context_len)
+    need = kvp_workspace_size(1, B, Hq, d, splits)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.kvp_decode_attn_q(pool.c, qpool.c, _ptr(qpages), _ptr(q), _ptr(out), _ptr(lse), _ptr(context_lens),
+                                 _ptr(block_tables), int(block_tables.shape[1]), B, Hq, int(max_context_len),
+                                 float(softmax_scale), int(splits), _ptr(workspace), ws_bytes, _stream(stream)),
+           "kvp_decode_attn_q")
+    return out, lse
 
 
 class HostKVPool:

@@ -263,15 +263,57 @@ kvp_status kvp_prefix_attn(const kvp_pool* pool, const void* q, void* out, float
     return from_cuda(e);
 }
 
-kvp_status kvp_decode_attn(const kvp_pool* pool, const void* q, void* out, float* lse, const int32_t* context_lens,
-                           const int32_t* block_tables, int32_t max_blocks, int32_t B, int32_t num_q_heads,
-                           int32_t max_context_len, float softmax_scale, int32_t num_splits, void* workspace,
-                           size_t workspace_bytes, void* stream) {
+static kvp_status check_qpool(const kvp_pool* pool, const kvp_qpool* qp) {
+    if (!qp || !qp->k_codes || !qp->v_codes || !qp->k_meta || !qp->v_meta || qp->num_blocks < 1)
+        return KVP_ERR_INVALID_ARG;
+    if (!aligned16(qp->k_codes) || !aligned16(qp->v_codes) || !aligned16(qp->k_meta) || !aligned16(qp->v_meta))
+        return KVP_ERR_INVALID_ARG;
+    if (qp->bits != 8 && qp->bits != 4) return KVP_ERR_UNSUPPORTED;
+    if (qp->block_size != pool->block_size || qp->num_kv_heads != pool->num_kv_heads ||
+        qp->head_dim != pool->head_dim)
+        return KVP_ERR_INVALID_ARG;
+    return KVP_OK;
+}
+
+static QPoolView qview_of(const kvp_qpool* qp) {
+    QPoolView v;
+    v.k_codes = static_cast<uint8_t*>(qp->k_codes);
+    v.v_codes = static_cast<uint8_t*>(qp->v_codes);
+    v.k_meta = static_cast<__half*>(qp->k_meta);
+    v.v_meta = static_cast<__half*>(qp->v_meta);
+    v.num_blocks = qp->num_blocks;
+    v.bits = qp->bits;
+    return v;
+}
+
+kvp_status kvp_quantize_blocks(const kvp_pool* pool, const kvp_qpool* qpool, const int32_t* pairs, int32_t n,
+                               void* stream) {
     kvp_status st = check_pool(pool);
     if (st != KVP_OK) return st;
+    if ((st = check_qpool(pool, qpool)) != KVP_OK) return st;
+    if (n < 0 || n > 65535) return KVP_ERR_INVALID_ARG;
+    if (n == 0) return KVP_OK;
+    if (!pairs) return KVP_ERR_INVALID_ARG;
+    return from_cuda(launch_quantize_blocks(view_of(pool), pool->k_pool, pool->v_pool, qview_of(qpool), pairs, n,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+// Decode attention, with (qpool != nullptr) or without a quantized prefix.
+static kvp_status decode_common(const kvp_pool* pool, const kvp_qpool* qpool, const int32_t* qpages, const void* q,
+                                void* out, float* lse, const int32_t* context_lens, const int32_t* block_tables,
+                                int32_t max_blocks, int32_t B, int32_t num_q_heads, int32_t max_context_len,
+                                float softmax_scale, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+    kvp_status st = check_pool(pool);
+    if (st != KVP_OK) return st;
+    if (qpool) {
+        if ((st = check_qpool(pool, qpool)) != KVP_OK) return st;
+        if (pool->block_size != 16) return KVP_ERR_UNSUPPORTED;
+    }
     if (B < 0 || max_blocks < 0 || num_splits < 0 || max_context_len < 0) return KVP_ERR_INVALID_ARG;
     if (B == 0) return KVP_OK;
     if (!q || !out || !context_lens || !block_tables || max_blocks == 0) return KVP_ERR_INVALID_ARG;
+    if (qpool && !qpages) return KVP_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(out)) return KVP_ERR_INVALID_ARG;
     if (num_q_heads < 1 || num_q_heads % pool->num_kv_heads != 0) return KVP_ERR_INVALID_ARG;
     const int32_t g = num_q_heads / pool->num_kv_heads;
@@ -297,6 +339,8 @@ kvp_status kvp_decode_attn(const kvp_pool* pool, const void* q, void* out, float
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
     p.ws_o = nullptr;
     p.ws_lse = nullptr;
+    p.qpool = qpool ? qview_of(qpool) : QPoolView{nullptr, nullptr, nullptr, nullptr, 0, 0};
+    p.qpages = qpool ? qpages : nullptr;
     if (p.max_splits > 1) {
         const size_t need = kvp_workspace_size(1, B, num_q_heads, pool->head_dim, p.max_splits);
         if (!workspace || workspace_bytes < need || !aligned16(workspace)) return KVP_ERR_WORKSPACE;
@@ -308,12 +352,30 @@ kvp_status kvp_decode_attn(const kvp_pool* pool, const void* q, void* out, float
     if ((st = make_pool_map(&tk, pool->k_pool, pool)) != KVP_OK) return st;
     if ((st = make_pool_map(&tv, pool->v_pool, pool)) != KVP_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_decode_attn(p, tk, tv, s);
+    cudaError_t e = qpool ? launch_decode_attn_q(p, tk, tv, s) : launch_decode_attn(p, tk, tv, s);
     if (e != cudaSuccess) return KVP_ERR_CUDA;
     if (p.max_splits > 1)
         e = launch_merge(p.ws_o, p.ws_lse, B * num_q_heads, num_q_heads, pool->head_dim, p.max_splits, pool->dtype,
                          out, lse, B, context_lens, pool->block_size, p.pages_per_split, decode_parts_per_split(), s);
     return from_cuda(e);
+}
+
+kvp_status kvp_decode_attn(const kvp_pool* pool, const void* q, void* out, float* lse, const int32_t* context_lens,
+                           const int32_t* block_tables, int32_t max_blocks, int32_t B, int32_t num_q_heads,
+                           int32_t max_context_len, float softmax_scale, int32_t num_splits, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+    return decode_common(pool, nullptr, nullptr, q, out, lse, context_lens, block_tables, max_blocks, B, num_q_heads,
+                         max_context_len, softmax_scale, num_splits, workspace, workspace_bytes, stream);
+}
+
+kvp_status kvp_decode_attn_q(const kvp_pool* pool, const kvp_qpool* qpool, const int32_t* qpages, const void* q,
+                             void* out, float* lse, const int32_t* context_lens, const int32_t* block_tables,
+                             int32_t max_blocks, int32_t B, int32_t num_q_heads, int32_t max_context_len,
+                             float softmax_scale, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+    if (!qpool) return KVP_ERR_INVALID_ARG;
+    return decode_common(pool, qpool, qpages, q, out, lse, context_lens, block_tables, max_blocks, B, num_q_heads,
+                         max_context_len, softmax_scale, num_splits, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -22,6 +22,16 @@ struct PoolView {
     uint32_t* err_word;
 };
 
+// A quantized pool (see kvp_qpool in kvp.h).  bits == 0: none.
+struct QPoolView {
+    uint8_t* k_codes;
+    uint8_t* v_codes;
+    __half* k_meta;
+    __half* v_meta;
+    int64_t num_blocks;
+    int32_t bits;
+};
+
 struct PrefixParams {
     PoolView pool;
     const void* q;
@@ -51,6 +61,8 @@ struct DecodeParams {
     float scale_log2;
     float* ws_o;    // [B * Hq][max_splits * parts][head_dim]
     float* ws_lse;  // [B * Hq][max_splits * parts], log2 domain
+    QPoolView qpool;         // quantized prefix pages (bits 0: none)
+    const int32_t* qpages;   // [B]: leading table entries that name qpool blocks
 };
 
 // Host-side launchers (defined in the kernel .cu files).
@@ -61,6 +73,10 @@ cudaError_t launch_cache_append(const PoolView& pool, void* k_pool, void* v_pool
                                 const void* v_new, const int64_t* slot_mapping, int32_t T, cudaStream_t stream);
 cudaError_t launch_block_copy(const PoolView& pool, void* k_pool, void* v_pool, const int32_t* pairs, int32_t n,
                               cudaStream_t stream);
+cudaError_t launch_quantize_blocks(const PoolView& pool, const void* k_pool, const void* v_pool,
+                                   const QPoolView& qpool, const int32_t* pairs, int32_t n, cudaStream_t stream);
+cudaError_t launch_decode_attn_q(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                                 cudaStream_t stream);
 cudaError_t launch_block_swap(const PoolView& pool, void* k_pool, void* v_pool, void* host_k, void* host_v,
                               int64_t host_blocks, const int32_t* pairs, int32_t n, bool to_host,
                               cudaStream_t stream);
@@ -167,6 +183,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst_smem, const CUtensorMap* m
             "r"(smem_u32(dst_smem)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
+}
+
+// 1-D bulk copy global -> shared, completion on an mbarrier (both addresses
+// 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst_smem)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

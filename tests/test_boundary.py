@@ -161,6 +161,42 @@ def test_swap_validation(lib):
     assert lib.kvp_block_swap(P, ctypes.byref(nullk), 0x30000, 1, 0, None) == KVP_ERR_INVALID_ARG
 
 
+def test_quantized_pool_validation(lib):
+    """kvp_quantize_blocks / kvp_decode_attn_q reject bad quantized pools before any device work."""
+    pool = _pool()
+    P = ctypes.byref(pool)
+    nb, bs, hkv, d = pool.num_blocks, pool.block_size, pool.num_kv_heads, pool.head_dim
+
+    def qp(bits=8, **kw):
+        f = dict(k_codes=0x100000, v_codes=0x200000, k_meta=0x300000, v_meta=0x400000, num_blocks=64,
+                 block_size=bs, num_kv_heads=hkv, head_dim=d, bits=bits)
+        f.update(kw)
+        return kvp._QPool(**f)
+
+    good = qp()
+    assert lib.kvp_quantize_blocks(P, ctypes.byref(good), 0x30000, 0, None) == KVP_OK
+    assert lib.kvp_quantize_blocks(P, None, 0x30000, 1, None) == KVP_ERR_INVALID_ARG
+    assert lib.kvp_quantize_blocks(P, ctypes.byref(qp(bits=2)), 0x30000, 1, None) == KVP_ERR_UNSUPPORTED
+    assert lib.kvp_quantize_blocks(P, ctypes.byref(qp(head_dim=d // 2)), 0x30000, 1, None) == KVP_ERR_INVALID_ARG
+    assert lib.kvp_quantize_blocks(P, ctypes.byref(qp(k_meta=0x300008)), 0x30000, 1, None) == KVP_ERR_INVALID_ARG
+    assert lib.kvp_quantize_blocks(P, ctypes.byref(good), None, 1, None) == KVP_ERR_INVALID_ARG
+    assert lib.kvp_quantize_blocks(P, ctypes.byref(good), 0x30000, -1, None) == KVP_ERR_INVALID_ARG
+
+    def dq(qpool, qpages=0x60000, B=2):
+        return lib.kvp_decode_attn_q(P, qpool, qpages, 0x30000, 0x40000, None, 0x50000, 0x70000, 8, B, hkv * 2,
+                                     100, 0.1, 1, None, 0, None)
+
+    assert dq(ctypes.byref(good), B=0) == KVP_OK
+    assert dq(None) == KVP_ERR_INVALID_ARG
+    assert dq(ctypes.byref(good), qpages=None) == KVP_ERR_INVALID_ARG
+    assert dq(ctypes.byref(qp(bits=16))) == KVP_ERR_UNSUPPORTED
+    assert dq(ctypes.byref(qp(num_blocks=0))) == KVP_ERR_INVALID_ARG
+    pool32 = _pool(block_size=32)
+    q32 = kvp._QPool(0x100000, 0x200000, 0x300000, 0x400000, 64, 32, hkv, d, 8)
+    assert lib.kvp_decode_attn_q(ctypes.byref(pool32), ctypes.byref(q32), 0x60000, 0x30000, 0x40000, None, 0x50000,
+                                 0x70000, 8, 2, hkv * 2, 100, 0.1, 1, None, 0, None) == KVP_ERR_UNSUPPORTED
+
+
 def test_workspace_and_split_helpers(lib):
     assert kvp.kvp_workspace_size(0, 100, 8, 128, 1) == 0
     ws = kvp.kvp_workspace_size(0, 100, 8, 128, 3)

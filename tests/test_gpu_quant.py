@@ -1,0 +1,195 @@
+"""GPU parity of the quantized KV pool (8/4 bits) through the C ABI against
+the numpy oracle (oracle/quant.py) on the same seeded inputs.
+
+Bars: quantization codes bit-exact and scale/min equal as fp16 values;
+decode over a partly quantized context within max-abs 2e-2 (bf16) /
+5e-3 (fp16) of the fp64 oracle over the dequantized values, LSE within 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from oracle import quant
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 2e-2, "f16": 5e-3}
+LSE_TOL = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    from paged_prefix_reuse_gb300 import build
+
+    build.build_library()
+    import paged_prefix_reuse_gb300 as kvp
+
+    kvp.load_library()
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _qarrays(qp):
+    return (qp.k_codes.cpu().numpy(), qp.v_codes.cpu().numpy(), qp.k_meta.cpu().numpy(), qp.v_meta.cpu().numpy())
+
+
+@pytest.mark.parametrize("dtype,d,bits", [("bf16", 128, 8), ("bf16", 128, 4), ("f16", 96, 8), ("f16", 64, 4),
+                                          ("bf16", 96, 4)])
+def test_quantize_blocks_matches_oracle_bit_exact(dtype, d, bits):
+    import paged_prefix_reuse_gb300 as kvp
+
+    rng = np.random.default_rng(d * 10 + bits)
+    nb, Hkv, bs = 40, 3, 16
+    scale = np.geomspace(1e-2, 30, d).astype(np.float32)  # channels of very different ranges
+    K = (rng.standard_normal((nb, Hkv, bs, d)) * scale).astype(np.float32)
+    V = (rng.standard_normal((nb, Hkv, bs, d)) * rng.uniform(0.01, 10, (nb, Hkv, bs, 1))).astype(np.float32)
+    K[3] = 0.625  # constant groups
+    kb, vb = wl.round_to_bits(K, dtype), wl.round_to_bits(V, dtype)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    pool = kvp.PagedKVPool(torch.from_numpy(kb.view(np.int16)).view(tdt).cuda(),
+                           torch.from_numpy(vb.view(np.int16)).view(tdt).cuda())
+    qp = kvp.QuantKVPool.like(pool, 32, bits)
+    src = rng.choice(nb, size=29, replace=False)
+    src[0] = 3
+    pairs = np.stack([src, rng.choice(32, size=29, replace=False)], 1).astype(np.int32)
+    kvp.kvp_quantize_blocks(pool, qp, torch.from_numpy(pairs).cuda())
+    torch.cuda.synchronize()
+    assert pool.errors() == 0
+    want, bad = quant.quantize_blocks(dtype, kb, vb, quant.empty_qpool(32, Hkv, bs, d, bits), bits, pairs)
+    assert bad == 0
+    got = _qarrays(qp)
+    np.testing.assert_array_equal(got[0], want[0])
+    np.testing.assert_array_equal(got[1], want[1])
+    np.testing.assert_array_equal(got[2].astype(np.float32), want[2].astype(np.float32))
+    np.testing.assert_array_equal(got[3].astype(np.float32), want[3].astype(np.float32))
+
+
+def _decode_case(seed, contexts, dtype, d, Hq, Hkv, bits, qfrac, garbage_codes=False):
+    """A decode batch whose first pages per sequence are moved to a quantized
+    pool (a block index space of its own) and the rest stay 16-bit."""
+    import paged_prefix_reuse_gb300 as kvp
+    from paged_prefix_reuse_gb300.step import DeviceStep
+
+    w = wl.make_random(seed, [c - 1 for c in contexts], [1] * len(contexts), Hq=Hq, Hkv=Hkv, d=d, dtype=dtype,
+                       num_decode=len(contexts))
+    st = DeviceStep(w)
+    st.run_slots()
+    st.run_append()
+    torch.cuda.synchronize()
+    kb, vb = _bits(st.pool.k), _bits(st.pool.v)
+    rng = np.random.default_rng(seed)
+    bs = w.block_size
+    bt = st.bt.cpu().numpy().copy()
+    ctx = st.ctx.cpu().numpy()
+    qpages = []
+    pairs = []
+    for b, L in enumerate(ctx):
+        n = (int(L) + bs - 1) // bs
+        k = int(round(qfrac[b % len(qfrac)] * n))
+        qpages.append(k)
+        for p in range(k):
+            pairs.append((int(bt[b, p]), len(pairs)))
+            bt[b, p] = len(pairs) - 1
+    nq = max(1, len(pairs))
+    perm = rng.permutation(nq)  # scatter the quantized blocks
+    for b, k in enumerate(qpages):
+        bt[b, :k] = perm[bt[b, :k]]
+    pairs = np.array([(s_, perm[d_]) for s_, d_ in pairs], dtype=np.int32).reshape(-1, 2)
+    qp = kvp.QuantKVPool.like(st.pool, nq, bits)
+    if garbage_codes:
+        qp.k_codes.random_(0, 256)
+        qp.v_codes.random_(0, 256)
+    if len(pairs):
+        kvp.kvp_quantize_blocks(st.pool, qp, torch.from_numpy(pairs).cuda())
+    torch.cuda.synchronize()
+    assert st.pool.errors() == 0
+    oq, _ = quant.quantize_blocks(dtype, kb, vb, _qarrays(qp), bits, pairs)
+    return w, st, qp, oq, bt, np.array(qpages, dtype=np.int32), kb, vb
+
+
+@pytest.mark.parametrize("dtype,d,bits,splits", [("bf16", 128, 8, 1), ("bf16", 128, 4, 0), ("f16", 128, 8, 3),
+                                                 ("f16", 96, 4, 1), ("bf16", 64, 8, 2), ("bf16", 96, 8, 0)])
+def test_quantized_decode_matches_oracle(dtype, d, bits, splits):
+    import paged_prefix_reuse_gb300 as kvp
+
+    contexts = [700, 31, 1500, 2, 257, 16, 999]
+    w, st, qp, oq, bt, qpages, kb, vb = _decode_case(100 + d + bits, contexts, dtype, d, 10, 2, bits,
+                                                     qfrac=[1.0, 0.5, 0.9, 0.0, 1.0, 1.0, 0.3])
+    tq = torch.from_numpy(qpages).cuda()
+    tbt = torch.from_numpy(bt).cuda()
+    q = st.q[st.tq:]
+    out, lse = kvp.kvp_decode_attn_q(st.pool, qp, tq, q, st.ctx, tbt, st.max_ctx_dec, w.softmax_scale,
+                                     num_splits=splits)
+    torch.cuda.synchronize()
+    assert st.pool.errors() == 0
+    want, want_lse = quant.decode_attn_q(dtype, oq, bits, kb, vb, w.q[st.tq:], w.context_lens, bt, qpages,
+                                         w.softmax_scale)
+    o = out.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(o).all()
+    err = np.abs(o - want).max()
+    lerr = np.abs(lse.cpu().numpy().T.astype(np.float64) - want_lse).max()
+    assert err <= TOL[dtype], err
+    assert lerr <= LSE_TOL, lerr
+
+
+def test_quantized_decode_without_quantized_pages_equals_16bit_decode():
+    """qpages = 0 everywhere: the quantized entry point takes the 16-bit path
+    for every page and must reproduce kvp_decode_attn bit for bit."""
+    import paged_prefix_reuse_gb300 as kvp
+
+    w, st, qp, oq, bt, qpages, kb, vb = _decode_case(7, [300, 45, 1024], "bf16", 128, 8, 2, 8, qfrac=[0.0])
+    q = st.q[st.tq:]
+    a, la = kvp.kvp_decode_attn(st.pool, q, st.ctx, st.bt, st.max_ctx_dec, w.softmax_scale, num_splits=2)
+    b, lb = kvp.kvp_decode_attn_q(st.pool, qp, torch.zeros(3, dtype=torch.int32, device="cuda"), q, st.ctx, st.bt,
+                                  st.max_ctx_dec, w.softmax_scale, num_splits=2)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(la, lb)
+
+
+def test_quantized_decode_clamps_qpages_and_ignores_codes_past_the_context():
+    """qpages larger than the page count is clamped; a fully quantized last
+    page that is only partly inside the context (its codes past the context
+    are garbage) still gives the oracle's result."""
+    import paged_prefix_reuse_gb300 as kvp
+
+    contexts = [37, 100, 16]
+    w, st, qp, oq, bt, qpages, kb, vb = _decode_case(9, contexts, "f16", 64, 4, 2, 8, qfrac=[1.0],
+                                                     garbage_codes=True)
+    big = torch.tensor([100, 100, 100], dtype=torch.int32, device="cuda")
+    out, lse = kvp.kvp_decode_attn_q(st.pool, qp, big, st.q[st.tq:], st.ctx, torch.from_numpy(bt).cuda(),
+                                     st.max_ctx_dec, w.softmax_scale, num_splits=1)
+    torch.cuda.synchronize()
+    want, want_lse = quant.decode_attn_q("f16", oq, 8, kb, vb, w.q[st.tq:], w.context_lens, bt, qpages,
+                                         w.softmax_scale)
+    assert np.abs(out.float().cpu().numpy() - want).max() <= TOL["f16"]
+    assert np.abs(lse.cpu().numpy().T - want_lse).max() <= LSE_TOL
+
+
+def test_quantized_decode_bad_block_is_flagged_not_faulted():
+    import paged_prefix_reuse_gb300 as kvp
+
+    w, st, qp, oq, bt, qpages, kb, vb = _decode_case(11, [200, 90], "bf16", 128, 4, 2, 8, qfrac=[1.0])
+    bt = bt.copy()
+    bt[0, 1] = qp.num_blocks + 5  # outside the quantized pool
+    out, _ = kvp.kvp_decode_attn_q(st.pool, qp, torch.from_numpy(qpages).cuda(), st.q[st.tq:], st.ctx,
+                                   torch.from_numpy(bt).cuda(), st.max_ctx_dec, w.softmax_scale, num_splits=1)
+    torch.cuda.synchronize()
+    assert st.pool.errors() & kvp.DEVERR["bad_block"]
+    assert torch.isfinite(out[1].float()).all()
+
+
+def test_quantized_range_overflow_is_flagged():
+    import paged_prefix_reuse_gb300 as kvp
+
+    kb = wl.round_to_bits(np.full((2, 1, 16, 64), 1.0, np.float32), "bf16")
+    kb[0, 0, 3, 5] = wl.round_to_bits(np.array([-1e6], np.float32), "bf16")[0]  # min beyond fp16
+    pool = kvp.PagedKVPool(torch.from_numpy(kb.view(np.int16)).view(torch.bfloat16).cuda(),
+                           torch.from_numpy(kb.view(np.int16)).view(torch.bfloat16).cuda())
+    qp = kvp.QuantKVPool.like(pool, 2, 8)
+    kvp.kvp_quantize_blocks(pool, qp, torch.tensor([[0, 1]], dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert pool.errors() & 0x20
