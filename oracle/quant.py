@@ -14,10 +14,10 @@ give nothing more, so these readings are taken:
   the head_dim channels.
 * Asymmetric min/max quantization (KIVI's): levels = 2^bits - 1,
   s = (max - min) / levels, code = clamp(round((x - min) / s), 0, levels),
-  x' = code * s + min, delivered in the cache's 16-bit dtype (the type the
-  cached tensors are consumed in): code * s + min is exact in fp32 terms
-  (an 8-bit code times an fp16 scale plus an fp16 min), rounded to fp32 and
-  then to fp16/bf16, both to nearest even.
+  x' = code * s + min, exactly: the quantized cache stands for these values,
+  and an implementation's own rounding of them (the CUDA kernel computes
+  them in fp16, unit roundoff 2^-11) is part of its error, not of the
+  method.
 * s and min are stored as fp16: s rounded up and min rounded down, so that
   the grid still spans the group; the codes are computed against the stored
   (rounded) values, in fp32: d = x - z, q = d / s, code = round-half-even(q),
@@ -123,25 +123,14 @@ def quantize_blocks(dtype: str, k_pool, v_pool, qpool, bits: int, pairs):
     return (kc, vc, km, vm), bad
 
 
-def to_dtype(x: np.ndarray, dtype: str) -> np.ndarray:
-    """Round to fp32, then to the 16-bit type (nearest even); float64 out."""
-    x32 = np.asarray(x, dtype=np.float64).astype(np.float32)
-    if dtype == "f16":
-        return x32.astype(np.float16).astype(np.float64)
-    b = x32.view(np.uint32).astype(np.uint64)
-    r = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16) & 0xFFFF
-    return (r.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-
-
-def dequantize_block(qpool, bits: int, blk: int, head_dim: int, dtype: str):
-    """K, V of one quantized block as float64 [Hkv, bs, d]: code * s + min,
-    in the pool's 16-bit dtype."""
+def dequantize_block(qpool, bits: int, blk: int, head_dim: int):
+    """K, V of one quantized block as float64 [Hkv, bs, d]: code * s + min."""
     kc, vc, km, vm = qpool
     K = unpack_codes(kc[blk], bits, head_dim).astype(np.float64)
     V = unpack_codes(vc[blk], bits, head_dim).astype(np.float64)
     K = K * km[blk, :, 0, :].astype(np.float64)[:, None, :] + km[blk, :, 1, :].astype(np.float64)[:, None, :]
     V = V * vm[blk, :, :, 0].astype(np.float64)[:, :, None] + vm[blk, :, :, 1].astype(np.float64)[:, :, None]
-    return to_dtype(K, dtype), to_dtype(V, dtype)
+    return K, V
 
 
 def decode_attn_q(dtype: str, qpool, bits: int, k_pool, v_pool, q, context_lens, block_tables, qpages, scale):
@@ -162,7 +151,7 @@ def decode_attn_q(dtype: str, qpool, bits: int, k_pool, v_pool, q, context_lens,
         for p in range(npg):
             blk = int(block_tables[b][p])
             if p < int(qpages[b]):
-                K, V = dequantize_block(qpool, bits, blk, d, dtype)
+                K, V = dequantize_block(qpool, bits, blk, d)
             else:
                 K = decode_bits(k_pool[blk], dtype).astype(np.float64)
                 V = decode_bits(v_pool[blk], dtype).astype(np.float64)
