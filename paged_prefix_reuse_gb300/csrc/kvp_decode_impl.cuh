@@ -44,67 +44,114 @@ struct DecodeCfg {
     static constexpr int SMEM_BYTES = OFF_BAR + 2 * NS * 8 + 16 + 1024;
 };
 
-// 8 codes -> 8 exact floats: 2^23 + code is assembled in the bit pattern
-// (the code in the low mantissa byte under exponent 150), then 2^23 is
-// subtracted.  8 bits: one byte per channel; 4 bits: the even channel in the
-// low nibble of each byte.
+// Two codes -> half2 (1024 + c0, 1024 + c1): exact, since fp16 has unit
+// spacing on [1024, 2048).  The codes sit in bytes i and j of w; every byte
+// of the constant source is 0x64, the high byte of 1024.0 in fp16.
+__device__ __forceinline__ uint32_t magic_pair(uint32_t w, uint32_t sel) {
+    return __byte_perm(w, 0x64646464u, sel);
+}
+
+// Dequantize one 8-channel unit: codes -> fp16 (1024 + c) - 1024, then
+// c * s + z in one fp16 fused multiply-add per pair (a single rounding).
+// 8 bits: 8 code bytes; 4 bits: 8 nibbles, the even channel in the low one.
 template <int BITS>
-__device__ __forceinline__ void codes8(const uint8_t* p, float (&f)[8]) {
-    constexpr uint32_t kMagic = 0x4B000000u;
+__device__ __forceinline__ uint4 dequant_unit(const uint8_t* codes, const uint32_t (&s2)[4], const uint32_t (&z2)[4]) {
+    uint32_t h[4];
     if constexpr (BITS == 8) {
-        const uint2 w = *reinterpret_cast<const uint2*>(p);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            f[j] = __int_as_float(__byte_perm(w.x, kMagic, 0x7440 | j)) - 8388608.f;
-            f[4 + j] = __int_as_float(__byte_perm(w.y, kMagic, 0x7440 | j)) - 8388608.f;
-        }
+        const uint2 w = *reinterpret_cast<const uint2*>(codes);
+        h[0] = magic_pair(w.x, 0x4140);
+        h[1] = magic_pair(w.x, 0x4342);
+        h[2] = magic_pair(w.y, 0x4140);
+        h[3] = magic_pair(w.y, 0x4342);
     } else {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
-        const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            f[2 * j] = __int_as_float(__byte_perm(lo, kMagic, 0x7440 | j)) - 8388608.f;
-            f[2 * j + 1] = __int_as_float(__byte_perm(hi, kMagic, 0x7440 | j)) - 8388608.f;
-        }
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(codes);
+        const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;  // even / odd channels
+        const uint32_t t = __byte_perm(lo, hi, 0x5140), u = __byte_perm(lo, hi, 0x7362);  // c0..c3, c4..c7
+        h[0] = magic_pair(t, 0x4140);
+        h[1] = magic_pair(t, 0x4342);
+        h[2] = magic_pair(u, 0x4140);
+        h[3] = magic_pair(u, 0x4342);
     }
+    const __half2 k1024 = __float2half2_rn(1024.f);
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const __half2 c = __hsub2(*reinterpret_cast<const __half2*>(&h[j]), k1024);
+        const __half2 x = __hfma2(c, *reinterpret_cast<const __half2*>(&s2[j]), *reinterpret_cast<const __half2*>(&z2[j]));
+        o[j] = *reinterpret_cast<const uint32_t*>(&x);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // Dequantize one quantized stage (SK keys of one kv head) into the warp's
-// 16-bit K and V tiles, in the chunked, swizzled layout the TMA path gives:
-// x = code * scale + min in fp32 (K scale/min per channel, V per token),
-// rounded to the pool dtype.  Keys at or past nvalid become zeros.
-template <bool kBF16, int D, int SK, int BITS>
+// fp16 K and V tiles, in the chunked, swizzled layout the TMA path gives.
+// K scale/min are per channel (a lane's channels are fixed across its keys
+// when 32 is a multiple of the units per row), V's per token.  Keys at or
+// past nvalid become zeros.
+template <int D, int SK, int BITS>
 __device__ __forceinline__ void dequant_stage(const uint8_t* qs, uint8_t* stk, uint8_t* stv, int nvalid, int lane) {
     using C = DecodeCfg<D, SK, BITS>;
-    constexpr int U = D / 8;               // 16-byte output units per row
-    constexpr int CROW = D * BITS / 8;     // code bytes per row
+    constexpr int U = D / 8;            // 16-byte output units per row
+    constexpr int CROW = D * BITS / 8;  // code bytes per row
     const uint8_t* kc = qs;
     const uint8_t* vc = qs + C::QOFF_V;
     const __half* km = reinterpret_cast<const __half*>(qs + C::QOFF_KM);
-    const __half* vm = reinterpret_cast<const __half*>(qs + C::QOFF_VM);
-    for (int e = lane; e < SK * U; e += 32) {
+    const __half2* vm = reinterpret_cast<const __half2*>(qs + C::QOFF_VM);
+    uint32_t ks[4], kz[4];
+    auto load_kmeta = [&](int u) {
+        const uint4 a = *reinterpret_cast<const uint4*>(km + u * 8);
+        const uint4 b = *reinterpret_cast<const uint4*>(km + D + u * 8);
+        ks[0] = a.x; ks[1] = a.y; ks[2] = a.z; ks[3] = a.w;
+        kz[0] = b.x; kz[1] = b.y; kz[2] = b.z; kz[3] = b.w;
+    };
+    constexpr bool kFixedUnit = (32 % U) == 0;
+    if constexpr (kFixedUnit) load_kmeta(lane % U);
+    static_assert((SK * U) % 32 == 0, "whole units per lane");
+#pragma unroll
+    for (int it = 0; it < SK * U / 32; ++it) {
+        const int e = lane + 32 * it;
         const int key = e / U, u = e - (e / U) * U;
+        if constexpr (!kFixedUnit) load_kmeta(u);
         uint4 ko = make_uint4(0, 0, 0, 0), vo = make_uint4(0, 0, 0, 0);
         if (key < nvalid) {
-            float kf[8], vf[8];
-            codes8<BITS>(kc + key * CROW + u * BITS, kf);
-            codes8<BITS>(vc + key * CROW + u * BITS, vf);
-            const uint4 s4 = *reinterpret_cast<const uint4*>(km + u * 8);
-            const uint4 z4 = *reinterpret_cast<const uint4*>(km + D + u * 8);
-            const uint32_t sw[4] = {s4.x, s4.y, s4.z, s4.w}, zw[4] = {z4.x, z4.y, z4.z, z4.w};
-            const float2 vsz = __half22float2(*reinterpret_cast<const __half2*>(vm + 2 * key));
-            uint32_t kp[4], vp[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 sj = __half22float2(*reinterpret_cast<const __half2*>(&sw[j]));
-                const float2 zj = __half22float2(*reinterpret_cast<const __half2*>(&zw[j]));
-                kp[j] = pack2<kBF16>(fmaf(kf[2 * j], sj.x, zj.x), fmaf(kf[2 * j + 1], sj.y, zj.y));
-                vp[j] = pack2<kBF16>(fmaf(vf[2 * j], vsz.x, vsz.y), fmaf(vf[2 * j + 1], vsz.x, vsz.y));
-            }
-            ko = make_uint4(kp[0], kp[1], kp[2], kp[3]);
-            vo = make_uint4(vp[0], vp[1], vp[2], vp[3]);
+            ko = dequant_unit<BITS>(kc + key * CROW + u * BITS, ks, kz);
+            const __half2 sz = vm[key];  // (scale, min) of this token
+            const __half2 s = __low2half2(sz), z = __high2half2(sz);
+            const uint32_t s1 = *reinterpret_cast<const uint32_t*>(&s), z1 = *reinterpret_cast<const uint32_t*>(&z);
+            const uint32_t vs[4] = {s1, s1, s1, s1}, vz[4] = {z1, z1, z1, z1};
+            vo = dequant_unit<BITS>(vc + key * CROW + u * BITS, vs, vz);
         }
         const int off = (u / (C::CW / 8)) * C::REGION + swz_offset(key, u % (C::CW / 8), C::ROWB);
+        *reinterpret_cast<uint4*>(stk + off) = ko;
+        *reinterpret_cast<uint4*>(stv + off) = vo;
+    }
+}
+
+// A 16-bit bf16 stage (the live suffix of a bf16 pool) converted to fp16 for
+// the fp16 products of the quantized-prefix kernel; keys at or past nvalid
+// become zeros.  Same swizzled layout in and out.
+template <int D, int SK, int BITS>
+__device__ __forceinline__ void bf16_stage_to_f16(const uint8_t* kin, const uint8_t* vin, uint8_t* stk, uint8_t* stv,
+                                                  int nvalid, int lane) {
+    using C = DecodeCfg<D, SK, BITS>;
+    constexpr int U = D / 8;
+#pragma unroll
+    for (int it = 0; it < SK * U / 32; ++it) {
+        const int e = lane + 32 * it;
+        const int key = e / U, u = e - (e / U) * U;
+        const int off = (u / (C::CW / 8)) * C::REGION + swz_offset(key, u % (C::CW / 8), C::ROWB);
+        uint4 ko = make_uint4(0, 0, 0, 0), vo = make_uint4(0, 0, 0, 0);
+        if (key < nvalid) {
+            const uint4 a = *reinterpret_cast<const uint4*>(kin + off), b = *reinterpret_cast<const uint4*>(vin + off);
+            ko = make_uint4(pack2<false>(unpack2<true>(a.x).x, unpack2<true>(a.x).y),
+                            pack2<false>(unpack2<true>(a.y).x, unpack2<true>(a.y).y),
+                            pack2<false>(unpack2<true>(a.z).x, unpack2<true>(a.z).y),
+                            pack2<false>(unpack2<true>(a.w).x, unpack2<true>(a.w).y));
+            vo = make_uint4(pack2<false>(unpack2<true>(b.x).x, unpack2<true>(b.x).y),
+                            pack2<false>(unpack2<true>(b.y).x, unpack2<true>(b.y).y),
+                            pack2<false>(unpack2<true>(b.z).x, unpack2<true>(b.z).y),
+                            pack2<false>(unpack2<true>(b.w).x, unpack2<true>(b.w).y));
+        }
         *reinterpret_cast<uint4*>(stk + off) = ko;
         *reinterpret_cast<uint4*>(stv + off) = vo;
     }
@@ -149,6 +196,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 4)
                   const DecodeParams p) {
     using C = DecodeCfg<D, SK, BITS>;
     static_assert(BITS == 0 || BITS == 4 || BITS == 8, "bits");
+    // The quantized-prefix kernel runs its tensor-core products in fp16
+    // whatever the pool dtype (fp16 holds the dequantized values and a bf16
+    // pool's values more closely than bf16); the output keeps the pool dtype.
+    constexpr bool kMma = BITS ? false : kBF16;
     constexpr int kStageKeys = SK;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
@@ -274,6 +325,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 4)
             qa[ks][1] = r1 < g ? __ldg(q32 + (qrow1 + ks * 16 + cq) / 2) : 0u;
             qa[ks][2] = r0 < g ? __ldg(q32 + (qrow0 + ks * 16 + cq + 8) / 2) : 0u;
             qa[ks][3] = r1 < g ? __ldg(q32 + (qrow1 + ks * 16 + cq + 8) / 2) : 0u;
+            if constexpr (kMma != kBF16) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 f = unpack2<kBF16>(qa[ks][j]);
+                    qa[ks][j] = pack2<kMma>(f.x, f.y);
+                }
+            }
         }
         const float sl2 = p.scale_log2;
 
@@ -285,19 +343,23 @@ __global__ void __launch_bounds__(kDecodeThreads, 4)
             const int kbeg = key0 + i * kStageKeys;
             const int nvalid = min(kStageKeys, key1 - kbeg);
             const bool qst = BITS > 0 && page0 + i < qp;
+            // Staged: dequantized (or converted to fp16) into this warp's own
+            // tile, after which the slot goes back at once.
+            const bool staged = BITS > 0 && (qst || kBF16);
             if constexpr (BITS > 0) {
-                if (qst) {
-                    // Dequantize into this warp's own tile, then hand the slot
-                    // back at once: the codes are no longer needed.
+                if (staged) {
                     uint8_t* stk = smem + C::OFF_STG + warp * C::STG_BYTES;
-                    dequant_stage<kBF16, D, SK, BITS>(kst, stk, stk + C::KBYTES, nvalid, lane);
+                    if (qst)
+                        dequant_stage<D, SK, BITS>(kst, stk, stk + C::KBYTES, nvalid, lane);
+                    else
+                        bf16_stage_to_f16<D, SK, BITS>(kst, vst, stk, stk + C::KBYTES, nvalid, lane);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[slot]);
                     kst = stk;
                     vst = stk + C::KBYTES;
                 }
             }
-            if (!qst && nvalid < kStageKeys) {
+            if (!staged && nvalid < kStageKeys) {
                 // Rows past the context may hold any bytes (even NaN); P is 0
                 // there, but 0 * NaN is NaN, so clear those V rows.
                 const int vecs_per_row = C::ROWB / 16;
@@ -329,8 +391,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 4)
                                           swz_offset(key, c16 % (C::CW / 8), C::ROWB);
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4(addr, b0, b1, b2, b3);
-                    mma16816<kBF16>(s[2 * np], qa[ks], b0, b1);
-                    mma16816<kBF16>(s[2 * np + 1], qa[ks], b2, b3);
+                    mma16816<kMma>(s[2 * np], qa[ks], b0, b1);
+                    mma16816<kMma>(s[2 * np + 1], qa[ks], b2, b3);
                 }
             }
             if (nvalid < kStageKeys) {
@@ -351,12 +413,23 @@ __global__ void __launch_bounds__(kDecodeThreads, 4)
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            const float mn0 = fmaxf(m_run[0], mx0 * sl2);
-            const float mn1 = fmaxf(m_run[1], mx1 * sl2);
-            const float a0 = fast_exp2(m_run[0] - mn0);
-            const float a1 = fast_exp2(m_run[1] - mn1);
-            m_run[0] = mn0;
-            m_run[1] = mn1;
+            // Lazy reference maximum: it moves (and O, l are rescaled) only
+            // when a row maximum grows by more than 2^8; exps against a stale
+            // reference stay <= 2^8, and the final 1/l uses the same one.
+            const float mx0s = mx0 * sl2, mx1s = mx1 * sl2;
+            float a0 = 1.f, a1 = 1.f;
+            if (mx0s > m_run[0] + 8.f) {
+                a0 = fast_exp2(m_run[0] - mx0s);
+                m_run[0] = mx0s;
+                l_run[0] *= a0;
+            }
+            if (mx1s > m_run[1] + 8.f) {
+                a1 = fast_exp2(m_run[1] - mx1s);
+                m_run[1] = mx1s;
+                l_run[1] *= a1;
+            }
+            const float mn0 = m_run[0] == -INFINITY ? 0.f : m_run[0];
+            const float mn1 = m_run[1] == -INFINITY ? 0.f : m_run[1];
             float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
@@ -367,22 +440,24 @@ __global__ void __launch_bounds__(kDecodeThreads, 4)
                 ps0 += s[nt][0] + s[nt][1];
                 ps1 += s[nt][2] + s[nt][3];
             }
-            l_run[0] = l_run[0] * a0 + ps0;
-            l_run[1] = l_run[1] * a1 + ps1;
+            l_run[0] += ps0;
+            l_run[1] += ps1;
+            if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
-            for (int nd = 0; nd < D / 8; ++nd) {
-                o[nd][0] *= a0;
-                o[nd][1] *= a0;
-                o[nd][2] *= a1;
-                o[nd][3] *= a1;
+                for (int nd = 0; nd < D / 8; ++nd) {
+                    o[nd][0] *= a0;
+                    o[nd][1] *= a0;
+                    o[nd][2] *= a1;
+                    o[nd][3] *= a1;
+                }
             }
             uint32_t pa[SK / 16][4];
 #pragma unroll
             for (int kk = 0; kk < SK / 16; ++kk) {
-                pa[kk][0] = pack2<kBF16>(s[2 * kk][0], s[2 * kk][1]);
-                pa[kk][1] = pack2<kBF16>(s[2 * kk][2], s[2 * kk][3]);
-                pa[kk][2] = pack2<kBF16>(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-                pa[kk][3] = pack2<kBF16>(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+                pa[kk][0] = pack2<kMma>(s[2 * kk][0], s[2 * kk][1]);
+                pa[kk][1] = pack2<kMma>(s[2 * kk][2], s[2 * kk][3]);
+                pa[kk][2] = pack2<kMma>(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+                pa[kk][3] = pack2<kMma>(s[2 * kk + 1][2], s[2 * kk + 1][3]);
             }
             // O += P V: V is [key][dim] in shared memory, loaded transposed.
 #pragma unroll
@@ -395,11 +470,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 4)
                                           swz_offset(key, c16 % (C::CW / 8), C::ROWB);
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4_t(addr, b0, b1, b2, b3);
-                    mma16816<kBF16>(o[2 * nd2], pa[kk], b0, b1);
-                    mma16816<kBF16>(o[2 * nd2 + 1], pa[kk], b2, b3);
+                    mma16816<kMma>(o[2 * nd2], pa[kk], b0, b1);
+                    mma16816<kMma>(o[2 * nd2 + 1], pa[kk], b2, b3);
                 }
             }
-            if (!qst) {
+            if (!staged) {
                 if (nvalid < kStageKeys) fence_proxy_async_smem();  // generic zeroing before the next TMA write
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[slot]);
