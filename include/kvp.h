@@ -57,7 +57,8 @@ typedef enum {
     KVP_ERR_UNSUPPORTED = 2, /* head_dim not 64/96/128, dtype, block_size not 8/16/32 */
     KVP_ERR_WORKSPACE = 3,   /* workspace missing or smaller than kvp_workspace_size() */
     KVP_ERR_CUDA = 4,        /* a CUDA runtime/driver call or launch failed */
-    KVP_ERR_TIMEOUT = 5      /* reserved for host-side reporting of KVP_DEVERR_TIMEOUT */
+    KVP_ERR_TIMEOUT = 5,     /* reserved for host-side reporting of KVP_DEVERR_TIMEOUT */
+    KVP_ERR_NO_BLOCKS = 6    /* block manager: too few free or evictable blocks (state unchanged) */
 } kvp_status;
 
 typedef enum { KVP_F16 = 0, KVP_BF16 = 1 } kvp_dtype;

@@ -27,6 +27,9 @@ __all__ = [
     "PagedKVPool",
     "HostKVPool",
     "QuantKVPool",
+    "BlockManager",
+    "NoBlocks",
+    "kvp_hash_chunks",
     "EXPORTED_SYMBOLS",
     "lib_path",
     "load_library",
@@ -71,6 +74,21 @@ EXPORTED_SYMBOLS = (
     "kvp_workspace_size",
     "kvp_status_string",
     "kvp_version",
+)
+
+# Host block manager entry points (include/kvp_blockmgr.h).
+BLOCKMGR_SYMBOLS = (
+    "kvp_bm_create",
+    "kvp_bm_destroy",
+    "kvp_hash_chunks",
+    "kvp_bm_admit",
+    "kvp_bm_append",
+    "kvp_bm_fork",
+    "kvp_bm_finish",
+    "kvp_bm_table",
+    "kvp_bm_evict_one",
+    "kvp_bm_stats",
+    "kvp_bm_audit",
 )
 
 
@@ -146,6 +164,25 @@ def load_library():
         lib.kvp_prefix_attn.argtypes = [PP, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, i32, P, sz, P]
         lib.kvp_decode_attn.argtypes = [PP, P, P, P, P, P, i32, i32, i32, i32, f32, i32, P, sz, P]
         lib.kvp_decode_attn_noalloc.argtypes = [PP, P, P, P, P, P, i32, i32, i32, i32, f32, i32, P]
+        i64p, i32p, i8p = ctypes.POINTER(i64), ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_int8)
+        lib.kvp_bm_create.argtypes = [i64, i32, i32]
+        lib.kvp_bm_create.restype = P
+        lib.kvp_bm_destroy.argtypes = [P]
+        lib.kvp_bm_destroy.restype = None
+        lib.kvp_hash_chunks.argtypes = [i32p, i64, i32, P, P]
+        lib.kvp_hash_chunks.restype = i64
+        lib.kvp_bm_admit.argtypes = [P, i64, i32p, i64, i32p, i32, i64p, i8p, i64]
+        lib.kvp_bm_append.argtypes = [P, i64, i64, i32p, i32, i32p, i32, i32p]
+        lib.kvp_bm_fork.argtypes = [P, i64, i64]
+        lib.kvp_bm_finish.argtypes = [P, i64, i32p, i64]
+        lib.kvp_bm_table.argtypes = [P, i64, i32p, i32, i64p]
+        lib.kvp_bm_evict_one.argtypes = [P]
+        lib.kvp_bm_evict_one.restype = i32
+        lib.kvp_bm_stats.argtypes = [P, i64p]
+        lib.kvp_bm_stats.restype = None
+        lib.kvp_bm_audit.argtypes = [P]
+        for name in ("kvp_bm_admit", "kvp_bm_append", "kvp_bm_fork", "kvp_bm_finish", "kvp_bm_table", "kvp_bm_audit"):
+            getattr(lib, name).restype = ctypes.c_int
         for name in ("kvp_slot_mapping", "kvp_cache_append", "kvp_block_copy", "kvp_block_swap",
                      "kvp_quantize_blocks", "kvp_prefix_attn", "kvp_decode_attn", "kvp_decode_attn_q",
                      "kvp_decode_attn_noalloc"):
@@ -307,6 +344,113 @@ def kvp_decode_attn_q(pool: PagedKVPool, qpool: QuantKVPool, qpages: torch.Tenso
                                  float(softmax_scale), int(splits), _ptr(workspace), ws_bytes, _stream(stream)),
            "kvp_decode_attn_q")
     return out, lse
+
+
+KVP_ERR_NO_BLOCKS = 6
+
+
+class NoBlocks(KvpError):
+    """The block manager could not supply enough blocks, even after eviction
+    (its state is unchanged)."""
+
+
+def kvp_hash_chunks(tokens, chunk_size: int):
+    """The two-level hashes of the full chunks: (prefix_hashes, content_hashes),
+    lists of 32-byte digests (see kvp_blockmgr.h)."""
+    import numpy as np
+
+    t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+    nc = len(t) // chunk_size
+    pre = ctypes.create_string_buffer(32 * max(nc, 1))
+    con = ctypes.create_string_buffer(32 * max(nc, 1))
+    got = load_library().kvp_hash_chunks(t.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), len(t), chunk_size,
+                                          pre, con)
+    if got < 0:
+        raise ValueError("bad arguments")
+    return [pre.raw[32 * c:32 * c + 32] for c in range(got)], [con.raw[32 * c:32 * c + 32] for c in range(got)]
+
+
+class BlockManager:
+    """Host block manager (include/kvp_blockmgr.h): chunk hashing and prefix
+    reuse, page allocation, copy-on-write forks, registration and eviction.
+    Sequence ids are integers chosen by the caller."""
+
+    def __init__(self, num_blocks: int, block_size: int, chunk_size: int, max_blocks_per_seq: int = 4096):
+        self._lib = load_library()
+        self._h = self._lib.kvp_bm_create(num_blocks, block_size, chunk_size)
+        if not self._h:
+            raise ValueError("bad block manager sizes")
+        self.num_blocks, self.block_size, self.chunk_size = num_blocks, block_size, chunk_size
+        self.max_blocks = max_blocks_per_seq
+
+    def __del__(self):
+        h, self._h = getattr(self, "_h", None), None
+        if h:
+            self._lib.kvp_bm_destroy(h)
+
+    @staticmethod
+    def _i32(a):
+        import numpy as np
+
+        a = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+        return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+    def _status(self, st, where):
+        if st == KVP_ERR_NO_BLOCKS:
+            raise NoBlocks(st, where)
+        _check(st, where)
+
+    def admit(self, seq: int, tokens):
+        """-> (table list, cached_tokens, match kinds per full chunk)."""
+        import numpy as np
+
+        t, tp = self._i32(tokens)
+        table, tbp = self._i32(np.full(self.max_blocks, -1))
+        cached = ctypes.c_int64(0)
+        nc = max(1, len(t) // self.chunk_size)
+        kinds = (ctypes.c_int8 * nc)()
+        self._status(self._lib.kvp_bm_admit(self._h, seq, tp, len(t), tbp, self.max_blocks, ctypes.byref(cached),
+                                            kinds, nc), "kvp_bm_admit")
+        n = int((table >= 0).sum())
+        return table[:n].tolist(), int(cached.value), list(kinds)[: len(t) // self.chunk_size]
+
+    def append(self, seq: int, n: int):
+        """-> (table list, copy-on-write pairs [(src, dst)])."""
+        import numpy as np
+
+        table, tbp = self._i32(np.full(self.max_blocks, -1))
+        pairs, pp = self._i32(np.zeros(2))
+        npairs = ctypes.c_int32(0)
+        self._status(self._lib.kvp_bm_append(self._h, seq, n, tbp, self.max_blocks, pp, 1, ctypes.byref(npairs)),
+                     "kvp_bm_append")
+        k = int((table >= 0).sum())
+        return table[:k].tolist(), [tuple(pairs.tolist())] if npairs.value else []
+
+    def fork(self, parent: int, child: int):
+        self._status(self._lib.kvp_bm_fork(self._h, parent, child), "kvp_bm_fork")
+
+    def finish(self, seq: int, tokens):
+        t, tp = self._i32(tokens)
+        self._status(self._lib.kvp_bm_finish(self._h, seq, tp, len(t)), "kvp_bm_finish")
+
+    def table(self, seq: int):
+        import numpy as np
+
+        table, tbp = self._i32(np.full(self.max_blocks, -1))
+        n = ctypes.c_int64(0)
+        self._status(self._lib.kvp_bm_table(self._h, seq, tbp, self.max_blocks, ctypes.byref(n)), "kvp_bm_table")
+        return table[: int((table >= 0).sum())].tolist(), int(n.value)
+
+    def evict_one(self) -> bool:
+        return bool(self._lib.kvp_bm_evict_one(self._h))
+
+    def stats(self) -> dict:
+        out = (ctypes.c_int64 * 5)()
+        self._lib.kvp_bm_stats(self._h, out)
+        return dict(zip(("free", "cached", "used", "hits", "misses"), list(out)))
+
+    def audit(self) -> bool:
+        return self._lib.kvp_bm_audit(self._h) == 0
 
 
 class HostKVPool:

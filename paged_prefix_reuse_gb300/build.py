@@ -1,6 +1,6 @@
 """Build libkvp.so in-tree with nvcc for sm_103a (no cmake, no torch extension).
 
-Each .cu file is compiled to an object in parallel, then linked into
+Each .cu (and host-only .cpp) file is compiled to an object in parallel, then linked into
 ``paged_prefix_reuse_gb300/libkvp.so``.  Run ``python -m
 paged_prefix_reuse_gb300.build`` or call :func:`build_library`.
 """
@@ -40,7 +40,7 @@ def nvcc() -> str:
 
 
 def sources() -> list[str]:
-    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cpp")))
 
 
 def _stale(lib: str) -> bool:
@@ -48,7 +48,7 @@ def _stale(lib: str) -> bool:
         return True
     t = os.path.getmtime(lib)
     deps = sources() + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
-    deps.append(os.path.join(INCLUDE, "kvp.h"))
+    deps += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     deps.append(os.path.abspath(__file__))
     return any(os.path.getmtime(d) > t for d in deps)
 
@@ -60,7 +60,7 @@ def build_library(force: bool = False, verbose: bool = False, ptxas_info: bool =
     cc = nvcc()
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [cc] + NVCC_FLAGS + (["-Xptxas", "-v"] if ptxas_info else []) + ["-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)

@@ -108,6 +108,7 @@ const char* kvp_status_string(kvp_status status) {
         case KVP_ERR_WORKSPACE: return "workspace missing or too small";
         case KVP_ERR_CUDA: return "CUDA error";
         case KVP_ERR_TIMEOUT: return "an in-kernel wait timed out";
+        case KVP_ERR_NO_BLOCKS: return "too few free or evictable blocks";
         default: return "unknown status";
     }
 }
