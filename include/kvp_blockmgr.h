@@ -69,6 +69,16 @@ kvp_status kvp_bm_admit(kvp_block_manager *bm, int64_t seq, const int32_t *token
 kvp_status kvp_bm_append(kvp_block_manager *bm, int64_t seq, int64_t n, int32_t *table, int32_t max_blocks,
                          int32_t *cow_pairs, int32_t max_pairs, int32_t *n_pairs);
 
+/* One decode step for a batch: kvp_bm_append(seqs[i], n_tokens[i]) for i in
+ * order, writing sequence i's table to tables[i][0..max_blocks) (the
+ * [count][max_blocks] block-table array the device calls take) and its
+ * copy-on-write pair, if any, to the next free row of cow_pairs[count][2];
+ * *n_pairs counts them.  Stops at the first failure: *done is the number of
+ * sequences appended (all of them on KVP_OK), the rest unchanged. */
+kvp_status kvp_bm_append_batch(kvp_block_manager *bm, const int64_t *seqs, const int32_t *n_tokens, int32_t count,
+                               int32_t *tables, int32_t max_blocks, int32_t *cow_pairs, int32_t *n_pairs,
+                               int32_t *done);
+
 /* `child` (a new id) shares every block of `parent` (copy-on-write). */
 kvp_status kvp_bm_fork(kvp_block_manager *bm, int64_t parent, int64_t child);
 

@@ -83,6 +83,7 @@ BLOCKMGR_SYMBOLS = (
     "kvp_hash_chunks",
     "kvp_bm_admit",
     "kvp_bm_append",
+    "kvp_bm_append_batch",
     "kvp_bm_fork",
     "kvp_bm_finish",
     "kvp_bm_table",
@@ -173,6 +174,8 @@ def load_library():
         lib.kvp_hash_chunks.restype = i64
         lib.kvp_bm_admit.argtypes = [P, i64, i32p, i64, i32p, i32, i64p, i8p, i64]
         lib.kvp_bm_append.argtypes = [P, i64, i64, i32p, i32, i32p, i32, i32p]
+        lib.kvp_bm_append_batch.argtypes = [P, P, P, i32, P, i32, P, i32p, i32p]
+        lib.kvp_bm_append_batch.restype = ctypes.c_int
         lib.kvp_bm_fork.argtypes = [P, i64, i64]
         lib.kvp_bm_finish.argtypes = [P, i64, i32p, i64]
         lib.kvp_bm_table.argtypes = [P, i64, i32p, i32, i64p]
@@ -367,7 +370,8 @@ def kvp_hash_chunks(tokens, chunk_size: int):
                                           pre, con)
     if got < 0:
         raise ValueError("bad arguments")
-    return [pre.raw[32 * c:32 * c + 32] for c in range(got)], [con.raw[32 * c:32 * c + 32] for c in range(got)]
+    pr, cr = pre.raw, con.raw
+    return [pr[32 * c:32 * c + 32] for c in range(got)], [cr[32 * c:32 * c + 32] for c in range(got)]
 
 
 class BlockManager:
@@ -382,6 +386,12 @@ class BlockManager:
             raise ValueError("bad block manager sizes")
         self.num_blocks, self.block_size, self.chunk_size = num_blocks, block_size, chunk_size
         self.max_blocks = max_blocks_per_seq
+        import numpy as np
+
+        self._tbuf = np.full(max_blocks_per_seq, -1, dtype=np.int32)  # reused table buffer
+        self._tptr = self._tbuf.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+        self._pbuf = np.zeros(2, dtype=np.int32)
+        self._pptr = self._pbuf.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
 
     def __del__(self):
         h, self._h = getattr(self, "_h", None), None
@@ -392,8 +402,15 @@ class BlockManager:
     def _i32(a):
         import numpy as np
 
-        a = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+        if not (isinstance(a, np.ndarray) and a.dtype == np.int32 and a.flags.c_contiguous):
+            a = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
         return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+    def _table_list(self):
+        import numpy as np
+
+        neg = np.flatnonzero(self._tbuf < 0)
+        return self._tbuf[: neg[0] if len(neg) else len(self._tbuf)].tolist()
 
     def _status(self, st, where):
         if st == KVP_ERR_NO_BLOCKS:
@@ -405,26 +422,42 @@ class BlockManager:
         import numpy as np
 
         t, tp = self._i32(tokens)
-        table, tbp = self._i32(np.full(self.max_blocks, -1))
         cached = ctypes.c_int64(0)
         nc = max(1, len(t) // self.chunk_size)
         kinds = (ctypes.c_int8 * nc)()
-        self._status(self._lib.kvp_bm_admit(self._h, seq, tp, len(t), tbp, self.max_blocks, ctypes.byref(cached),
-                                            kinds, nc), "kvp_bm_admit")
-        n = int((table >= 0).sum())
-        return table[:n].tolist(), int(cached.value), list(kinds)[: len(t) // self.chunk_size]
+        self._status(self._lib.kvp_bm_admit(self._h, seq, tp, len(t), self._tptr, self.max_blocks,
+                                            ctypes.byref(cached), kinds, nc), "kvp_bm_admit")
+        return self._table_list(), int(cached.value), list(kinds)[: len(t) // self.chunk_size]
 
     def append(self, seq: int, n: int):
         """-> (table list, copy-on-write pairs [(src, dst)])."""
         import numpy as np
 
-        table, tbp = self._i32(np.full(self.max_blocks, -1))
-        pairs, pp = self._i32(np.zeros(2))
         npairs = ctypes.c_int32(0)
-        self._status(self._lib.kvp_bm_append(self._h, seq, n, tbp, self.max_blocks, pp, 1, ctypes.byref(npairs)),
-                     "kvp_bm_append")
-        k = int((table >= 0).sum())
-        return table[:k].tolist(), [tuple(pairs.tolist())] if npairs.value else []
+        self._status(self._lib.kvp_bm_append(self._h, seq, n, self._tptr, self.max_blocks, self._pptr, 1,
+                                             ctypes.byref(npairs)), "kvp_bm_append")
+        return self._table_list(), [tuple(self._pbuf.tolist())] if npairs.value else []
+
+    def append_batch(self, seqs, n_tokens, max_blocks: int | None = None):
+        """One decode step for many sequences: -> (tables int32 [count,
+        max_blocks] (-1 padded), cow_pairs int32 [k, 2]).  On running out of
+        blocks raises NoBlocks with ``.done`` = sequences appended."""
+        import numpy as np
+
+        mb = max_blocks or self.max_blocks
+        s = np.ascontiguousarray(np.asarray(seqs, dtype=np.int64))
+        n, np_ = self._i32(n_tokens)
+        tables = np.full((len(s), mb), -1, dtype=np.int32)
+        pairs = np.zeros((max(len(s), 1), 2), dtype=np.int32)
+        npairs, done = ctypes.c_int32(0), ctypes.c_int32(0)
+        st = self._lib.kvp_bm_append_batch(self._h, s.ctypes.data, n.ctypes.data, len(s), tables.ctypes.data, mb,
+                                           pairs.ctypes.data, ctypes.byref(npairs), ctypes.byref(done))
+        if st == KVP_ERR_NO_BLOCKS:
+            e = NoBlocks(st, "kvp_bm_append_batch")
+            e.done = int(done.value)
+            raise e
+        _check(st, "kvp_bm_append_batch")
+        return tables, pairs[: npairs.value]
 
     def fork(self, parent: int, child: int):
         self._status(self._lib.kvp_bm_fork(self._h, parent, child), "kvp_bm_fork")
@@ -436,10 +469,10 @@ class BlockManager:
     def table(self, seq: int):
         import numpy as np
 
-        table, tbp = self._i32(np.full(self.max_blocks, -1))
         n = ctypes.c_int64(0)
-        self._status(self._lib.kvp_bm_table(self._h, seq, tbp, self.max_blocks, ctypes.byref(n)), "kvp_bm_table")
-        return table[: int((table >= 0).sum())].tolist(), int(n.value)
+        self._status(self._lib.kvp_bm_table(self._h, seq, self._tptr, self.max_blocks, ctypes.byref(n)),
+                     "kvp_bm_table")
+        return self._table_list(), int(n.value)
 
     def evict_one(self) -> bool:
         return bool(self._lib.kvp_bm_evict_one(self._h))

@@ -61,7 +61,8 @@ def build_library(force: bool = False, verbose: bool = False, ptxas_info: bool =
 
     def compile_one(src: str) -> str:
         obj = os.path.join(BUILD_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
-        cmd = [cc] + NVCC_FLAGS + (["-Xptxas", "-v"] if ptxas_info else []) + ["-c", src, "-o", obj]
+        flags = NVCC_FLAGS + (["-Xcompiler", "-O3"] if src.endswith(".cpp") else [])
+        cmd = [cc] + flags + (["-Xptxas", "-v"] if ptxas_info else []) + ["-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
         r = subprocess.run(cmd, capture_output=True, text=True)

@@ -68,36 +68,68 @@ struct DigestHash {
     }
 };
 
-Digest sha256(const std::vector<uint8_t>& msg) {
+// Streaming SHA-256: 64-byte blocks are compressed straight from the input;
+// only the last partial block and the padding go through the buffer.
+struct Sha256 {
     uint32_t h[8] = {0x6a09e667, 0xbb67ae85, 0x3c6ef372, 0xa54ff53a, 0x510e527f, 0x9b05688c, 0x1f83d9ab, 0x5be0cd19};
-    const uint64_t bits = uint64_t(msg.size()) * 8;
-    std::vector<uint8_t> m(msg);
-    m.push_back(0x80);
-    while (m.size() % 64 != 56) m.push_back(0);
-    for (int i = 7; i >= 0; --i) m.push_back(uint8_t(bits >> (8 * i)));
-    for (size_t off = 0; off < m.size(); off += 64) sha256_block(h, m.data() + off);
-    Digest d;
-    for (int i = 0; i < 8; ++i)
-        for (int j = 0; j < 4; ++j) d.b[4 * i + j] = uint8_t(h[i] >> (24 - 8 * j));
-    return d;
-}
+    uint8_t buf[64];
+    size_t nbuf = 0;
+    uint64_t total = 0;
+    void update(const uint8_t* p, size_t n) {
+        total += n;
+        if (nbuf) {
+            const size_t k = n < 64 - nbuf ? n : 64 - nbuf;
+            std::memcpy(buf + nbuf, p, k);
+            nbuf += k;
+            p += k;
+            n -= k;
+            if (nbuf < 64) return;
+            sha256_block(h, buf);
+            nbuf = 0;
+        }
+        for (; n >= 64; p += 64, n -= 64) sha256_block(h, p);
+        std::memcpy(buf, p, n);
+        nbuf = n;
+    }
+    Digest final() {
+        const uint64_t bits = total * 8;
+        buf[nbuf++] = 0x80;
+        if (nbuf > 56) {
+            std::memset(buf + nbuf, 0, 64 - nbuf);
+            sha256_block(h, buf);
+            nbuf = 0;
+        }
+        std::memset(buf + nbuf, 0, 56 - nbuf);
+        for (int i = 0; i < 8; ++i) buf[56 + i] = uint8_t(bits >> (8 * (7 - i)));
+        sha256_block(h, buf);
+        Digest d;
+        for (int i = 0; i < 8; ++i)
+            for (int j = 0; j < 4; ++j) d.b[4 * i + j] = uint8_t(h[i] >> (24 - 8 * j));
+        return d;
+    }
+};
 
 // The full chunks' (prefix, content) hashes; tokens serialised little-endian.
 void hash_chunks(const int32_t* tokens, int64_t n, int32_t cs, std::vector<Digest>* pre, std::vector<Digest>* con) {
     const int64_t nc = n / cs;
     pre->resize(nc);
     con->resize(nc);
-    std::vector<uint8_t> data(size_t(cs) * 4), chained;
+    std::vector<uint8_t> data(size_t(cs) * 4);
     for (int64_t c = 0; c < nc; ++c) {
         for (int32_t i = 0; i < cs; ++i) {
             const uint32_t t = uint32_t(tokens[c * cs + i]);
-            for (int j = 0; j < 4; ++j) data[4 * i + j] = uint8_t(t >> (8 * j));
+            data[4 * i] = uint8_t(t);
+            data[4 * i + 1] = uint8_t(t >> 8);
+            data[4 * i + 2] = uint8_t(t >> 16);
+            data[4 * i + 3] = uint8_t(t >> 24);
         }
-        (*con)[c] = sha256(data);
-        chained.clear();
-        if (c > 0) chained.insert(chained.end(), (*pre)[c - 1].b, (*pre)[c - 1].b + 32);
-        chained.insert(chained.end(), data.begin(), data.end());
-        (*pre)[c] = sha256(chained);
+        Sha256 hc;
+        hc.update(data.data(), data.size());
+        (*con)[c] = hc.final();
+        Sha256 hp;
+        if (c > 0) hp.update((*pre)[c - 1].b, 32);
+        hp.update(data.data(), data.size());
+        (*pre)[c] = hp.final();
     }
 }
 
@@ -286,6 +318,24 @@ kvp_status kvp_bm_append(kvp_block_manager* bm, int64_t seq, int64_t n, int32_t*
     while (int64_t(s.table.size()) * bm->bs < L + n) s.table.push_back(bm->alloc());
     s.len = L + n;
     write_table(s.table, table, max_blocks);
+    return KVP_OK;
+}
+
+kvp_status kvp_bm_append_batch(kvp_block_manager* bm, const int64_t* seqs, const int32_t* n_tokens, int32_t count,
+                               int32_t* tables, int32_t max_blocks, int32_t* cow_pairs, int32_t* n_pairs,
+                               int32_t* done) {
+    if (!bm || count < 0 || (count > 0 && (!seqs || !n_tokens || !tables || !cow_pairs)) || !n_pairs || !done)
+        return KVP_ERR_INVALID_ARG;
+    *n_pairs = 0;
+    *done = 0;
+    for (int32_t i = 0; i < count; ++i) {
+        int32_t np_i = 0;
+        const kvp_status st = kvp_bm_append(bm, seqs[i], n_tokens[i], tables + int64_t(i) * max_blocks, max_blocks,
+                                            cow_pairs + 2 * int64_t(*n_pairs), 1, &np_i);
+        if (st != KVP_OK) return st;
+        *n_pairs += np_i;
+        *done = i + 1;
+    }
     return KVP_OK;
 }
 

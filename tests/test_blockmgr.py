@@ -126,3 +126,31 @@ def test_random_streams_match_reference(seed, nb, bs, cs):
         if not a:
             break
     assert native.stats()["free"] == nb and native.audit()
+
+
+def test_append_batch_equals_sequential_appends():
+    rng = np.random.default_rng(9)
+    a, b = kvp.BlockManager(64, 16, 32, 64), kvp.BlockManager(64, 16, 32, 64)
+    seqs = list(range(6))
+    prompts = [list(rng.integers(0, 9, size=int(rng.integers(5, 60)))) for _ in seqs]
+    for m in (a, b):
+        for s, p in zip(seqs, prompts):
+            m.admit(s, p)
+        m.fork(0, 100)
+        m.fork(3, 103)
+    order = [0, 100, 3, 103, 5, 1]
+    for step in range(6):
+        n = [int(x) for x in rng.integers(0, 9, size=len(order))]
+        tables, pairs = a.append_batch(order, n)
+        want_pairs = []
+        for i, (s, k) in enumerate(zip(order, n)):
+            t, p = b.append(s, k)
+            assert tables[i][: len(t)].tolist() == t and (tables[i][len(t):] == -1).all()
+            want_pairs += p
+        assert [tuple(r) for r in pairs.tolist()] == want_pairs
+        assert a.audit() and b.audit() and a.stats() == b.stats()
+    # running out of blocks part-way: the first `done` sequences appended, the rest unchanged
+    with pytest.raises(kvp.NoBlocks) as ei:
+        a.append_batch(order, [16 * 40] * len(order))
+    assert ei.value.done < len(order)
+    assert a.audit()
