@@ -12,7 +12,8 @@ context, and recomputes only the ~15% most-deviated tokens; content-hash
 
 Readings taken where the pages are silent:
 * a token's vector is its K and V for all kv heads, concatenated;
-  deviation = 1 - cos(cached, fresh), in [0, 2]; a zero vector on either
+  deviation = 1 - cos(cached, fresh), clamped to [0, 2] (the range of
+  1 - cos, which rounding can leave by an ulp); a zero vector on either
   side gives deviation 1 (no direction to agree with) unless both are zero
   (deviation 0);
 * per sequence, k = ceil(n * permille / 1000) tokens are selected (150 per
@@ -40,6 +41,9 @@ def kv_deviation(dtype: str, k_pool, v_pool, k_fresh, v_fresh, slots):
     vf = decode_bits(v_fresh, dtype).reshape(T, -1)
     for t in range(T):
         s = int(slots[t])
+        if not 0 <= s < nb * bs:
+            dev[t] = -1.0  # no cached entry to compare
+            continue
         blk, off = s // bs, s % bs
         a = np.concatenate([decode_bits(k_pool[blk, :, off], dtype).ravel(),
                             decode_bits(v_pool[blk, :, off], dtype).ravel()])
@@ -50,7 +54,7 @@ def kv_deviation(dtype: str, k_pool, v_pool, k_fresh, v_fresh, slots):
         elif na == 0.0 or nb_ == 0.0:
             dev[t] = 1.0
         else:
-            dev[t] = 1.0 - (a @ b) / (na * nb_)
+            dev[t] = min(max(1.0 - (a @ b) / (na * nb_), 0.0), 2.0)  # cos is in [-1, 1]
     return dev
 
 
