@@ -172,6 +172,33 @@ kvp_status kvp_decode_attn_q(const kvp_pool *pool, const kvp_qpool *qpool, const
                              float softmax_scale, int32_t num_splits, void *workspace, size_t workspace_bytes,
                              void *stream);
 
+/* CacheBlend recompute selection (kvboost "How it works" > "4. Seam
+ * repair": the cacheblend strategy measures per-token cosine deviation
+ * between the cached K/V and the K/V with full context in one forward pass
+ * and recomputes only the ~15% most-deviated tokens; content-hash matches
+ * always take it).  Three calls: kvp_kv_deviation, kvp_select_recompute,
+ * then kvp_cache_append(pool, k_fresh, v_fresh, recompute_slots, T), which
+ * overwrites the selected tokens' pool entries with their fresh K/V.
+ *
+ * Deviation: for token t with pool slot slots[t], the vector of its K and V
+ * for all kv heads, cached (in the pool) and fresh (k_fresh/v_fresh, device
+ * [T][num_kv_heads][head_dim] in the pool dtype, 16-byte aligned):
+ *     deviation[t] = 1 - cos(cached, fresh), clamped to [0, 2] (fp32; 0 if both vectors are
+ *     zero, 1 if only one is).
+ * A slot outside the pool gives -1 and sets KVP_DEVERR_BAD_SLOT.
+ * deviation: device float [T], written.  T == 0 is a no-op. */
+kvp_status kvp_kv_deviation(const kvp_pool *pool, const void *k_fresh, const void *v_fresh, const int64_t *slots,
+                            int32_t T, float *deviation, void *stream);
+
+/* Selection: tokens of sequence s are t in [cu_seqlens[s], cu_seqlens[s+1]);
+ * k_s = ceil(n_s * permille / 1000) of them (integer arithmetic; 150 per
+ * mille = the pages' ~15%) are selected, the largest deviations first, ties
+ * to the lower position.  recompute_slots[t] = slots[t] if selected, else -1
+ * (device int64 [T]); counts[s] = k_s (device int32 [B]).  permille in
+ * [0, 1000].  B == 0 is a no-op. */
+kvp_status kvp_select_recompute(const float *deviation, const int64_t *slots, const int32_t *cu_seqlens, int32_t B,
+                                int32_t permille, int64_t *recompute_slots, int32_t *counts, void *stream);
+
 /* A pool of blocks in host memory with the same block geometry (num_kv_heads,
  * block_size, head_dim, dtype) as a device pool: the swap buffer of
  * preempted sequences.  k_pool, v_pool: host [num_blocks][Hkv][bs][d],

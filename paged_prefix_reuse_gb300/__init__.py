@@ -10,6 +10,7 @@ raises ``KvpLibraryMissing``.
 Functions carry the names of the C entry points declared in
 ``include/kvp.h``: ``kvp_slot_mapping``, ``kvp_cache_append``,
 ``kvp_block_copy``, ``kvp_block_swap``, ``kvp_quantize_blocks``,
+``kvp_kv_deviation``, ``kvp_select_recompute``,
 ``kvp_prefix_attn``, ``kvp_decode_attn``, ``kvp_decode_attn_q`` and
 ``kvp_workspace_size`` (plus the split-count helpers).
 """
@@ -38,6 +39,8 @@ __all__ = [
     "kvp_block_copy",
     "kvp_block_swap",
     "kvp_quantize_blocks",
+    "kvp_kv_deviation",
+    "kvp_select_recompute",
     "kvp_prefix_attn",
     "kvp_decode_attn",
     "kvp_decode_attn_q",
@@ -65,6 +68,8 @@ EXPORTED_SYMBOLS = (
     "kvp_block_copy",
     "kvp_block_swap",
     "kvp_quantize_blocks",
+    "kvp_kv_deviation",
+    "kvp_select_recompute",
     "kvp_prefix_attn",
     "kvp_decode_attn",
     "kvp_decode_attn_q",
@@ -159,6 +164,8 @@ def load_library():
         lib.kvp_cache_append.argtypes = [PP, P, P, P, i32, P]
         lib.kvp_block_copy.argtypes = [PP, P, i32, P]
         lib.kvp_block_swap.argtypes = [PP, ctypes.POINTER(_HostPool), P, i32, i32, P]
+        lib.kvp_kv_deviation.argtypes = [PP, P, P, P, i32, P, P]
+        lib.kvp_select_recompute.argtypes = [P, P, P, i32, i32, P, P, P]
         QP = ctypes.POINTER(_QPool)
         lib.kvp_quantize_blocks.argtypes = [PP, QP, P, i32, P]
         lib.kvp_decode_attn_q.argtypes = [PP, QP, P, P, P, P, P, P, i32, i32, i32, i32, f32, i32, P, sz, P]
@@ -187,7 +194,8 @@ def load_library():
         for name in ("kvp_bm_admit", "kvp_bm_append", "kvp_bm_fork", "kvp_bm_finish", "kvp_bm_table", "kvp_bm_audit"):
             getattr(lib, name).restype = ctypes.c_int
         for name in ("kvp_slot_mapping", "kvp_cache_append", "kvp_block_copy", "kvp_block_swap",
-                     "kvp_quantize_blocks", "kvp_prefix_attn", "kvp_decode_attn", "kvp_decode_attn_q",
+                     "kvp_quantize_blocks", "kvp_kv_deviation", "kvp_select_recompute", "kvp_prefix_attn",
+                     "kvp_decode_attn", "kvp_decode_attn_q",
                      "kvp_decode_attn_noalloc"):
             getattr(lib, name).restype = ctypes.c_int
         lib.kvp_prefix_num_splits.argtypes = [i32, i32, i32, i32, i32, i32]
@@ -277,6 +285,29 @@ class PagedKVPool:
 
     def clear_errors(self) -> None:
         self.err_word.zero_()
+
+
+def kvp_kv_deviation(pool: PagedKVPool, k_fresh: torch.Tensor, v_fresh: torch.Tensor, slots: torch.Tensor,
+                     out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Per-token 1 - cos([K;V] in the pool at slots[t], [K;V] fresh[t]) (float32 [T])."""
+    T = int(slots.shape[0])
+    if out is None:
+        out = torch.empty(T, dtype=torch.float32, device=slots.device)
+    _check(load_library().kvp_kv_deviation(pool.c, _ptr(k_fresh), _ptr(v_fresh), _ptr(slots), T, _ptr(out),
+                                           _stream(stream)), "kvp_kv_deviation")
+    return out
+
+
+def kvp_select_recompute(deviation: torch.Tensor, slots: torch.Tensor, cu_seqlens: torch.Tensor,
+                         permille: int = 150, stream=None):
+    """CacheBlend selection: -> (recompute_slots int64 [T] (-1 = keep), counts int32 [B]).
+    Follow with kvp_cache_append(pool, k_fresh, v_fresh, recompute_slots)."""
+    B = int(cu_seqlens.shape[0]) - 1
+    rs = torch.empty_like(slots)
+    counts = torch.empty(max(B, 0), dtype=torch.int32, device=slots.device)
+    _check(load_library().kvp_select_recompute(_ptr(deviation), _ptr(slots), _ptr(cu_seqlens), B, int(permille),
+                                               _ptr(rs), _ptr(counts), _stream(stream)), "kvp_select_recompute")
+    return rs, counts
 
 
 class QuantKVPool:

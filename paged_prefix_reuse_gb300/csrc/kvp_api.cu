@@ -204,6 +204,27 @@ kvp_status kvp_block_swap(const kvp_pool* pool, const kvp_host_pool* host, const
                                        static_cast<cudaStream_t>(stream)));
 }
 
+kvp_status kvp_kv_deviation(const kvp_pool* pool, const void* k_fresh, const void* v_fresh, const int64_t* slots,
+                            int32_t T, float* deviation, void* stream) {
+    kvp_status st = check_pool(pool);
+    if (st != KVP_OK) return st;
+    if (T < 0) return KVP_ERR_INVALID_ARG;
+    if (T == 0) return KVP_OK;
+    if (!k_fresh || !v_fresh || !slots || !deviation || !aligned16(k_fresh) || !aligned16(v_fresh))
+        return KVP_ERR_INVALID_ARG;
+    return from_cuda(launch_kv_deviation(view_of(pool), pool->k_pool, pool->v_pool, k_fresh, v_fresh, slots, T,
+                                         deviation, static_cast<cudaStream_t>(stream)));
+}
+
+kvp_status kvp_select_recompute(const float* deviation, const int64_t* slots, const int32_t* cu_seqlens, int32_t B,
+                                int32_t permille, int64_t* recompute_slots, int32_t* counts, void* stream) {
+    if (B < 0 || permille < 0 || permille > 1000) return KVP_ERR_INVALID_ARG;
+    if (B == 0) return KVP_OK;
+    if (!deviation || !slots || !cu_seqlens || !recompute_slots || !counts) return KVP_ERR_INVALID_ARG;
+    return from_cuda(launch_select_recompute(deviation, slots, cu_seqlens, B, permille, recompute_slots, counts,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
 kvp_status kvp_prefix_attn(const kvp_pool* pool, const void* q, void* out, float* lse, const int32_t* cu_seqlens_q,
                            const int32_t* context_lens, const int32_t* block_tables, int32_t max_blocks, int32_t B,
                            int32_t total_q, int32_t num_q_heads, int32_t max_q_len, int32_t max_context_len,

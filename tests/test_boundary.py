@@ -197,6 +197,19 @@ def test_quantized_pool_validation(lib):
                                  0x70000, 8, 2, hkv * 2, 100, 0.1, 1, None, 0, None) == KVP_ERR_UNSUPPORTED
 
 
+def test_cacheblend_validation(lib):
+    pool = _pool()
+    P = ctypes.byref(pool)
+    assert lib.kvp_kv_deviation(P, 0x30000, 0x40000, 0x50000, 0, 0x60000, None) == KVP_OK
+    assert lib.kvp_kv_deviation(P, 0x30008, 0x40000, 0x50000, 4, 0x60000, None) == KVP_ERR_INVALID_ARG
+    assert lib.kvp_kv_deviation(P, 0x30000, 0x40000, None, 4, 0x60000, None) == KVP_ERR_INVALID_ARG
+    assert lib.kvp_kv_deviation(P, 0x30000, 0x40000, 0x50000, -1, 0x60000, None) == KVP_ERR_INVALID_ARG
+    assert lib.kvp_select_recompute(0x10000, 0x20000, 0x30000, 0, 150, 0x40000, 0x50000, None) == KVP_OK
+    assert lib.kvp_select_recompute(0x10000, 0x20000, 0x30000, 2, 1001, 0x40000, 0x50000, None) == KVP_ERR_INVALID_ARG
+    assert lib.kvp_select_recompute(0x10000, 0x20000, 0x30000, 2, -1, 0x40000, 0x50000, None) == KVP_ERR_INVALID_ARG
+    assert lib.kvp_select_recompute(None, 0x20000, 0x30000, 2, 150, 0x40000, 0x50000, None) == KVP_ERR_INVALID_ARG
+
+
 def test_workspace_and_split_helpers(lib):
     assert kvp.kvp_workspace_size(0, 100, 8, 128, 1) == 0
     ws = kvp.kvp_workspace_size(0, 100, 8, 128, 3)
