@@ -107,6 +107,8 @@ def _peak_value(peaks, *keys):
 # processed: long_context_prefix is four independent copies of the B=1 case
 # (own block tables, Q and O), so its traffic is four times B=1's.
 TRAFFIC_PROXY = {"long_context_prefix": ("long_context_prefix_b1", 4.0)}
+# The source files a kernel's code comes from (besides kvp_internal.cuh).
+KERNEL_SOURCES = {"prefix": ["kvp_prefix.cu"], "decode": ["kvp_decode.cu", "kvp_decode_impl.cuh"]}
 
 
 def committed_traffic(kernel: str, workload: str):
@@ -119,11 +121,12 @@ def committed_traffic(kernel: str, workload: str):
 
 def _committed_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if that summary
-    was taken on the kernel source as it is now -- the kernel's .cu file and
-    the shared kvp_internal.cuh, hashed together -- else None."""
+    was taken on the kernel source as it is now -- the kernel's source files
+    and the shared kvp_internal.cuh, hashed together -- else None."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
     csrc = os.path.join(ROOT, "paged_prefix_reuse_gb300", "csrc")
-    srcs = [os.path.join(csrc, f"kvp_{kernel}.cu"), os.path.join(csrc, "kvp_internal.cuh")]
+    srcs = [os.path.join(csrc, f) for f in KERNEL_SOURCES.get(kernel, [f"kvp_{kernel}.cu"])]
+    srcs.append(os.path.join(csrc, "kvp_internal.cuh"))
     if not (os.path.exists(path) and all(os.path.exists(f) for f in srcs)):
         return None
     digest = hashlib.sha256(b"".join(open(f, "rb").read() for f in srcs)).hexdigest()[:16]
