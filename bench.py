@@ -292,6 +292,7 @@ def run_kvp(args):
     from paged_prefix_reuse_gb300.step import DeviceStep
 
     kvp.load_library()
+    kvp.kvp_set_launch_options(kvp.LAUNCH_PDL if args.pdl else 0)
     w = wl.make_config(WORKLOADS[args.workload], **WORKLOAD_ARGS.get(args.workload, {}))
     st = DeviceStep(w, device=dev, prefix_splits=args.prefix_splits, decode_splits=args.decode_splits)
     stream = torch.cuda.Stream(device=dev)
@@ -465,6 +466,7 @@ def run_kvp(args):
             "l2": "flushed before every timed step (512 MB write, then read back)",
             "launch": "CUDA graph replay of the step; the graph holds the kernels the C-ABI calls enqueued",
             "parallelism": f"replicas x{world}",
+            "pdl": bool(args.pdl),
         },
         "gpu_launches": launches * args.steps,
         "kernel_ms": kern_ms,
@@ -537,6 +539,7 @@ def run_swap(args):
     from paged_prefix_reuse_gb300.step import DeviceStep
 
     kvp.load_library()
+    kvp.kvp_set_launch_options(kvp.LAUNCH_PDL if args.pdl else 0)
     w = wl.make_config(4)
     st = DeviceStep(w, device=dev)
     pool = st.pool
@@ -608,6 +611,7 @@ def run_decode_q(args):
     from paged_prefix_reuse_gb300.step import DeviceStep
 
     kvp.load_library()
+    kvp.kvp_set_launch_options(kvp.LAUNCH_PDL if args.pdl else 0)
     w = wl.make_config(4)
     st = DeviceStep(w, device=dev)
     st.run_slots()
@@ -693,6 +697,7 @@ def run_blockmgr(args):
     import paged_prefix_reuse_gb300 as kvp
 
     kvp.load_library()
+    kvp.kvp_set_launch_options(kvp.LAUNCH_PDL if args.pdl else 0)
     rng = np.random.default_rng(0)
     toks = rng.integers(0, 50000, size=1 << 20).astype(np.int32)
     kvp.kvp_hash_chunks(toks[:4096], 128)
@@ -773,6 +778,7 @@ def run_cacheblend(args):
     from paged_prefix_reuse_gb300.step import DeviceStep
 
     kvp.load_library()
+    kvp.kvp_set_launch_options(kvp.LAUNCH_PDL if args.pdl else 0)
     w = wl.make_config(3)
     st = DeviceStep(w, device=dev)
     pool = st.pool
@@ -860,6 +866,8 @@ def main():
                          "decode_q: decode over a quantized cached prefix; blockmgr: host block manager; "
                          "cacheblend: CacheBlend recompute selection")
     ap.add_argument("--bits", type=int, choices=[8, 4], default=8, help="quantized pool width for --op decode_q")
+    ap.add_argument("--pdl", type=int, choices=[0, 1], default=1,
+                    help="1: programmatic dependent launch between the step's kernels (kvp_set_launch_options)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -199,6 +199,22 @@ kvp_status kvp_kv_deviation(const kvp_pool *pool, const void *k_fresh, const voi
 kvp_status kvp_select_recompute(const float *deviation, const int64_t *slots, const int32_t *cu_seqlens, int32_t B,
                                 int32_t permille, int64_t *recompute_slots, int32_t *counts, void *stream);
 
+/* Launch options, process-wide (all devices, all streams); default 0.
+ * KVP_LAUNCH_PDL: every kernel the library launches may begin before the
+ * kernel queued before it on the same stream has finished (programmatic
+ * dependent launch), overlapping its start-up (barrier setup, tensor memory,
+ * reads of metadata, block tables and q) with that kernel's tail.  Before
+ * its first global write and before reading any pool, slot, workspace or
+ * deviation buffer, every kernel waits for the preceding kernel to complete
+ * (griddepcontrol.wait), so completions stay ordered down the stream.
+ * Contract with the caller when enabled: the kernel queued immediately
+ * before a kvp_* call must not write that call's q, cu_seqlens_q,
+ * context_lens, block_tables or qpages.  (Within the library's own step --
+ * copy, slot mapping, append, prefix attention, decode -- this holds.) */
+#define KVP_LAUNCH_PDL 0x1u
+void kvp_set_launch_options(uint32_t flags);
+uint32_t kvp_get_launch_options(void);
+
 /* A pool of blocks in host memory with the same block geometry (num_kv_heads,
  * block_size, head_dim, dtype) as a device pool: the swap buffer of
  * preempted sequences.  k_pool, v_pool: host [num_blocks][Hkv][bs][d],

@@ -49,6 +49,9 @@ __all__ = [
     "kvp_prefix_num_splits",
     "kvp_decode_num_splits",
     "kvp_status_string",
+    "kvp_set_launch_options",
+    "kvp_get_launch_options",
+    "LAUNCH_PDL",
     "DEVERR",
 ]
 
@@ -57,6 +60,8 @@ _LIB_PATH = os.path.join(_HERE, "libkvp.so")
 
 KVP_F16, KVP_BF16 = 0, 1
 _DTYPES = {torch.float16: KVP_F16, torch.bfloat16: KVP_BF16}
+
+LAUNCH_PDL = 0x1  # KVP_LAUNCH_PDL in kvp.h
 
 # Device error-word bits (KVP_DEVERR_* in kvp.h).
 DEVERR = {"bad_block": 0x1, "bad_slot": 0x2, "bad_pair": 0x4, "bad_len": 0x8, "timeout": 0x10, "qrange": 0x20}
@@ -78,6 +83,8 @@ EXPORTED_SYMBOLS = (
     "kvp_decode_num_splits",
     "kvp_workspace_size",
     "kvp_status_string",
+    "kvp_set_launch_options",
+    "kvp_get_launch_options",
     "kvp_version",
 )
 
@@ -206,6 +213,10 @@ def load_library():
         lib.kvp_workspace_size.restype = sz
         lib.kvp_status_string.argtypes = [ctypes.c_int]
         lib.kvp_status_string.restype = ctypes.c_char_p
+        lib.kvp_set_launch_options.argtypes = [ctypes.c_uint32]
+        lib.kvp_set_launch_options.restype = None
+        lib.kvp_get_launch_options.argtypes = []
+        lib.kvp_get_launch_options.restype = ctypes.c_uint32
         lib.kvp_version.argtypes = []
         lib.kvp_version.restype = i32
         _lib = lib
@@ -221,6 +232,17 @@ def _status_text(status: int) -> str:
 
 def kvp_status_string(status: int) -> str:
     return load_library().kvp_status_string(status).decode()
+
+
+def kvp_set_launch_options(flags: int) -> None:
+    """Process-wide launch options (``LAUNCH_PDL``: each kernel may start
+    while the one before it on the stream finishes; see kvp.h for the
+    caller's side of that contract)."""
+    load_library().kvp_set_launch_options(int(flags))
+
+
+def kvp_get_launch_options() -> int:
+    return int(load_library().kvp_get_launch_options())
 
 
 def _check(status: int, where: str) -> None:

@@ -4,9 +4,14 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "kvp_internal.cuh"
 
 namespace kvp {
+
+std::atomic<uint32_t> g_launch_flags{0};
+uint32_t launch_flags() { return g_launch_flags.load(std::memory_order_relaxed); }
 namespace {
 
 constexpr int kNumSMs = 152;  // GB300; used only by the split heuristics
@@ -99,6 +104,9 @@ using namespace kvp;
 extern "C" {
 
 int32_t kvp_version(void) { return 100; }
+
+void kvp_set_launch_options(uint32_t flags) { kvp::g_launch_flags.store(flags, std::memory_order_relaxed); }
+uint32_t kvp_get_launch_options(void) { return kvp::g_launch_flags.load(std::memory_order_relaxed); }
 
 const char* kvp_status_string(kvp_status status) {
     switch (status) {

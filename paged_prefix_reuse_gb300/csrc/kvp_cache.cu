@@ -36,7 +36,9 @@ __global__ void slot_mapping_kernel(PoolView pool, const int32_t* __restrict__ c
                                     const int32_t* __restrict__ ctx, const int32_t* __restrict__ bt,
                                     int32_t max_blocks, int32_t B, int32_t total_q,
                                     int64_t* __restrict__ slots) {
+    pdl_trigger();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    bool waited = false;
     for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total_q; t += stride) {
         int lo = 0, hi = B;
         while (hi - lo > 1) {
@@ -57,8 +59,13 @@ __global__ void slot_mapping_kernel(PoolView pool, const int32_t* __restrict__ c
             else
                 report(pool.err_word, KVP_DEVERR_BAD_BLOCK);
         }
+        if (!waited) {
+            pdl_wait();  // before the first write: the slots may still be read upstream
+            waited = true;
+        }
         slots[t] = slot;
     }
+    if (!waited) pdl_wait();
 }
 
 // Append.  A token's K (and V) rows for all kv heads are vpt = Hkv * d / 8
@@ -73,6 +80,8 @@ __global__ void __launch_bounds__(kThreads) append_kernel(PoolView pool, uint4* 
                                                           const uint4* __restrict__ v_new,
                                                           const int64_t* __restrict__ slots, int32_t T, int32_t vpt,
                                                           int32_t tpb) {
+    pdl_trigger();
+    pdl_wait();  // the slots come from the kernel before
     const int vph = pool.head_dim / 8;  // vectors per (token, head)
     const int64_t num_slots = pool.num_blocks * pool.block_size;
     const bool wide = vpt >= kThreads;          // one token per step, several vectors per thread
@@ -124,6 +133,8 @@ __global__ void __launch_bounds__(kThreads) block_move_kernel(const uint4* __res
                                                               uint4* __restrict__ kd, uint4* __restrict__ vd,
                                                               int64_t dst_blocks, const int32_t* __restrict__ pairs,
                                                               int32_t vpb, uint32_t* err_word) {
+    pdl_trigger();
+    pdl_wait();
     const int i = blockIdx.y;
     const int64_t src = __ldg(pairs + 2 * i);
     const int64_t dst = __ldg(pairs + 2 * i + 1);
@@ -161,9 +172,8 @@ cudaError_t launch_slot_mapping(const PoolView& pool, const int32_t* cu_seqlens_
                                 const int32_t* block_tables, int32_t max_blocks, int32_t B, int32_t total_q,
                                 int64_t* slot_mapping, cudaStream_t stream) {
     if (total_q <= 0) return cudaSuccess;
-    slot_mapping_kernel<<<grid_for(total_q, kThreads), kThreads, 0, stream>>>(
-        pool, cu_seqlens_q, context_lens, block_tables, max_blocks, B, total_q, slot_mapping);
-    return cudaGetLastError();
+    return launch_k(slot_mapping_kernel, grid_for(total_q, kThreads), kThreads, 0, stream, pool, cu_seqlens_q,
+                    context_lens, block_tables, max_blocks, B, total_q, slot_mapping);
 }
 
 cudaError_t launch_cache_append(const PoolView& pool, void* k_pool, void* v_pool, const void* k_new,
@@ -174,10 +184,9 @@ cudaError_t launch_cache_append(const PoolView& pool, void* k_pool, void* v_pool
     const int64_t steps = (static_cast<int64_t>(T) + tpb - 1) / tpb;
     // One step per block when there are few; a block loops (kUnroll steps per
     // pass) only once the steps outnumber the blocks the GPU holds.
-    append_kernel<<<grid_for(steps, 1), kThreads, 0, stream>>>(
-        pool, static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), static_cast<const uint4*>(k_new),
-        static_cast<const uint4*>(v_new), slot_mapping, T, vpt, tpb);
-    return cudaGetLastError();
+    return launch_k(append_kernel, grid_for(steps, 1), kThreads, 0, stream, pool, static_cast<uint4*>(k_pool),
+                    static_cast<uint4*>(v_pool), static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+                    slot_mapping, T, vpt, tpb);
 }
 
 cudaError_t launch_block_copy(const PoolView& pool, void* k_pool, void* v_pool, const int32_t* pairs, int32_t n,
@@ -186,11 +195,9 @@ cudaError_t launch_block_copy(const PoolView& pool, void* k_pool, void* v_pool, 
     const int32_t vpb = pool.num_kv_heads * pool.block_size * (pool.head_dim / 8);
     if (n > 65535) return cudaErrorInvalidValue;
     const dim3 grid((vpb + 2 * kThreads - 1) / (2 * kThreads), n);
-    block_move_kernel<<<grid, kThreads, 0, stream>>>(static_cast<const uint4*>(k_pool), static_cast<const uint4*>(v_pool),
-                                                     pool.num_blocks, static_cast<uint4*>(k_pool),
-                                                     static_cast<uint4*>(v_pool), pool.num_blocks, pairs, vpb,
-                                                     pool.err_word);
-    return cudaGetLastError();
+    return launch_k(block_move_kernel, grid, kThreads, 0, stream, static_cast<const uint4*>(k_pool),
+                    static_cast<const uint4*>(v_pool), pool.num_blocks, static_cast<uint4*>(k_pool),
+                    static_cast<uint4*>(v_pool), pool.num_blocks, pairs, vpb, pool.err_word);
 }
 
 cudaError_t launch_block_swap(const PoolView& pool, void* k_pool, void* v_pool, void* host_k, void* host_v,
@@ -201,14 +208,12 @@ cudaError_t launch_block_swap(const PoolView& pool, void* k_pool, void* v_pool, 
     if (n > 65535) return cudaErrorInvalidValue;
     const dim3 grid((vpb + 2 * kThreads - 1) / (2 * kThreads), n);
     if (to_host)
-        block_move_kernel<<<grid, kThreads, 0, stream>>>(
-            static_cast<const uint4*>(k_pool), static_cast<const uint4*>(v_pool), pool.num_blocks,
-            static_cast<uint4*>(host_k), static_cast<uint4*>(host_v), host_blocks, pairs, vpb, pool.err_word);
-    else
-        block_move_kernel<<<grid, kThreads, 0, stream>>>(
-            static_cast<const uint4*>(host_k), static_cast<const uint4*>(host_v), host_blocks,
-            static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), pool.num_blocks, pairs, vpb, pool.err_word);
-    return cudaGetLastError();
+        return launch_k(block_move_kernel, grid, kThreads, 0, stream, static_cast<const uint4*>(k_pool),
+                        static_cast<const uint4*>(v_pool), pool.num_blocks, static_cast<uint4*>(host_k),
+                        static_cast<uint4*>(host_v), host_blocks, pairs, vpb, pool.err_word);
+    return launch_k(block_move_kernel, grid, kThreads, 0, stream, static_cast<const uint4*>(host_k),
+                    static_cast<const uint4*>(host_v), host_blocks, static_cast<uint4*>(k_pool),
+                    static_cast<uint4*>(v_pool), pool.num_blocks, pairs, vpb, pool.err_word);
 }
 
 }  // namespace kvp

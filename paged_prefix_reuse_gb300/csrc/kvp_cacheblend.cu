@@ -40,6 +40,8 @@ __global__ void __launch_bounds__(kDevThreads) deviation_kernel(PoolView pool, c
                                                                 const uint4* __restrict__ v_fresh,
                                                                 const int64_t* __restrict__ slots, int32_t T,
                                                                 float* __restrict__ dev) {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int vph = pool.head_dim / 8;             // 16-byte units per (token, head)
     const int vpt = pool.num_kv_heads * vph;       // per token
@@ -96,6 +98,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __rest
     __shared__ uint32_t sh_prefix, sh_need;
     __shared__ uint32_t warp_cnt[kSelThreads / 32];
     __shared__ uint32_t sh_base;
+    pdl_trigger();
+    pdl_wait();  // the deviations come from the kernel before
     const int s = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int a = __ldg(cu + s), n = __ldg(cu + s + 1) - a;
     const uint32_t k = static_cast<uint32_t>((static_cast<int64_t>(n) * permille + 999) / 1000);
@@ -178,18 +182,16 @@ cudaError_t launch_kv_deviation(const PoolView& pool, const void* k_pool, const 
     const uint4* vp = static_cast<const uint4*>(v_pool);
     const uint4* kf = static_cast<const uint4*>(k_fresh);
     const uint4* vf = static_cast<const uint4*>(v_fresh);
-    if (pool.dtype == KVP_BF16)
-        deviation_kernel<true><<<blocks, kDevThreads, 0, stream>>>(pool, kp, vp, kf, vf, slots, T, dev);
-    else
-        deviation_kernel<false><<<blocks, kDevThreads, 0, stream>>>(pool, kp, vp, kf, vf, slots, T, dev);
-    return cudaGetLastError();
+    return pool.dtype == KVP_BF16
+               ? launch_k(deviation_kernel<true>, blocks, kDevThreads, 0, stream, pool, kp, vp, kf, vf, slots, T, dev)
+               : launch_k(deviation_kernel<false>, blocks, kDevThreads, 0, stream, pool, kp, vp, kf, vf, slots, T,
+                          dev);
 }
 
 cudaError_t launch_select_recompute(const float* dev, const int64_t* slots, const int32_t* cu, int32_t B,
                                     int32_t permille, int64_t* out_slots, int32_t* counts, cudaStream_t stream) {
     if (B <= 0) return cudaSuccess;
-    select_kernel<<<B, kSelThreads, 0, stream>>>(dev, slots, cu, permille, out_slots, counts);
-    return cudaGetLastError();
+    return launch_k(select_kernel, B, kSelThreads, 0, stream, dev, slots, cu, permille, out_slots, counts);
 }
 
 }  // namespace kvp

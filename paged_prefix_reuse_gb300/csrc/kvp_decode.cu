@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ ws
                                                     int32_t lse_stride, const int32_t* __restrict__ ctx,
                                                     int32_t block_size, int32_t pages_per_split,
                                                     int32_t parts_per_split) {
+    pdl_trigger();
+    pdl_wait();  // the partials come from the kernel before
     constexpr int V4 = D / 4;  // float4 columns per row: 16, 24 or 32
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -147,14 +149,13 @@ cudaError_t launch_merge(const float* ws_o, const float* ws_lse, int32_t rows, i
     const int threads = 256;
     const int blocks = (rows * 32 + threads - 1) / threads;
     const bool bf = dtype == KVP_BF16;
-#define KVP_MERGE(BF, DD)                                                                                      \
-    merge_kernel<BF, DD><<<blocks, threads, 0, stream>>>(ws_o, ws_lse, rows, num_q_heads, max_splits, out, lse, \
-                                                        lse_stride, context_lens, block_size, pages_per_split,     \
-                                                        parts_per_split)
+#define KVP_MERGE(BF, DD)                                                                                     \
+    return launch_k(merge_kernel<BF, DD>, blocks, threads, 0, stream, ws_o, ws_lse, rows, num_q_heads, max_splits, \
+                    out, lse, lse_stride, context_lens, block_size, pages_per_split, parts_per_split)
     switch (head_dim) {
-        case 64: if (bf) KVP_MERGE(true, 64); else KVP_MERGE(false, 64); break;
-        case 96: if (bf) KVP_MERGE(true, 96); else KVP_MERGE(false, 96); break;
-        case 128: if (bf) KVP_MERGE(true, 128); else KVP_MERGE(false, 128); break;
+        case 64: if (bf) KVP_MERGE(true, 64); else KVP_MERGE(false, 64);
+        case 96: if (bf) KVP_MERGE(true, 96); else KVP_MERGE(false, 96);
+        case 128: if (bf) KVP_MERGE(true, 128); else KVP_MERGE(false, 128);
         default: return cudaErrorInvalidValue;
     }
 #undef KVP_MERGE

@@ -209,6 +209,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 4)
 
     const int sp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_trigger();
     const int BS = p.pool.block_size;
     const int Hkv = p.pool.num_kv_heads;
     const int g = p.group;
@@ -218,10 +219,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 4)
     const int npages = (L + BS - 1) / BS;
     if (L < 1 || npages > p.max_blocks) {
         if (sp == 0 && tid == 0) report(err, KVP_DEVERR_BAD_LEN);
+        pdl_wait();  // every CTA waits, so the grid completes after the one before
         return;
     }
     const int page0 = sp * p.pages_per_split;
-    if (page0 >= npages) return;
+    if (page0 >= npages) {
+        pdl_wait();
+        return;
+    }
     const int page1 = min(npages, page0 + p.pages_per_split);
     const int key0 = page0 * BS;
     const int key1 = min(L, page1 * BS);
@@ -254,6 +259,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 4)
             prefetch_tmap(&tmap_k);
             prefetch_tmap(&tmap_v);
         }
+        pdl_wait();  // pool contents from the kernel before are read from here on
         int my_blk = 0;
         int issued = 0;
         for (int i = 0; i < nstages; ++i) {
@@ -572,8 +578,7 @@ cudaError_t launch_decode_kernel(const DecodeParams& p, const CUtensorMap& tk, c
         attr_set = true;
     }
     dim3 grid(p.max_splits, p.pool.num_kv_heads, p.B);
-    decode_kernel<kBF16, D, SK, BITS><<<grid, kDecodeThreads, C::SMEM_BYTES, stream>>>(tk, tv, p);
-    return cudaGetLastError();
+    return launch_k(decode_kernel<kBF16, D, SK, BITS>, grid, kDecodeThreads, C::SMEM_BYTES, stream, tk, tv, p);
 }
 
 }  // namespace

@@ -22,6 +22,33 @@ struct PoolView {
     uint32_t* err_word;
 };
 
+// ---- programmatic dependent launch (KVP_LAUNCH_PDL) -------------------------
+// Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+uint32_t launch_flags();  // kvp_set_launch_options
+
+// Launch with the programmatic-stream-serialization attribute when
+// KVP_LAUNCH_PDL is set, a plain launch otherwise.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                     Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (launch_flags() & KVP_LAUNCH_PDL) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // A quantized pool (see kvp_qpool in kvp.h).  bits == 0: none.
 struct QPoolView {
     uint8_t* k_codes;

@@ -141,6 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_trigger();
     const int split = blockIdx.x % p.num_splits;
     const int ct = p.q_tiles - 1 - static_cast<int>(blockIdx.x) / p.num_splits;  // heavy tiles first
     const int h = blockIdx.y, s = blockIdx.z;
@@ -154,11 +155,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int N = cu1 - cu0;
     const int rows_total = N * g;
     const int r0 = ct * kRowsPerCta;
-    if (r0 >= rows_total) return;
+    if (r0 >= rows_total) {
+        pdl_wait();  // every CTA waits, so the grid completes after the one before
+        return;
+    }
     const int P = L - N;
     const int npages = (L + BS - 1) / BS;
     if (P < 0 || npages > p.max_blocks) {
         if (tid == 0 && split == 0) report(err, KVP_DEVERR_BAD_LEN);
+        pdl_wait();
         return;
     }
     const bool has1 = r0 + kBM < rows_total;  // is the second query tile non-empty?
@@ -171,6 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (n_local <= 0) {
         // This split's key range is empty for the whole CTA: empty partials.
+        pdl_wait();
         if (tid < kRowsPerCta && r0 + tid < rows_total) {
             const int rg = r0 + tid;
             const int64_t wrow = static_cast<int64_t>(cu0 + rg / g) * p.num_q_heads + h * g + rg % g;
@@ -406,6 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         int blk_cur = load_batch(0);
         int blk_nxt = load_batch(1);
+        pdl_wait();  // pool contents from the kernel before (the append) are read from here on
         int loads = 0;  // ring loads issued: K_j is load 2j, V_j is load 2j+1
         bool stop = false;
         for (int jj = 0; jj < n_local && !stop; ++jj) {
@@ -574,8 +581,7 @@ cudaError_t launch_prefix_t(const PrefixParams& p, const CUtensorMap& tk, const 
         attr_set = true;
     }
     dim3 grid(p.q_tiles * p.num_splits, p.pool.num_kv_heads, p.B);
-    prefix_kernel<kBF16, D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(tk, tv, p);
-    return cudaGetLastError();
+    return launch_k(prefix_kernel<kBF16, D>, grid, kThreads, C::SMEM_BYTES, stream, tk, tv, p);
 }
 
 }  // namespace

@@ -48,6 +48,8 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const uint16_t* __r
                                                              const uint16_t* __restrict__ vp, PoolView pool,
                                                              QPoolView qp, const int32_t* __restrict__ pairs) {
     constexpr int kLevels = (1 << BITS) - 1;
+    pdl_trigger();
+    pdl_wait();
     const int i = blockIdx.x, h = blockIdx.y;
     const int64_t src = __ldg(pairs + 2 * i), dst = __ldg(pairs + 2 * i + 1);
     if (src < 0 || src >= pool.num_blocks || dst < 0 || dst >= qp.num_blocks) {
@@ -139,14 +141,11 @@ cudaError_t launch_quantize_blocks(const PoolView& pool, const void* k_pool, con
     const uint16_t* k = static_cast<const uint16_t*>(k_pool);
     const uint16_t* v = static_cast<const uint16_t*>(v_pool);
     const bool bf = pool.dtype == KVP_BF16;
-    if (qpool.bits == 8) {
-        if (bf) quantize_kernel<true, 8><<<grid, kQThreads, 0, stream>>>(k, v, pool, qpool, pairs);
-        else quantize_kernel<false, 8><<<grid, kQThreads, 0, stream>>>(k, v, pool, qpool, pairs);
-    } else {
-        if (bf) quantize_kernel<true, 4><<<grid, kQThreads, 0, stream>>>(k, v, pool, qpool, pairs);
-        else quantize_kernel<false, 4><<<grid, kQThreads, 0, stream>>>(k, v, pool, qpool, pairs);
-    }
-    return cudaGetLastError();
+    if (qpool.bits == 8)
+        return bf ? launch_k(quantize_kernel<true, 8>, grid, kQThreads, 0, stream, k, v, pool, qpool, pairs)
+                  : launch_k(quantize_kernel<false, 8>, grid, kQThreads, 0, stream, k, v, pool, qpool, pairs);
+    return bf ? launch_k(quantize_kernel<true, 4>, grid, kQThreads, 0, stream, k, v, pool, qpool, pairs)
+              : launch_k(quantize_kernel<false, 4>, grid, kQThreads, 0, stream, k, v, pool, qpool, pairs);
 }
 
 cudaError_t launch_decode_attn_q(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,

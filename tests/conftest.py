@@ -26,3 +26,15 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _launch_options(request):
+    """GPU tests run with programmatic dependent launch on, as the benchmark
+    does (KVP_TEST_PDL=0 runs them with plain stream ordering)."""
+    if "gpu" in request.keywords:
+        import paged_prefix_reuse_gb300 as kvp
+
+        if kvp._lib is not None:
+            kvp.kvp_set_launch_options(kvp.LAUNCH_PDL if os.environ.get("KVP_TEST_PDL", "1") != "0" else 0)
+    yield
