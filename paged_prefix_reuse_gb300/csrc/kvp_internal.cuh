@@ -177,6 +177,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same test, but a thread whose phase is not complete sleeps in hardware
+// until the phase completes (or the hint, in ns, runs out) instead of
+// returning at once: a waiting warp then takes no issue slots from the warps
+// that share its scheduler.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(100000u)
+        : "memory");
+    return ok != 0;
+}
+
 // Give up on any single wait after this long; a healthy wait lasts microseconds.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
@@ -189,7 +205,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(a, parity)) return true;
+        if (mbar_try_wait_sleep(a, parity)) return true;
         if ((it & 63u) == 0) {
             if (*abort) return false;
             if (global_timer_ns() - t0 > kWaitLimitNs) {

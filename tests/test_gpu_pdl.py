@@ -44,8 +44,9 @@ CASES = {
     "mixed_small": lambda: wl.continuous_batching_step(n_decode=10, n_prefill=2, prefill_new=70, prefill_lo=100,
                                                        prefill_hi=400, median=300, sigma=0.6, ctx_lo=20,
                                                        ctx_hi=900, n_forks=3, num_blocks=512, Hq=10, Hkv=2),
-    "shared_prompt": lambda: wl.make_config(1),
-    "decode_batch": lambda: wl.make_config(4),
+    "tiny": lambda: wl.make_config(1),
+    "shared_prompt": lambda: wl.make_config(2),
+    "mixed_full": lambda: wl.make_config(4),
 }
 
 
