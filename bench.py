@@ -202,6 +202,24 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest per-rank value (a time) over the process group, or the value
+    itself with one process.  Replicas end when the slowest rank does."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank processed units_per_rank in at most ms."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def cpu_oracle_sample(w, budget_s: float, seed: int = 0):
     """Time the fp64 oracle on a bounded random sample of prefill rows (and
     decode rows) of the workload; returns (tflops, seconds, rows, threads)."""
@@ -391,13 +409,7 @@ def run_kvp(args):
             kern_ms[k] = float(np.mean(times))
         stream.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms = float(np.mean(step_ms))
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(float(np.mean(step_ms)), dev)
 
     # ---- end to end through the C ABI with pinned host buffers ----
     host_in = {name: getattr(st, name).cpu().pin_memory() for name in ("q", "k_new", "v_new", "cu", "ctx", "bt")}
@@ -426,18 +438,12 @@ def run_kvp(args):
             stream.synchronize()
             if i >= args.warmup:
                 e2e_ms.append(a.elapsed_time(b))
-    e2e = float(np.mean(e2e_ms))
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e = float(t.item())
+    e2e = max_over_ranks(float(np.mean(e2e_ms)), dev)
 
     if rank != 0:
         return 0
     peaks, peak_src = load_peaks()
-    value = world * flops / (ms * 1e-3) / 1e12
+    value = job_rate(flops, world, ms) / 1e12
     line = {
         "metric": METRIC,
         "value": value,
@@ -471,7 +477,7 @@ def run_kvp(args):
         "gpu_launches": launches * args.steps,
         "kernel_ms": kern_ms,
         "wall_s": wall,
-        "e2e": {"value": world * flops / (e2e * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e,
+        "e2e": {"value": job_rate(flops, world, e2e) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clk,
     }
