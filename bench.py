@@ -12,7 +12,9 @@ TFLOP/s of the whole step (4*d*Hq*sum(N*P + N(N+1)/2) per step, divided by
 the device time of the step), with inputs resident in HBM and L2 flushed
 between timed steps.  ``e2e`` is the same metric measured through the C ABI
 with pinned host buffers: the step's inputs are copied host->device and its
-outputs device->host inside the timed region.
+outputs device->host inside the timed region, the sequences in groups on
+their own streams so that copies overlap kernels (``step.HostStep``),
+replayed as one CUDA graph that includes the copies.
 
     python bench.py [--steps K] [--warmup W] [--workload NAME] [--impl kvp|reference]
 
@@ -412,28 +414,20 @@ def run_kvp(args):
     ms = max_over_ranks(float(np.mean(step_ms)), dev)
 
     # ---- end to end through the C ABI with pinned host buffers ----
-    host_in = {name: getattr(st, name).cpu().pin_memory() for name in ("q", "k_new", "v_new", "cu", "ctx", "bt")}
-    if st.pairs.shape[0]:
-        host_in["pairs"] = st.pairs.cpu().pin_memory()
-    outs = []
-    if st.npf:
-        outs += [st.out_pf, st.lse_pf]
-    if st.ndec:
-        outs += [st.out_dec, st.lse_dec]
-    host_out = [o.cpu().pin_memory() for o in outs]
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    # HostStep: the same calls per group of sequences, each group's copies
+    # overlapping the other groups' kernels.
+    from paged_prefix_reuse_gb300.step import HostStep
+
+    hs = HostStep(st, groups=args.e2e_groups)
+    h2d, d2h = hs.h2d_bytes, hs.d2h_bytes
     e2e_ms = []
     with torch.cuda.stream(stream):
+        hgraph = hs.capture(stream)
         for i in range(args.warmup + args.steps):
             flush_l2()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            for name, t in host_in.items():
-                getattr(st, name).copy_(t, non_blocking=True)
-            st.run(stream)
-            for o, h in zip(outs, host_out):
-                h.copy_(o, non_blocking=True)
+            hgraph.replay()
             b.record(stream)
             stream.synchronize()
             if i >= args.warmup:
@@ -478,7 +472,7 @@ def run_kvp(args):
         "kernel_ms": kern_ms,
         "wall_s": wall,
         "e2e": {"value": job_rate(flops, world, e2e) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "groups": len(hs.groups)},
         "clocks": clk,
     }
     if st.npf:
@@ -872,6 +866,8 @@ def main():
                          "decode_q: decode over a quantized cached prefix; blockmgr: host block manager; "
                          "cacheblend: CacheBlend recompute selection")
     ap.add_argument("--bits", type=int, choices=[8, 4], default=8, help="quantized pool width for --op decode_q")
+    ap.add_argument("--e2e-groups", type=int, default=0,
+                    help="sequence groups of the host-buffer (e2e) step, each on its own stream (0: auto)")
     ap.add_argument("--pdl", type=int, choices=[0, 1], default=1,
                     help="1: programmatic dependent launch between the step's kernels (kvp_set_launch_options)")
     args = ap.parse_args()

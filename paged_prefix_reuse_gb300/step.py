@@ -116,3 +116,166 @@ class DeviceStep:
         """Restore the pool contents the workload started with."""
         self.pool.k.copy_(bits_to_device(self.w.k_pool, self.w.dtype, self.device))
         self.pool.v.copy_(bits_to_device(self.w.v_pool, self.w.dtype, self.device))
+
+
+class HostStep:
+    """The step from pinned host buffers, with its transfers overlapped.
+
+    The inputs (q, the new K/V, the tables and the copy-on-write pairs) sit in
+    pinned host memory and the outputs (O and LSE) go back to pinned host
+    memory.  The prefill sequences are split into ``groups`` contiguous
+    ranges of about equal token counts (0: one group per GPU's worth of
+    prefix-attention CTAs, see ``auto_groups``) and the decode batch forms one more
+    group; each group runs on its own stream as host->device copy of its
+    tokens, slot mapping, append, attention and device->host copy of its
+    outputs, so one group's copies overlap another group's kernels and the
+    two copy directions overlap each other.  The tables of all groups travel
+    in one copy on ``stream``, followed by the copy-on-write block copies;
+    every group's kernels wait for both.  Groups share no pool block they write (a write
+    goes only into a block its sequence owns alone), so their order does not
+    matter.
+
+    The groups' calls are the library calls the one-stream step makes, on
+    slices of the same device buffers; with the same split counts the
+    outputs are bit-identical to ``DeviceStep.run``.  LSE comes back per
+    group (``lse_host[i]`` is [Hq, tokens of group i]).
+    """
+
+    def __init__(self, st: DeviceStep, groups: int = 0, prefix_splits: int = 0, decode_splits: int = 0):
+        self.st = st
+        w = st.w
+        dev = st.device
+        cu = np.asarray(w.cu_seqlens_q, dtype=np.int64)
+        ctx = np.asarray(w.context_lens, dtype=np.int32)
+        bt = np.ascontiguousarray(w.block_tables, dtype=np.int32)
+        mb = int(bt.shape[1])
+        Hq, d = w.num_q_heads, w.head_dim
+        if groups <= 0:
+            groups = self.auto_groups(w, st.npf)
+        ranges = []
+        if st.npf and st.tq:
+            tq = int(cu[st.npf])
+            bounds = [0]
+            for k in range(1, max(1, groups)):
+                s = int(np.searchsorted(cu[1 : st.npf + 1], tq * k / groups)) + 1
+                bounds.append(min(max(s, bounds[-1]), st.npf))
+            bounds.append(st.npf)
+            ranges = [("prefill", a, b) for a, b in zip(bounds[:-1], bounds[1:]) if cu[b] > cu[a]]
+        if st.ndec:
+            ranges.append(("decode", st.npf, st.npf + st.ndec))
+
+        parts, off = [], 0
+
+        def put(a):
+            nonlocal off
+            a = np.ascontiguousarray(a, dtype=np.int32).ravel()
+            start = off
+            pad = (-a.size) % 4  # 16-byte aligned starts
+            parts.append(np.concatenate([a, np.zeros(pad, dtype=np.int32)]))
+            off += a.size + pad
+            return start, a.size
+
+        self.groups = []
+        for kind, a, b in ranges:
+            g = {"kind": kind, "n": b - a, "t0": int(cu[a]), "t1": int(cu[b]),
+                 "cu": put(cu[a : b + 1] - cu[a]), "ctx": put(ctx[a:b]), "bt": put(bt[a:b]),
+                 "max_q": int(np.diff(cu[a : b + 1]).max()), "max_ctx": int(ctx[a:b].max())}
+            self.groups.append(g)
+        meta = np.concatenate(parts) if parts else np.zeros(4, dtype=np.int32)
+        self.h_meta = torch.from_numpy(meta).pin_memory()
+        self.d_meta = torch.empty(meta.shape, dtype=torch.int32, device=dev)
+        for g in self.groups:
+            n, T = g["n"], g["t1"] - g["t0"]
+            g["d_cu"] = self.d_meta[g["cu"][0] : g["cu"][0] + n + 1]
+            g["d_ctx"] = self.d_meta[g["ctx"][0] : g["ctx"][0] + n]
+            g["d_bt"] = self.d_meta[g["bt"][0] : g["bt"][0] + n * mb].view(n, mb)
+            g["lse"] = torch.empty((Hq, T), dtype=torch.float32, device=dev)
+            g["lse_host"] = torch.empty((Hq, T), dtype=torch.float32).pin_memory()
+            if g["kind"] == "prefill":
+                g["splits"] = prefix_splits or st.prefix_splits
+                need = kvp_workspace_size(0, T, Hq, d, g["splits"])
+            else:
+                g["splits"] = decode_splits or st.decode_splits
+                need = kvp_workspace_size(1, T, Hq, d, g["splits"])
+            g["ws"] = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        self.lse_host = [g["lse_host"] for g in self.groups]
+        self.h_q = st.q.cpu().pin_memory()
+        self.h_k = st.k_new.cpu().pin_memory()
+        self.h_v = st.v_new.cpu().pin_memory()
+        self.h_pairs = st.pairs.cpu().pin_memory()
+        self.out_host = torch.empty(st.q.shape, dtype=st.q.dtype).pin_memory()  # O of every token
+        self.streams = [torch.cuda.Stream(device=dev) for _ in self.groups]
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in (self.h_meta, self.h_q, self.h_k, self.h_v,
+                                                                     self.h_pairs))
+        self.d2h_bytes = self.out_host.numel() * self.out_host.element_size() + sum(
+            g["lse_host"].numel() * 4 for g in self.groups)
+
+    @staticmethod
+    def auto_groups(w, npf: int, sms: int = 152, rows_per_cta: int = 256, most: int = 4) -> int:
+        """One group per GPU's worth of prefix-attention CTAs (at most
+        ``most``): a group that leaves SMs idle gains nothing from starting
+        early, and each group adds its own launches and copies."""
+        if npf <= 0:
+            return 1
+        g = w.num_q_heads // w.num_kv_heads
+        n = np.diff(np.asarray(w.cu_seqlens_q, dtype=np.int64))[:npf]
+        ctas = int(np.sum((n * g + rows_per_cta - 1) // rows_per_cta)) * w.num_kv_heads
+        return max(1, min(most, ctas // sms))
+
+    def run(self, stream=None):
+        """Enqueue the step; everything is ordered before work later queued on
+        ``stream`` (default: current stream).  The host outputs are complete
+        once that stream has passed this point."""
+        st = self.st
+        s0 = stream if stream is not None else torch.cuda.current_stream()
+        # Every group stream first follows ``stream`` (in a graph capture, this
+        # is how a side stream joins the capture).
+        fork = torch.cuda.Event()
+        fork.record(s0)
+        with torch.cuda.stream(s0):
+            self.d_meta.copy_(self.h_meta, non_blocking=True)
+            if st.pairs.shape[0]:
+                st.pairs.copy_(self.h_pairs, non_blocking=True)
+                kvp_block_copy(st.pool, st.pairs, stream=s0)
+        ready = torch.cuda.Event()
+        ready.record(s0)
+        done = []
+        for g, s in zip(self.groups, self.streams):
+            t0, t1 = g["t0"], g["t1"]
+            s.wait_event(fork)
+            with torch.cuda.stream(s):
+                # The group's tokens need no table: their copies start at once.
+                st.q[t0:t1].copy_(self.h_q[t0:t1], non_blocking=True)
+                st.k_new[t0:t1].copy_(self.h_k[t0:t1], non_blocking=True)
+                st.v_new[t0:t1].copy_(self.h_v[t0:t1], non_blocking=True)
+                s.wait_event(ready)
+                kvp_slot_mapping(st.pool, g["d_cu"], g["d_ctx"], g["d_bt"], t1 - t0, out=st.slots[t0:t1], stream=s)
+                kvp_cache_append(st.pool, st.k_new[t0:t1], st.v_new[t0:t1], st.slots[t0:t1], stream=s)
+                if g["kind"] == "prefill":
+                    out = st.out_pf[t0:t1]
+                    kvp_prefix_attn(st.pool, st.q[t0:t1], g["d_cu"], g["d_ctx"], g["d_bt"], g["max_q"], g["max_ctx"],
+                                    st.scale, num_splits=g["splits"], out=out, lse=g["lse"], workspace=g["ws"],
+                                    stream=s)
+                else:
+                    out = st.out_dec
+                    kvp_decode_attn(st.pool, st.q[t0:t1], g["d_ctx"], g["d_bt"], g["max_ctx"], st.scale,
+                                    num_splits=g["splits"], out=out, lse=g["lse"], workspace=g["ws"], stream=s)
+                self.out_host[t0:t1].copy_(out, non_blocking=True)
+                g["lse_host"].copy_(g["lse"], non_blocking=True)
+            e = torch.cuda.Event()
+            e.record(s)
+            done.append(e)
+        for e in done:
+            s0.wait_event(e)
+
+    def capture(self, stream) -> torch.cuda.CUDAGraph:
+        """The step as one CUDA graph, copies included: each replay moves the
+        current contents of the pinned inputs in, runs every group and moves
+        the outputs out, with no host work per step.  ``stream`` is the
+        capture (and replay-ordering) stream."""
+        self.run(stream)  # once outside capture: the library's one-time setup
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            self.run(stream)
+        return graph
