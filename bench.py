@@ -110,7 +110,9 @@ def _peak_value(peaks, *keys):
 # (own block tables, Q and O), so its traffic is four times B=1's.
 TRAFFIC_PROXY = {"long_context_prefix": ("long_context_prefix_b1", 4.0)}
 # The source files a kernel's code comes from (besides kvp_internal.cuh).
-KERNEL_SOURCES = {"prefix": ["kvp_prefix.cu"], "decode": ["kvp_decode.cu", "kvp_decode_impl.cuh"]}
+KERNEL_SOURCES = {"prefix": ["kvp_prefix.cu"], "decode": ["kvp_decode.cu", "kvp_decode_impl.cuh"],
+                  "decode_q_int8": ["kvp_quant.cu", "kvp_decode_impl.cuh"], "deviation": ["kvp_cacheblend.cu"],
+                  "block_swap": ["kvp_cache.cu"]}
 
 
 def committed_traffic(kernel: str, workload: str):
@@ -587,7 +589,9 @@ def run_swap(args):
         "out_gbs": gbs(t_out), "in_gbs": gbs(t_in), "gpu_launches": 2,
         "roofline": {"bound": "host link", "achieved": value, "peak": peak, "unit": "GB/s", "frac": value / peak,
                      "peak_source": "one contiguous pinned cudaMemcpyAsync of the same bytes each way, this run",
-                     "memcpy_d2h_gbs": gbs(t_d2h), "memcpy_h2d_gbs": gbs(t_h2d), "traffic": None},
+                     "memcpy_d2h_gbs": gbs(t_d2h), "memcpy_h2d_gbs": gbs(t_h2d),
+                     # device DRAM bytes of one swap-out launch (the host side is not device DRAM)
+                     "traffic": committed_traffic("block_swap", "continuous_batching_step_swap_out")},
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -675,7 +679,8 @@ def run_decode_q(args):
             len(ctx), hkv, bs, mctx) > 1 else 0),
         "roofline": {"kernel": "decode_attn_q", "bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
                      "frac": gbs / hbm, "peak_source": f"{peak_src} HBM copy",
-                     "traffic": None},
+                     "traffic": committed_traffic("decode_q_int8", "continuous_batching_step_int8_prefix")
+                     if args.bits == 8 else None},
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -843,7 +848,8 @@ def run_cacheblend(args):
                    "l2": "flushed before every timed call"},
         "deviation_ms": t_dev * 1e3, "select_ms": t_sel * 1e3, "overwrite_ms": t_ovw * 1e3, "gpu_launches": 3,
         "roofline": {"kernel": "kv_deviation", "bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
-                     "frac": gbs / hbm, "peak_source": f"{peak_src} HBM copy", "traffic": None},
+                     "frac": gbs / hbm, "peak_source": f"{peak_src} HBM copy",
+                     "traffic": committed_traffic("deviation", "rag_chunk_reuse_cached")},
     }
     print(json.dumps(line), flush=True)
     return 0
