@@ -219,5 +219,5 @@ def test_workspace_and_split_helpers(lib):
     assert kvp.kvp_prefix_num_splits(1, 2, 2, 64, 16, 48) == 1
     assert kvp.kvp_prefix_num_splits(8, 16, 2, 128, 256, 1280) == 1  # 128 CTAs: no split
     assert kvp.kvp_prefix_num_splits(1, 8, 8, 128, 128, 32768) >= 2  # 8 CTAs over 256 key tiles: split
-    assert kvp.kvp_decode_num_splits(64, 8, 16, 8193) == 17
-    assert kvp.kvp_decode_num_splits(1, 1, 16, 300) == 3
+    assert kvp.kvp_decode_num_splits(64, 8, 16, 8193) == 9  # about 1024 keys per split
+    assert kvp.kvp_decode_num_splits(1, 1, 16, 300) == 3  # few pairs: >= 128 keys per split, more CTAs
