@@ -191,7 +191,7 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }
 
 template <bool kBF16, int D, int SK, int BITS>
-__global__ void __launch_bounds__(kDecodeThreads, 4)
+__global__ void __launch_bounds__(kDecodeThreads, BITS ? 4 : 5)
     decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                   const DecodeParams p) {
     using C = DecodeCfg<D, SK, BITS>;
