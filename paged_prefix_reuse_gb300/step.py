@@ -152,17 +152,7 @@ class HostStep:
         Hq, d = w.num_q_heads, w.head_dim
         if groups <= 0:
             groups = self.auto_groups(w, st.npf)
-        ranges = []
-        if st.npf and st.tq:
-            tq = int(cu[st.npf])
-            bounds = [0]
-            for k in range(1, max(1, groups)):
-                s = int(np.searchsorted(cu[1 : st.npf + 1], tq * k / groups)) + 1
-                bounds.append(min(max(s, bounds[-1]), st.npf))
-            bounds.append(st.npf)
-            ranges = [("prefill", a, b) for a, b in zip(bounds[:-1], bounds[1:]) if cu[b] > cu[a]]
-        if st.ndec:
-            ranges.append(("decode", st.npf, st.npf + st.ndec))
+        ranges = self.partition(cu, st.npf, st.ndec, groups)
 
         parts, off = [], 0
 
@@ -209,6 +199,25 @@ class HostStep:
                                                                      self.h_pairs))
         self.d2h_bytes = self.out_host.numel() * self.out_host.element_size() + sum(
             g["lse_host"].numel() * 4 for g in self.groups)
+
+    @staticmethod
+    def partition(cu_seqlens_q, npf: int, ndec: int, groups: int):
+        """[(kind, first sequence, end sequence)]: the prefill sequences [0, npf)
+        cut into at most ``groups`` contiguous ranges of about equal token
+        counts (ranges without tokens dropped), then the decode batch."""
+        cu = np.asarray(cu_seqlens_q, dtype=np.int64)
+        ranges = []
+        if npf and cu[npf] > 0:
+            tq = int(cu[npf])
+            bounds = [0]
+            for k in range(1, max(1, groups)):
+                s = int(np.searchsorted(cu[1 : npf + 1], tq * k / groups)) + 1
+                bounds.append(min(max(s, bounds[-1]), npf))
+            bounds.append(npf)
+            ranges = [("prefill", a, b) for a, b in zip(bounds[:-1], bounds[1:]) if cu[b] > cu[a]]
+        if ndec:
+            ranges.append(("decode", npf, npf + ndec))
+        return ranges
 
     @staticmethod
     def auto_groups(w, npf: int, sms: int = 152, rows_per_cta: int = 256, most: int = 4) -> int:
