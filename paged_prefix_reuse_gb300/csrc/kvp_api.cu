@@ -37,10 +37,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // The pool viewed as a 2-D tensor of rows (block, kv head, slot) x head_dim;
 // one TMA box is one block of one kv head, `chunk_elems` columns wide.
-kvp_status make_pool_map(CUtensorMap* map, void* base, const kvp_pool* pool) {
+kvp_status make_pool_map(CUtensorMap* map, void* base, const kvp_pool* pool, int CW = 0) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return KVP_ERR_CUDA;
-    const int D = pool->head_dim, CW = chunk_elems(D);
+    const int D = pool->head_dim;
+    if (CW == 0) CW = chunk_elems(D);  // else a box wider than the row reads zeros past it
     const cuuint64_t rows = static_cast<cuuint64_t>(pool->num_blocks) * pool->num_kv_heads * pool->block_size;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), rows};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
@@ -285,8 +286,9 @@ kvp_status kvp_prefix_attn(const kvp_pool* pool, const void* q, void* out, float
         p.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(r * pool->head_dim * 4));
     }
     CUtensorMap tk, tv;
-    if ((st = make_pool_map(&tk, pool->k_pool, pool)) != KVP_OK) return st;
-    if ((st = make_pool_map(&tv, pool->v_pool, pool)) != KVP_OK) return st;
+    const int pcw = prefix_chunk_elems(pool->head_dim);
+    if ((st = make_pool_map(&tk, pool->k_pool, pool, pcw)) != KVP_OK) return st;
+    if ((st = make_pool_map(&tv, pool->v_pool, pool, pcw)) != KVP_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_prefix_attn(p, tk, tv, s);
     if (e != cudaSuccess) return KVP_ERR_CUDA;

@@ -115,6 +115,9 @@ cudaError_t launch_prefix_attn(const PrefixParams& p, const CUtensorMap& tmap_k,
                                cudaStream_t stream);
 // Query rows (token, head-of-group pairs) one prefix CTA covers.
 int prefix_rows_per_cta();
+// Columns of one TMA box of the prefix kernel's K/V tiles (64 at head_dim 96:
+// that kernel runs head_dim 96 padded to 128).
+int prefix_chunk_elems(int head_dim);
 cudaError_t launch_decode_attn(const DecodeParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                cudaStream_t stream);
 // Merge of split partials: rows = total_q*Hq (prefix) or B*Hq (decode), with

@@ -52,6 +52,13 @@ constexpr int kBN = 128;  // keys per K/V tile
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSmemBudget = 227 * 1024 - 2048;
 
+// Width of the shared-memory tiles and of the products: head_dim 96 runs as
+// 128 with zero columns, because a 96-column page needs three 32-column TMA
+// boxes (64B swizzle) where 128 takes two 64-column ones (128B swizzle; the
+// second box's columns past 96 are out of the tensor and arrive as zeros).
+// At d = 96 the kernel is bound by its TMA box rate, not by its products.
+__host__ __device__ constexpr int prefix_width(int head_dim) { return head_dim == 96 ? 128 : head_dim; }
+
 template <int D>
 struct PrefixCfg {
     static constexpr int CW = chunk_elems(D);
@@ -127,7 +134,8 @@ template <bool kBF16, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefix_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                   const PrefixParams p) {
-    using C = PrefixCfg<D>;
+    constexpr int DP = prefix_width(D);  // tile and product width (>= D; the extra columns are zeros)
+    using C = PrefixCfg<DP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -245,6 +253,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int rr = e / V16, c16 = e % V16;
                     const int ch = c16 / (C::CW / 8), ci = c16 % (C::CW / 8);
                     *reinterpret_cast<uint4*>(qt + ch * C::CHUNK_BYTES + swz_offset(rr, ci, C::ROWB)) = qv[k];
+                }
+#pragma unroll
+                for (int c16 = V16; c16 < DP / 8; ++c16) {  // padded columns of this thread's row: zeros
+                    const int ch = c16 / (C::CW / 8), ci = c16 % (C::CW / 8);
+                    *reinterpret_cast<uint4*>(qt + ch * C::CHUNK_BYTES + swz_offset(row, ci, C::ROWB)) =
+                        make_uint4(0, 0, 0, 0);
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&q_full[wg]);
@@ -462,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ============================ MMA issuer warp ============================
         constexpr uint32_t idesc_s = instr_desc_f16(kBF16, kBM, kBN, false);
-        constexpr uint32_t idesc_o = instr_desc_f16(kBF16, kBM, D, true);
+        constexpr uint32_t idesc_o = instr_desc_f16(kBF16, kBM, DP, true);
         const uint32_t ring = smem_u32(smem + C::OFF_RING);
         const uint32_t qb0 = smem_u32(smem + C::OFF_Q), qb1 = qb0 + C::TILE_BYTES;
         uint64_t* last_bar = nullptr;
@@ -480,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto issue_s = [&](int i, uint32_t kbase) {
             const uint32_t qb = i ? qb1 : qb0;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
+            for (int kk = 0; kk < DP / 16; ++kk) {
                 const uint32_t off = ((kk * 16) / C::CW) * C::CHUNK_BYTES + ((kk * 16) % C::CW) * 2;
                 const uint64_t ad = smem_desc(qb + off, 16, 8 * C::ROWB, C::SWZ);
                 const uint64_t bd = smem_desc(kbase + off, 16, 8 * C::ROWB, C::SWZ);
@@ -572,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <bool kBF16, int D>
 cudaError_t launch_prefix_t(const PrefixParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                             cudaStream_t stream) {
-    using C = PrefixCfg<D>;
+    using C = PrefixCfg<prefix_width(D)>;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(prefix_kernel<kBF16, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -587,6 +601,8 @@ cudaError_t launch_prefix_t(const PrefixParams& p, const CUtensorMap& tk, const 
 }  // namespace
 
 int prefix_rows_per_cta() { return kRowsPerCta; }
+
+int prefix_chunk_elems(int head_dim) { return chunk_elems(prefix_width(head_dim)); }
 
 cudaError_t launch_prefix_attn(const PrefixParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                cudaStream_t stream) {
