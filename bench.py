@@ -123,17 +123,31 @@ def committed_traffic(kernel: str, workload: str):
     return _committed_traffic(kernel, workload)
 
 
+def code_digest(paths) -> str:
+    """sha256 (16 hex digits) of the files' code with their // comments and
+    blank lines removed: a comment edit leaves a kernel, and its counters,
+    unchanged.  (The CUDA sources hold no string literal containing //.)"""
+    h = hashlib.sha256()
+    for path in paths:
+        for line in open(path, encoding="utf-8"):
+            code = line.split("//", 1)[0].rstrip()
+            if code:
+                h.update(code.encode() + b"\n")
+    return h.hexdigest()[:16]
+
+
 def _committed_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if that summary
-    was taken on the kernel source as it is now -- the kernel's source files
-    and the shared kvp_internal.cuh, hashed together -- else None."""
+    was taken on the kernel code as it is now -- the kernel's source files and
+    the shared kvp_internal.cuh, hashed together without comments -- else
+    None."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
     csrc = os.path.join(ROOT, "paged_prefix_reuse_gb300", "csrc")
     srcs = [os.path.join(csrc, f) for f in KERNEL_SOURCES.get(kernel, [f"kvp_{kernel}.cu"])]
     srcs.append(os.path.join(csrc, "kvp_internal.cuh"))
     if not (os.path.exists(path) and all(os.path.exists(f) for f in srcs)):
         return None
-    digest = hashlib.sha256(b"".join(open(f, "rb").read() for f in srcs)).hexdigest()[:16]
+    digest = code_digest(srcs)
     vals = {}
     for line in open(path):
         if ":" in line:

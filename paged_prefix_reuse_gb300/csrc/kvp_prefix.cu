@@ -18,10 +18,12 @@
 //  * warp 8 (producer) gathers 128-key K and V tiles into a ring of shared
 //    memory slots with 2-D TMA boxes, one box per (physical block, 64-column
 //    chunk) found through the block table, one lane per block; 128B-swizzled
-//    (64B at d=96) to match the UMMA descriptors;
-//  * warp 9 (MMA) issues tcgen05.mma from one thread: S_i = Q_i K^T (SS,
-//    M=128, N=128) into TMEM, and O_i += P_i V (TS: P_i read from TMEM,
-//    M=128, N=d).  The two query tiles alternate on the tensor core --
+//    to match the UMMA descriptors (head_dim 96 runs 128 wide: see
+//    prefix_width);
+//  * warp 9 (MMA) runs converged and elects one lane to issue each
+//    tcgen05.mma: S_i = Q_i K^T (SS, M=128, N=128) into TMEM, and
+//    O_i += P_i V (TS: P_i read from TMEM, M=128, N = the tile width).  The
+//    two query tiles alternate on the tensor core --
 //    PV_0, S_0, PV_1, S_1 -- so each softmax warpgroup works while the tensor
 //    core serves the other;
 //  * warps 0-3 and 4-7 (softmax warpgroups, one per query tile; thread i
