@@ -10,9 +10,13 @@ raises ``KvpLibraryMissing``.
 Functions carry the names of the C entry points declared in
 ``include/kvp.h``: ``kvp_slot_mapping``, ``kvp_cache_append``,
 ``kvp_block_copy``, ``kvp_block_swap``, ``kvp_quantize_blocks``,
-``kvp_kv_deviation``, ``kvp_select_recompute``,
-``kvp_prefix_attn``, ``kvp_decode_attn``, ``kvp_decode_attn_q`` and
-``kvp_workspace_size`` (plus the split-count helpers).
+``kvp_kv_deviation``, ``kvp_select_recompute``, ``kvp_prefix_attn``,
+``kvp_decode_attn``, ``kvp_decode_attn_noalloc``, ``kvp_decode_attn_q``,
+``kvp_workspace_size``, the split-count helpers and
+``kvp_set_launch_options``.  ``BlockManager`` and ``kvp_hash_chunks`` wrap
+the host block manager of ``include/kvp_blockmgr.h``.  ``step`` runs a
+whole step from device buffers (``DeviceStep``) or from pinned host buffers
+(``HostStep``).
 """
 from __future__ import annotations
 
