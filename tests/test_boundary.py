@@ -221,3 +221,33 @@ def test_workspace_and_split_helpers(lib):
     assert kvp.kvp_prefix_num_splits(1, 8, 8, 128, 128, 32768) >= 2  # 8 CTAs over 256 key tiles: split
     assert kvp.kvp_decode_num_splits(64, 8, 16, 8193) == 9  # about 1024 keys per split
     assert kvp.kvp_decode_num_splits(1, 1, 16, 300) == 3  # few pairs: >= 128 keys per split, more CTAs
+
+
+def test_launch_options_round_trip(lib):
+    before = kvp.kvp_get_launch_options()
+    try:
+        kvp.kvp_set_launch_options(kvp.LAUNCH_PDL)
+        assert kvp.kvp_get_launch_options() == kvp.LAUNCH_PDL == 0x1
+        kvp.kvp_set_launch_options(0)
+        assert kvp.kvp_get_launch_options() == 0
+    finally:
+        kvp.kvp_set_launch_options(before)
+
+
+def test_noalloc_decode_host_checks(lib):
+    """kvp_decode_attn_noalloc refuses, before any device work, what its fixed
+    scratch array cannot hold, and checks its own arguments."""
+    pool = _pool(head_dim=128)
+
+    def call(P, B=1, Hq=2, max_ctx=48, splits=1):
+        return lib.kvp_decode_attn_noalloc(P, 0x30000, 0x40000, None, 0x60000, 0x70000, 4, B, Hq, max_ctx, 0.125,
+                                           splits, None)
+
+    assert call(None) == KVP_ERR_INVALID_ARG
+    assert call(ctypes.byref(pool), Hq=0) == KVP_ERR_INVALID_ARG
+    assert call(ctypes.byref(pool), splits=-1) == KVP_ERR_INVALID_ARG
+    assert call(ctypes.byref(pool), B=0) == KVP_OK
+    # 4096 sequences x 64 heads x 64 splits of fp32 partials: far beyond 32 MiB
+    need = kvp.kvp_workspace_size(1, 4096, 64, 128, 64)
+    assert need > kvp.DECODE_NOALLOC_SCRATCH_BYTES
+    assert call(ctypes.byref(pool), B=4096, Hq=64, max_ctx=65536, splits=64) == KVP_ERR_WORKSPACE
