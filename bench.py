@@ -17,6 +17,7 @@ their own streams so that copies overlap kernels (``step.HostStep``),
 replayed as one CUDA graph that includes the copies.
 
     python bench.py [--steps K] [--warmup W] [--workload NAME] [--impl kvp|reference]
+    python bench.py --op block_swap|decode_q [--bits 8|4]|blockmgr|cacheblend
 
 With several GPUs (torchrun), every rank runs an independent replica (the
 path has no exchange step) and the slowest rank's time is reported.
@@ -871,16 +872,19 @@ def run_cacheblend(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", choices=["kvp", "reference"], default="kvp")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="shared_system_prompt")
-    ap.add_argument("--prefix-splits", type=int, default=0)
-    ap.add_argument("--decode-splits", type=int, default=0)
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--preroll-s", type=float, default=0.4)
+    ap.add_argument("--gpus", type=int, default=1, help="GPUs of the run (replicas; launch N > 1 with torchrun)")
+    ap.add_argument("--steps", type=int, default=20, help="timed steps")
+    ap.add_argument("--warmup", type=int, default=5, help="untimed warm-up steps (at least 3)")
+    ap.add_argument("--impl", choices=["kvp", "reference"], default="kvp",
+                    help="kvp: the CUDA library; reference: the fp64 oracle on the host cores")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="shared_system_prompt",
+                    help="synthetic batch shape (default: the shared system prompt)")
+    ap.add_argument("--prefix-splits", type=int, default=0, help="split-KV count of prefix attention (0: the library's)")
+    ap.add_argument("--decode-splits", type=int, default=0, help="split-KV count of decode (0: the library's)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the timed oracle sample")
+    ap.add_argument("--preroll-s", type=float, default=0.4,
+                    help="seconds of untimed steps before timing, so the clock samples see load")
     ap.add_argument("--op", choices=["step", "block_swap", "decode_q", "blockmgr", "cacheblend"], default="step",
                     help="step: the prefill/decode step (default); block_swap: host <-> device page swap; "
                          "decode_q: decode over a quantized cached prefix; blockmgr: host block manager; "
