@@ -310,10 +310,14 @@ kvp_status kvp_decode_attn(const kvp_pool *pool, const void *q, void *out, float
  * because each call writes every partial it reads.  Calls whose kernels
  * overlap on the GPU (e.g. on two streams without ordering) race on the
  * array: order them on one stream or with events.
- * Returns KVP_ERR_WORKSPACE, launching nothing, when the resolved split
- * count needs more than the array holds, i.e. when
- * kvp_workspace_size(1, B, num_q_heads, head_dim, splits) exceeds
- * KVP_DECODE_NOALLOC_SCRATCH_BYTES; pass a smaller num_splits or batch.
+ * Arguments are validated first, with kvp_decode_attn's error codes.  Then
+ * the call returns KVP_ERR_WORKSPACE, launching nothing, when the split count
+ * kvp_decode_attn would resolve (num_splits, or the library's choice for 0,
+ * after rounding each split up to whole 32-key stages -- so a large
+ * num_splits over short contexts may resolve to far fewer) needs more than
+ * the array holds, i.e. when kvp_workspace_size(1, B, num_q_heads, head_dim,
+ * resolved splits) exceeds KVP_DECODE_NOALLOC_SCRATCH_BYTES; pass a smaller
+ * num_splits or batch.
  * It calls no cudaMalloc, cudaFree or other allocating routine. */
 kvp_status kvp_decode_attn_noalloc(const kvp_pool *pool, const void *q, void *out, float *lse,
                                    const int32_t *context_lens, const int32_t *block_tables, int32_t max_blocks,

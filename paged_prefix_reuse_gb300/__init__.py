@@ -269,6 +269,43 @@ def _dev_i32(x, device) -> torch.Tensor:
     return t.to(device, non_blocking=True).contiguous()
 
 
+def _arg(t, name: str, dtype, ndim: int | None = None, tail: tuple | None = None, optional: bool = False):
+    """The C ABI sees only a pointer, so check here what it cannot: the
+    element type, the layout (dense, row-major), the device and the trailing
+    shape.  An fp16 q against a bf16 pool, or a transposed view, would
+    otherwise be read as garbage without an error."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor, not {type(t).__name__}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}; expected {dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, not {t.dim()}")
+    if tail is not None and tuple(t.shape[-len(tail):]) != tuple(tail):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}; its trailing dimensions must be {tuple(tail)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (row-major, no strides or transposes)")
+
+
+def _on_device(**tensors):
+    """After the structural checks of a call: every tensor is device memory."""
+    for name, t in tensors.items():
+        if t is not None and not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _decode_index_args(q, context_lens, block_tables, out, lse):
+    _arg(context_lens, "context_lens", torch.int32, 1)
+    _arg(block_tables, "block_tables", torch.int32, 2)
+    _arg(out, "out", q.dtype, 3, tuple(q.shape), optional=True)
+    _arg(lse, "lse", torch.float32, 2, (q.shape[1], q.shape[0]), optional=True)
+    if context_lens.shape[0] != q.shape[0] or block_tables.shape[0] < q.shape[0]:
+        raise ValueError("context_lens and block_tables need one row per sequence of q")
+
+
 class PagedKVPool:
     """A pool of physical KV blocks: k/v tensors [num_blocks, Hkv, block_size, d].
 
@@ -317,6 +354,14 @@ def kvp_kv_deviation(pool: PagedKVPool, k_fresh: torch.Tensor, v_fresh: torch.Te
                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Per-token 1 - cos([K;V] in the pool at slots[t], [K;V] fresh[t]) (float32 [T])."""
     T = int(slots.shape[0])
+    tail = (pool.num_kv_heads, pool.head_dim)
+    _arg(k_fresh, "k_fresh", pool.dtype, 3, tail)
+    _arg(v_fresh, "v_fresh", pool.dtype, 3, tail)
+    _arg(slots, "slots", torch.int64, 1)
+    _arg(out, "out", torch.float32, 1, optional=True)
+    if k_fresh.shape[0] != T or v_fresh.shape[0] != T:
+        raise ValueError("k_fresh, v_fresh and slots must have one row per token")
+    _on_device(k_fresh=k_fresh, v_fresh=v_fresh, slots=slots, out=out)
     if out is None:
         out = torch.empty(T, dtype=torch.float32, device=slots.device)
     _check(load_library().kvp_kv_deviation(pool.c, _ptr(k_fresh), _ptr(v_fresh), _ptr(slots), T, _ptr(out),
@@ -328,6 +373,10 @@ def kvp_select_recompute(deviation: torch.Tensor, slots: torch.Tensor, cu_seqlen
                          permille: int = 150, stream=None):
     """CacheBlend selection: -> (recompute_slots int64 [T] (-1 = keep), counts int32 [B]).
     Follow with kvp_cache_append(pool, k_fresh, v_fresh, recompute_slots)."""
+    _arg(deviation, "deviation", torch.float32, 1)
+    _arg(slots, "slots", torch.int64, 1)
+    _arg(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    _on_device(deviation=deviation, slots=slots, cu_seqlens=cu_seqlens)
     B = int(cu_seqlens.shape[0]) - 1
     rs = torch.empty_like(slots)
     counts = torch.empty(max(B, 0), dtype=torch.int32, device=slots.device)
@@ -374,6 +423,8 @@ class QuantKVPool:
 
 def kvp_quantize_blocks(pool: PagedKVPool, qpool: QuantKVPool, pairs: torch.Tensor, stream=None) -> None:
     """qpool[dst] = quantize(pool[src]) per (src, dst) row of ``pairs`` (device int32 [n, 2])."""
+    _arg(pairs, "pairs", torch.int32, 2, (2,))
+    _on_device(pairs=pairs)
     lib = load_library()
     n = int(pairs.shape[0]) if pairs.numel() else 0
     _check(lib.kvp_quantize_blocks(pool.c, qpool.c, _ptr(pairs) if n else None, n, _stream(stream)),
@@ -388,6 +439,10 @@ def kvp_decode_attn_q(pool: PagedKVPool, qpool: QuantKVPool, qpages: torch.Tenso
     """Decode attention where the first ``qpages[s]`` table entries of each
     sequence name blocks of the quantized pool and the rest blocks of the
     16-bit pool.  Returns (out [B, Hq, d], lse [Hq, B] float32 or None)."""
+    _arg(q, "q", pool.dtype, 3, (pool.head_dim,))
+    _arg(qpages, "qpages", torch.int32, 1)
+    _decode_index_args(q, context_lens, block_tables, out, lse)
+    _on_device(q=q, qpages=qpages, context_lens=context_lens, block_tables=block_tables, out=out, lse=lse)
     lib = load_library()
     B, Hq, d = (int(x) for x in q.shape)
     if out is None:
@@ -584,6 +639,8 @@ def kvp_block_swap(pool: PagedKVPool, host: HostKVPool, pairs: torch.Tensor, dir
     ``pairs`` (device int32 [n, 2])."""
     if tuple(host.k.shape[1:]) != (pool.num_kv_heads, pool.block_size, pool.head_dim) or host.k.dtype != pool.dtype:
         raise ValueError("host pool geometry or dtype differs from the device pool")
+    _arg(pairs, "pairs", torch.int32, 2, (2,))
+    _on_device(pairs=pairs)
     lib = load_library()
     n = int(pairs.shape[0]) if pairs.numel() else 0
     _check(lib.kvp_block_swap(pool.c, host.c, _ptr(pairs) if n else None, n, int(direction), _stream(stream)),
@@ -607,6 +664,11 @@ def kvp_slot_mapping(pool: PagedKVPool, cu_seqlens_q: torch.Tensor, context_lens
                      block_tables: torch.Tensor, total_q: int, out: torch.Tensor | None = None,
                      stream=None) -> torch.Tensor:
     """Pool slot of every new token (int64 [total_q]); see kvp.h."""
+    _arg(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _arg(context_lens, "context_lens", torch.int32, 1)
+    _arg(block_tables, "block_tables", torch.int32, 2)
+    _arg(out, "out", torch.int64, 1, optional=True)
+    _on_device(cu_seqlens_q=cu_seqlens_q, context_lens=context_lens, block_tables=block_tables, out=out)
     lib = load_library()
     if out is None:
         out = torch.empty(total_q, dtype=torch.int64, device=pool.k.device)
@@ -620,14 +682,23 @@ def kvp_slot_mapping(pool: PagedKVPool, cu_seqlens_q: torch.Tensor, context_lens
 def kvp_cache_append(pool: PagedKVPool, k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
                      stream=None) -> None:
     """Scatter new K/V [T, Hkv, d] into the pool slots (-1 = skip)."""
+    tail = (pool.num_kv_heads, pool.head_dim)
+    _arg(k_new, "k_new", pool.dtype, 3, tail)
+    _arg(v_new, "v_new", pool.dtype, 3, tail)
+    _arg(slot_mapping, "slot_mapping", torch.int64, 1)
+    T = int(k_new.shape[0])
+    if v_new.shape[0] != T or slot_mapping.shape[0] < T:
+        raise ValueError("k_new, v_new and slot_mapping must have one row per token")
+    _on_device(k_new=k_new, v_new=v_new, slot_mapping=slot_mapping)
     lib = load_library()
-    T = int(k_new.shape[0]) if k_new.dim() else 0
     _check(lib.kvp_cache_append(pool.c, _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), T, _stream(stream)),
            "kvp_cache_append")
 
 
 def kvp_block_copy(pool: PagedKVPool, pairs: torch.Tensor, stream=None) -> None:
     """Copy-on-write fork: pool[dst] = pool[src] for each (src, dst) row of ``pairs``."""
+    _arg(pairs, "pairs", torch.int32, 2, (2,))
+    _on_device(pairs=pairs)
     lib = load_library()
     n = int(pairs.shape[0]) if pairs.numel() else 0
     _check(lib.kvp_block_copy(pool.c, _ptr(pairs) if n else None, n, _stream(stream)), "kvp_block_copy")
@@ -639,6 +710,13 @@ def kvp_prefix_attn(pool: PagedKVPool, q: torch.Tensor, cu_seqlens_q: torch.Tens
                     workspace: torch.Tensor | None = None, want_lse: bool = True, stream=None):
     """Causal attention of the packed new tokens q [T, Hq, d] over their
     sequences' paged K/V.  Returns (out [T, Hq, d], lse [Hq, T] float32 or None)."""
+    _arg(q, "q", pool.dtype, 3, (pool.head_dim,))
+    _arg(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _arg(context_lens, "context_lens", torch.int32, 1)
+    _arg(block_tables, "block_tables", torch.int32, 2)
+    _arg(out, "out", pool.dtype, 3, tuple(q.shape), optional=True)
+    _arg(lse, "lse", torch.float32, 2, (q.shape[1], q.shape[0]), optional=True)
+    _on_device(q=q, cu_seqlens_q=cu_seqlens_q, context_lens=context_lens, block_tables=block_tables, out=out, lse=lse)
     lib = load_library()
     T, Hq, d = (int(x) for x in q.shape)
     B = int(context_lens.shape[0])
@@ -665,6 +743,9 @@ def kvp_decode_attn(pool: PagedKVPool, q: torch.Tensor, context_lens: torch.Tens
                     workspace: torch.Tensor | None = None, want_lse: bool = True, stream=None):
     """One query per sequence q [B, Hq, d] over its paged context.
     Returns (out [B, Hq, d], lse [Hq, B] float32 or None)."""
+    _arg(q, "q", pool.dtype, 3, (pool.head_dim,))
+    _decode_index_args(q, context_lens, block_tables, out, lse)
+    _on_device(q=q, context_lens=context_lens, block_tables=block_tables, out=out, lse=lse)
     lib = load_library()
     B, Hq, d = (int(x) for x in q.shape)
     if out is None:
@@ -694,6 +775,9 @@ def kvp_decode_attn_noalloc(pool: PagedKVPool, q: torch.Tensor, context_lens: to
     """Decode attention without a workspace: the split partials use the
     library's fixed device array (see kvp.h).  The caller still provides
     ``out`` and ``lse`` (allocated here only when omitted)."""
+    _arg(q, "q", pool.dtype, 3, (pool.head_dim,))
+    _decode_index_args(q, context_lens, block_tables, out, lse)
+    _on_device(q=q, context_lens=context_lens, block_tables=block_tables, out=out, lse=lse)
     lib = load_library()
     B, Hq, d = (int(x) for x in q.shape)
     if out is None:

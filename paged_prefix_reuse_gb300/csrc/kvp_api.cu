@@ -333,12 +333,13 @@ kvp_status kvp_quantize_blocks(const kvp_pool* pool, const kvp_qpool* qpool, con
                                             static_cast<cudaStream_t>(stream)));
 }
 
-// Decode attention, with (qpool != nullptr) or without a quantized prefix.
-static kvp_status decode_common(const kvp_pool* pool, const kvp_qpool* qpool, const int32_t* qpages, const void* q,
-                                void* out, float* lse, const int32_t* context_lens, const int32_t* block_tables,
-                                int32_t max_blocks, int32_t B, int32_t num_q_heads, int32_t max_context_len,
-                                float softmax_scale, int32_t num_splits, void* workspace, size_t workspace_bytes,
-                                void* stream) {
+// Host-side validation of a decode call and its launch parameters (without
+// workspace).  Returns KVP_OK with *empty set when there is nothing to do.
+static kvp_status decode_prepare(const kvp_pool* pool, const kvp_qpool* qpool, const int32_t* qpages, const void* q,
+                                 void* out, float* lse, const int32_t* context_lens, const int32_t* block_tables,
+                                 int32_t max_blocks, int32_t B, int32_t num_q_heads, int32_t max_context_len,
+                                 float softmax_scale, int32_t num_splits, DecodeParams* pp, bool* empty) {
+    *empty = false;
     kvp_status st = check_pool(pool);
     if (st != KVP_OK) return st;
     if (qpool) {
@@ -346,7 +347,10 @@ static kvp_status decode_common(const kvp_pool* pool, const kvp_qpool* qpool, co
         if (pool->block_size != 16) return KVP_ERR_UNSUPPORTED;
     }
     if (B < 0 || max_blocks < 0 || num_splits < 0 || max_context_len < 0) return KVP_ERR_INVALID_ARG;
-    if (B == 0) return KVP_OK;
+    if (B == 0) {
+        *empty = true;
+        return KVP_OK;
+    }
     if (!q || !out || !context_lens || !block_tables || max_blocks == 0) return KVP_ERR_INVALID_ARG;
     if (qpool && !qpages) return KVP_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(out)) return KVP_ERR_INVALID_ARG;
@@ -376,6 +380,21 @@ static kvp_status decode_common(const kvp_pool* pool, const kvp_qpool* qpool, co
     p.ws_lse = nullptr;
     p.qpool = qpool ? qview_of(qpool) : QPoolView{nullptr, nullptr, nullptr, nullptr, 0, 0};
     p.qpages = qpool ? qpages : nullptr;
+    *pp = p;
+    return KVP_OK;
+}
+
+// Decode attention, with (qpool != nullptr) or without a quantized prefix.
+static kvp_status decode_common(const kvp_pool* pool, const kvp_qpool* qpool, const int32_t* qpages, const void* q,
+                                void* out, float* lse, const int32_t* context_lens, const int32_t* block_tables,
+                                int32_t max_blocks, int32_t B, int32_t num_q_heads, int32_t max_context_len,
+                                float softmax_scale, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+    DecodeParams p;
+    bool empty = false;
+    kvp_status st = decode_prepare(pool, qpool, qpages, q, out, lse, context_lens, block_tables, max_blocks, B,
+                                   num_q_heads, max_context_len, softmax_scale, num_splits, &p, &empty);
+    if (st != KVP_OK || empty) return st;
     if (p.max_splits > 1) {
         const size_t need = kvp_workspace_size(1, B, num_q_heads, pool->head_dim, p.max_splits);
         if (!workspace || workspace_bytes < need || !aligned16(workspace)) return KVP_ERR_WORKSPACE;
@@ -414,3 +433,21 @@ kvp_status kvp_decode_attn_q(const kvp_pool* pool, const kvp_qpool* qpool, const
 }
 
 }  // extern "C"
+
+namespace kvp {
+
+kvp_status decode_workspace_need(const kvp_pool* pool, const void* q, void* out, float* lse,
+                                 const int32_t* context_lens, const int32_t* block_tables, int32_t max_blocks,
+                                 int32_t B, int32_t num_q_heads, int32_t max_context_len, float softmax_scale,
+                                 int32_t num_splits, size_t* need) {
+    *need = 0;
+    DecodeParams p;
+    bool empty = false;
+    kvp_status st = decode_prepare(pool, nullptr, nullptr, q, out, lse, context_lens, block_tables, max_blocks, B,
+                                   num_q_heads, max_context_len, softmax_scale, num_splits, &p, &empty);
+    if (st != KVP_OK || empty) return st;
+    *need = kvp_workspace_size(1, B, num_q_heads, pool->head_dim, p.max_splits);
+    return KVP_OK;
+}
+
+}  // namespace kvp

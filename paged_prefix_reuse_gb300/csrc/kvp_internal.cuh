@@ -129,6 +129,13 @@ cudaError_t launch_merge(const float* ws_o, const float* ws_lse, int32_t rows, i
                          int32_t pages_per_split, int32_t parts_per_split, cudaStream_t stream);
 // Partials one decode split writes (one per consumer warp).
 int decode_parts_per_split();
+// Validates a decode call's arguments exactly as kvp_decode_attn does and
+// sets *need to the workspace bytes of the split count that call would
+// resolve (split geometry included; 0 for one split or an empty batch).
+kvp_status decode_workspace_need(const kvp_pool* pool, const void* q, void* out, float* lse,
+                                 const int32_t* context_lens, const int32_t* block_tables, int32_t max_blocks,
+                                 int32_t B, int32_t num_q_heads, int32_t max_context_len, float softmax_scale,
+                                 int32_t num_splits, size_t* need);
 
 // Swizzle chunk width (elements of one TMA box row) for a head dimension:
 // 64 elements (128-byte rows, 128B swizzle) when head_dim is a multiple of

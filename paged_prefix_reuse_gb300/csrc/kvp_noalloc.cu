@@ -54,14 +54,15 @@ extern "C" kvp_status kvp_decode_attn_noalloc(const kvp_pool* pool, const void* 
                                               int32_t max_blocks, int32_t B, int32_t num_q_heads,
                                               int32_t max_context_len, float softmax_scale, int32_t num_splits,
                                               void* stream) {
-    if (!pool || num_q_heads < 1 || B < 0 || num_splits < 0 || max_context_len < 0) return KVP_ERR_INVALID_ARG;
+    // Validate exactly as kvp_decode_attn does (so its error codes come
+    // first), then size the request by the split count that call resolves --
+    // the geometry rounds pages per split up to whole stages, so it may be
+    // smaller than num_splits -- and refuse it if its partials do not fit.
+    size_t need = 0;
+    kvp_status st = kvp::decode_workspace_need(pool, q, out, lse, context_lens, block_tables, max_blocks, B,
+                                               num_q_heads, max_context_len, softmax_scale, num_splits, &need);
+    if (st != KVP_OK) return st;
     if (B == 0) return KVP_OK;
-    // Resolve the split count exactly as kvp_decode_attn does and refuse a
-    // request whose partials would not fit in the fixed scratch array.
-    const int32_t req = num_splits > 0
-                            ? num_splits
-                            : kvp_decode_num_splits(B, pool->num_kv_heads, pool->block_size, max_context_len);
-    const size_t need = kvp_workspace_size(1, B, num_q_heads, pool->head_dim, req);
     if (need > kScratchBytes) return KVP_ERR_WORKSPACE;
     void* scratch = nullptr;
     if (need > 0) {
@@ -70,5 +71,6 @@ extern "C" kvp_status kvp_decode_attn_noalloc(const kvp_pool* pool, const void* 
         if (!scratch) return KVP_ERR_CUDA;
     }
     return kvp_decode_attn(pool, q, out, lse, context_lens, block_tables, max_blocks, B, num_q_heads,
-                           max_context_len, softmax_scale, req, scratch, need > 0 ? kScratchBytes : 0, stream);
+                           max_context_len, softmax_scale, num_splits, scratch, need > 0 ? kScratchBytes : 0,
+                           stream);
 }

@@ -250,4 +250,70 @@ def test_noalloc_decode_host_checks(lib):
     # 4096 sequences x 64 heads x 64 splits of fp32 partials: far beyond 32 MiB
     need = kvp.kvp_workspace_size(1, 4096, 64, 128, 64)
     assert need > kvp.DECODE_NOALLOC_SCRATCH_BYTES
-    assert call(ctypes.byref(pool), B=4096, Hq=64, max_ctx=65536, splits=64) == KVP_ERR_WORKSPACE
+    pool8 = _pool(head_dim=128, num_kv_heads=8)
+    assert call(ctypes.byref(pool8), B=4096, Hq=64, max_ctx=65536, splits=64) == KVP_ERR_WORKSPACE
+    # argument errors come first, with kvp_decode_attn's codes: a bad pool is
+    # an invalid argument, a group of 32 query heads is unsupported, whatever
+    # the size of the request
+    bad = _pool(head_dim=128, num_kv_heads=8, k_pool=0)
+    assert call(ctypes.byref(bad), B=4096, Hq=64, max_ctx=65536, splits=64) == KVP_ERR_INVALID_ARG
+    assert call(ctypes.byref(pool), B=4096, Hq=64, max_ctx=65536, splits=64) == KVP_ERR_UNSUPPORTED
+    # 64 splits requested over 100-key contexts resolve to 4 (whole 32-key
+    # stages per split): the size check passes.  Without a GPU the call then
+    # fails at the device lookup; with one it would launch on these fake
+    # pointers, so that half runs only here (the GPU test uses real buffers).
+    assert kvp.kvp_workspace_size(1, 64, 32, 128, 64) > kvp.DECODE_NOALLOC_SCRATCH_BYTES
+    import torch
+
+    if not torch.cuda.is_available():
+        assert call(ctypes.byref(pool8), B=64, Hq=32, max_ctx=100, splits=64) == 4  # KVP_ERR_CUDA
+
+
+def test_binding_rejects_wrong_dtype_and_layout():
+    """The C ABI sees only pointers, so the binding checks what it cannot --
+    element type, density, device and trailing shape -- before any call.  No
+    library call is reached (the tensors here live on the CPU)."""
+    import types
+
+    import torch
+
+    pool = types.SimpleNamespace(dtype=torch.bfloat16, head_dim=128, num_kv_heads=2, block_size=16, c=None)
+    i32 = lambda *s: torch.zeros(s, dtype=torch.int32)
+    q16 = torch.zeros((4, 8, 128), dtype=torch.float16)  # fp16 q against a bf16 pool
+    qbf = torch.zeros((4, 8, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="dtype"):
+        kvp.kvp_prefix_attn(pool, q16, i32(2), i32(1), i32(1, 4), 4, 8, 1.0)
+    with pytest.raises(ValueError, match="contiguous"):
+        kvp.kvp_prefix_attn(pool, qbf.transpose(0, 1), i32(2), i32(1), i32(1, 4), 4, 8, 1.0)
+    with pytest.raises(ValueError, match="trailing"):
+        kvp.kvp_prefix_attn(pool, torch.zeros((4, 8, 64), dtype=torch.bfloat16), i32(2), i32(1), i32(1, 4), 4, 8, 1.0)
+    with pytest.raises(ValueError, match="CUDA"):
+        kvp.kvp_prefix_attn(pool, qbf, i32(2), i32(1), i32(1, 4), 4, 8, 1.0)
+    with pytest.raises(ValueError, match="cu_seqlens_q has dtype"):
+        kvp.kvp_prefix_attn(pool, qbf, torch.zeros(2, dtype=torch.int64), i32(1), i32(1, 4), 4, 8, 1.0)
+    with pytest.raises(ValueError, match="dtype"):
+        kvp.kvp_decode_attn(pool, q16, i32(4), i32(4, 4), 8, 1.0)
+    with pytest.raises(ValueError, match="dtype"):
+        kvp.kvp_decode_attn_noalloc(pool, q16, i32(4), i32(4, 4), 8, 1.0)
+    with pytest.raises(ValueError, match="one row per sequence"):
+        kvp.kvp_decode_attn(pool, qbf, i32(3), i32(4, 4), 8, 1.0)
+    kv16 = torch.zeros((4, 2, 128), dtype=torch.float16)
+    kvbf = torch.zeros((4, 2, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="k_new has dtype"):
+        kvp.kvp_cache_append(pool, kv16, kvbf, torch.zeros(4, dtype=torch.int64))
+    with pytest.raises(ValueError, match="slot_mapping has dtype"):
+        kvp.kvp_cache_append(pool, kvbf, kvbf, i32(4))
+    with pytest.raises(ValueError, match="contiguous"):
+        kvp.kvp_cache_append(pool, kvbf.as_strided((4, 2, 128), (0, 128, 1)), kvbf, torch.zeros(4, dtype=torch.int64))
+    with pytest.raises(ValueError, match="one row per token"):
+        kvp.kvp_cache_append(pool, kvbf, kvbf[:3], torch.zeros(4, dtype=torch.int64))
+    with pytest.raises(ValueError, match="CUDA"):
+        kvp.kvp_cache_append(pool, kvbf, kvbf, torch.zeros(4, dtype=torch.int64))
+    with pytest.raises(ValueError, match="k_fresh has dtype"):
+        kvp.kvp_kv_deviation(pool, kv16, kvbf, torch.zeros(4, dtype=torch.int64))
+    with pytest.raises(ValueError, match="pairs has dtype"):
+        kvp.kvp_block_copy(pool, torch.zeros((1, 2), dtype=torch.int64))
+    with pytest.raises(ValueError, match="trailing"):
+        kvp.kvp_block_copy(pool, i32(1, 3))
+    with pytest.raises(ValueError, match="deviation has dtype"):
+        kvp.kvp_select_recompute(torch.zeros(4, dtype=torch.float64), torch.zeros(4, dtype=torch.int64), i32(2))
