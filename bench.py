@@ -3,9 +3,14 @@
 A step is the whole path over one batch: copy-on-write block copies, slot
 indexing, append of the new tokens' K/V, prefix attention of the prefill
 chunks and decode attention of the decode batch (whichever the workload has).
-The default workload is the shared-system-prompt batch (Qwen2.5-3B-shaped
-layer: Hq=16, Hkv=2, d=128, bf16; 8 requests sharing a 1024-token prefix,
-256 new tokens each, 8192-block pool).
+The default workload is the long-context prefix batch, the largest of the
+five shapes (Hq=64, Hkv=8, d=128, bf16; 4 requests, each a 32768-token
+cached prefix at random physical placement plus a 2048-token new chunk).
+Its step has no decode sequences, so the same run also times the decode
+batch of the multi-turn continuous-batching shape (Qwen2.5-32B-shaped
+layer: 64 sequences, cached contexts lognormal around 2048 tokens) and
+reports it in a ``decode`` object: tokens/s and HBM GB/s against the
+measured copy bandwidth.
 
 Prints ONE JSON line.  ``value`` is the algorithmic prefix-attention
 TFLOP/s of the whole step (4*d*Hq*sum(N*P + N(N+1)/2) per step, divided by
@@ -16,7 +21,7 @@ outputs device->host inside the timed region, the sequences in groups on
 their own streams so that copies overlap kernels (``step.HostStep``),
 replayed as one CUDA graph that includes the copies.
 
-    python bench.py [--steps K] [--warmup W] [--workload NAME] [--impl kvp|reference]
+    python bench.py [--steps K] [--warmup W] [--workload NAME] [--decode-workload NAME] [--impl kvp|reference]
     python bench.py --op block_swap|decode_q [--bits 8|4]|blockmgr|cacheblend
 
 With several GPUs (torchrun), every rank runs an independent replica (the
@@ -309,6 +314,52 @@ def run_reference(args):
     return 0
 
 
+def time_decode(st, stream, flush_l2, warmup, steps):
+    """Device time (ms) of the decode call of ``st`` (kvp_decode_attn plus the
+    split merge), replayed from a CUDA graph after an L2 flush, like the
+    per-kernel times of the step."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            st.run_decode()
+        times = []
+        for i in range(warmup + steps):
+            flush_l2()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            stream.synchronize()
+            if i >= warmup:
+                times.append(a.elapsed_time(b))
+    return float(np.mean(times))
+
+
+def decode_block(w, st, ms, peaks, peak_src, workload, launches, steps):
+    """The decode half of the metric: tokens/s of one decode call over the
+    batch and its K/V bytes per second against the measured HBM copy rate."""
+    hbm = _peak_value(peaks, "hbm_gbs", "hbm_GBps") or FALLBACK_PEAKS["hbm_gbs"]
+    byts = decode_kv_bytes(w)
+    gbs = byts / (ms * 1e-3) / 1e9
+    return {
+        "workload": workload,
+        "sequences": int(w.num_decode),
+        "tok_s": w.num_decode / (ms * 1e-3),
+        "ms": ms,
+        "kv_bytes": byts,
+        "achieved_gbs": gbs,
+        "peak_gbs": hbm,
+        "frac": gbs / hbm,
+        "peak_source": f"{peak_src} HBM copy",
+        "splits": int(st.decode_splits),
+        "gpu_launches": launches * steps,
+        "l2": "flushed before every timed call",
+        "traffic": committed_traffic("decode", workload),
+    }
+
+
 def run_kvp(args):
     import torch
 
@@ -427,6 +478,24 @@ def run_kvp(args):
                     times.append(a.elapsed_time(b))
             kern_ms[k] = float(np.mean(times))
         stream.synchronize()
+    # The decode half of the metric, when the step itself has no decode
+    # batch: the decode sequences of another workload, appended once, then
+    # their decode call timed alone.
+    dec_w = dec_st = None
+    dec_ms = 0.0
+    if not st.ndec and args.decode_workload != "none":
+        dec_w = wl.make_config(WORKLOADS[args.decode_workload], **WORKLOAD_ARGS.get(args.decode_workload, {}))
+        dec_st = DeviceStep(dec_w, device=dev, decode_splits=args.decode_splits)
+        if dec_st.ndec:
+            with torch.cuda.stream(stream):
+                dec_st.run_copy(stream)
+                dec_st.run_slots(stream)
+                dec_st.run_append(stream)
+            stream.synchronize()
+            dec_ms = time_decode(dec_st, stream, flush_l2, args.warmup, args.steps)
+        torch.cuda.synchronize()
+        if dec_st.pool.errors():
+            raise RuntimeError(f"decode workload: device error word {dec_st.pool.errors():#x}")
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms = max_over_ranks(float(np.mean(step_ms)), dev)
 
@@ -505,21 +574,19 @@ def run_kvp(args):
             "peak_source": f"{peak_src} bf16 dense (burst)" + (", fp16 taken equal to bf16" if w.dtype == "f16" else ""),
             "traffic": committed_traffic("prefix", args.workload),
         }
+    dec_launches = lambda s: 1 + (1 if s.decode_splits > 1 else 0)
     if st.ndec:
         hbm = _peak_value(peaks, "hbm_gbs", "hbm_GBps") or FALLBACK_PEAKS["hbm_gbs"]
         gbs = dec_bytes / (kern_ms["decode"] * 1e-3) / 1e9
-        line["decode"] = {
-            "tok_s": w.num_decode / (kern_ms["decode"] * 1e-3),
-            "achieved_gbs": gbs,
-            "peak_gbs": hbm,
-            "frac": gbs / hbm,
-            "peak_source": peak_src,
-            "traffic": committed_traffic("decode", args.workload),
-        }
+        line["decode"] = decode_block(w, st, kern_ms["decode"], peaks, peak_src, args.workload, dec_launches(st),
+                                      args.steps)
         if not st.npf:
             line["roofline"] = {"kernel": "decode_attn", "bound": "hbm", "achieved": gbs, "peak": hbm,
                                 "unit": "GB/s", "frac": gbs / hbm, "peak_source": peak_src,
                                 "traffic": committed_traffic("decode", args.workload)}
+    elif dec_st is not None and dec_st.ndec:
+        line["decode"] = decode_block(dec_w, dec_st, dec_ms, peaks, peak_src, args.decode_workload,
+                                      dec_launches(dec_st), args.steps)
     if not args.no_cpu_baseline and world >= 1:
         v, s, r, threads = cpu_oracle_sample(w, args.cpu_seconds)
         line["cpu_baseline"] = {
@@ -877,8 +944,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5, help="untimed warm-up steps (at least 3)")
     ap.add_argument("--impl", choices=["kvp", "reference"], default="kvp",
                     help="kvp: the CUDA library; reference: the fp64 oracle on the host cores")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="shared_system_prompt",
-                    help="synthetic batch shape (default: the shared system prompt)")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="long_context_prefix",
+                    help="synthetic batch shape (default: the long-context prefix batch, the largest)")
+    ap.add_argument("--decode-workload", choices=sorted(WORKLOADS) + ["none"], default="continuous_batching_step",
+                    help="when the workload has no decode sequences, time the decode batch of this one too "
+                         "(reported as the line's decode object; none: skip)")
     ap.add_argument("--prefix-splits", type=int, default=0, help="split-KV count of prefix attention (0: the library's)")
     ap.add_argument("--decode-splits", type=int, default=0, help="split-KV count of decode (0: the library's)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU time of the oracle baseline sample")

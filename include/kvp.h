@@ -57,7 +57,7 @@ typedef enum {
     KVP_ERR_UNSUPPORTED = 2, /* head_dim not 64/96/128, dtype, block_size not 8/16/32 */
     KVP_ERR_WORKSPACE = 3,   /* workspace missing or smaller than kvp_workspace_size() */
     KVP_ERR_CUDA = 4,        /* a CUDA runtime/driver call or launch failed */
-    KVP_ERR_TIMEOUT = 5,     /* reserved for host-side reporting of KVP_DEVERR_TIMEOUT */
+    KVP_ERR_TIMEOUT = 5,     /* kvp_pool_errors: a kernel's bounded wait gave up (KVP_DEVERR_TIMEOUT) */
     KVP_ERR_NO_BLOCKS = 6    /* block manager: too few free or evictable blocks (state unchanged) */
 } kvp_status;
 
@@ -215,8 +215,38 @@ kvp_status kvp_select_recompute(const float *deviation, const int64_t *slots, co
  * context_lens, block_tables or qpages.  (Within the library's own step --
  * copy, slot mapping, append, prefix attention, decode -- this holds.) */
 #define KVP_LAUNCH_PDL 0x1u
+/* KVP_LAUNCH_STALL_TEST exercises the failure path of the bounded waits
+ * without faulting anything: in every prefix-attention and decode CTA one
+ * warp first waits on a shared-memory barrier that nothing ever arrives on.
+ * That wait gives up when the pipeline wait limit (kvp_set_wait_limit_ns)
+ * runs out, sets KVP_DEVERR_TIMEOUT and an abort flag, and the CTA winds down
+ * the way it does after any wait that gave up: the other warps leave their
+ * waits, copies already in flight are waited for (with the default limit),
+ * tensor memory is freed, and the kernel returns.  Outputs are then
+ * unspecified; the context stays usable.  For tests only -- with the default
+ * 2 s limit each CTA would stall for 2 s. */
+#define KVP_LAUNCH_STALL_TEST 0x2u
 void kvp_set_launch_options(uint32_t flags);
 uint32_t kvp_get_launch_options(void);
+
+/* How long a kernel's pipeline waits (a warp waiting for a copy, a
+ * tensor-core result or another warp's data) last before they give up and
+ * report KVP_DEVERR_TIMEOUT; process-wide, read at each call; 0 restores the
+ * default of 2 s.  A healthy wait lasts microseconds, so the limit only
+ * decides how soon a stuck kernel is reported.  The waits of a CTA that is
+ * winding down (for its own copies in flight and its last tensor-core
+ * commit) always keep the default, so nothing lands in its memory after it
+ * exits. */
+void kvp_set_wait_limit_ns(uint64_t ns);
+uint64_t kvp_get_wait_limit_ns(void);
+
+/* Reads pool->err_word on the host after everything queued on `stream`
+ * before it: synchronises `stream`, stores the KVP_DEVERR_* bits in *bits
+ * and returns KVP_ERR_TIMEOUT when KVP_DEVERR_TIMEOUT is among them, else
+ * KVP_OK (data errors -- bad blocks, slots, pairs, lengths -- are reported in
+ * *bits only).  With err_word NULL, *bits = 0.  The word is not cleared.
+ * Errors: KVP_ERR_INVALID_ARG (pool or bits NULL), KVP_ERR_CUDA. */
+kvp_status kvp_pool_errors(const kvp_pool *pool, uint32_t *bits, void *stream);
 
 /* A pool of blocks in host memory with the same block geometry (num_kv_heads,
  * block_size, head_dim, dtype) as a device pool: the swap buffer of

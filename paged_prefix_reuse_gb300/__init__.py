@@ -55,7 +55,11 @@ __all__ = [
     "kvp_status_string",
     "kvp_set_launch_options",
     "kvp_get_launch_options",
+    "kvp_set_wait_limit_ns",
+    "kvp_get_wait_limit_ns",
+    "kvp_pool_errors",
     "LAUNCH_PDL",
+    "LAUNCH_STALL_TEST",
     "DEVERR",
 ]
 
@@ -66,6 +70,8 @@ KVP_F16, KVP_BF16 = 0, 1
 _DTYPES = {torch.float16: KVP_F16, torch.bfloat16: KVP_BF16}
 
 LAUNCH_PDL = 0x1  # KVP_LAUNCH_PDL in kvp.h
+LAUNCH_STALL_TEST = 0x2  # KVP_LAUNCH_STALL_TEST: exercises the timed-out-wait path (tests only)
+KVP_ERR_TIMEOUT = 5
 
 # Device error-word bits (KVP_DEVERR_* in kvp.h).
 DEVERR = {"bad_block": 0x1, "bad_slot": 0x2, "bad_pair": 0x4, "bad_len": 0x8, "timeout": 0x10, "qrange": 0x20}
@@ -89,6 +95,9 @@ EXPORTED_SYMBOLS = (
     "kvp_status_string",
     "kvp_set_launch_options",
     "kvp_get_launch_options",
+    "kvp_set_wait_limit_ns",
+    "kvp_get_wait_limit_ns",
+    "kvp_pool_errors",
     "kvp_version",
 )
 
@@ -221,6 +230,12 @@ def load_library():
         lib.kvp_set_launch_options.restype = None
         lib.kvp_get_launch_options.argtypes = []
         lib.kvp_get_launch_options.restype = ctypes.c_uint32
+        lib.kvp_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        lib.kvp_set_wait_limit_ns.restype = None
+        lib.kvp_get_wait_limit_ns.argtypes = []
+        lib.kvp_get_wait_limit_ns.restype = ctypes.c_uint64
+        lib.kvp_pool_errors.argtypes = [PP, ctypes.POINTER(ctypes.c_uint32), P]
+        lib.kvp_pool_errors.restype = ctypes.c_int
         lib.kvp_version.argtypes = []
         lib.kvp_version.restype = i32
         _lib = lib
@@ -247,6 +262,28 @@ def kvp_set_launch_options(flags: int) -> None:
 
 def kvp_get_launch_options() -> int:
     return int(load_library().kvp_get_launch_options())
+
+
+def kvp_set_wait_limit_ns(ns: int) -> None:
+    """Limit of the kernels' pipeline waits before they give up and report
+    ``DEVERR["timeout"]`` (0: the default, 2 s)."""
+    load_library().kvp_set_wait_limit_ns(int(ns))
+
+
+def kvp_get_wait_limit_ns() -> int:
+    return int(load_library().kvp_get_wait_limit_ns())
+
+
+def kvp_pool_errors(pool: "PagedKVPool", stream=None) -> int:
+    """The pool's error bits after the work queued on ``stream``; raises
+    ``KvpError`` (status KVP_ERR_TIMEOUT) when a kernel's wait gave up."""
+    bits = ctypes.c_uint32(0)
+    st = load_library().kvp_pool_errors(pool.c, ctypes.byref(bits), _stream(stream))
+    if st not in (0, KVP_ERR_TIMEOUT):
+        _check(st, "kvp_pool_errors")
+    if st == KVP_ERR_TIMEOUT:
+        raise KvpError(st, f"kvp_pool_errors (error bits {bits.value:#x})")
+    return int(bits.value)
 
 
 def _check(status: int, where: str) -> None:

@@ -12,6 +12,8 @@ namespace kvp {
 
 std::atomic<uint32_t> g_launch_flags{0};
 uint32_t launch_flags() { return g_launch_flags.load(std::memory_order_relaxed); }
+std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 namespace {
 
 constexpr int kNumSMs = 152;  // GB300; used only by the split heuristics
@@ -108,6 +110,24 @@ int32_t kvp_version(void) { return 100; }
 
 void kvp_set_launch_options(uint32_t flags) { kvp::g_launch_flags.store(flags, std::memory_order_relaxed); }
 uint32_t kvp_get_launch_options(void) { return kvp::g_launch_flags.load(std::memory_order_relaxed); }
+
+void kvp_set_wait_limit_ns(uint64_t ns) {
+    kvp::g_wait_limit_ns.store(ns == 0 ? kWaitLimitNs : ns, std::memory_order_relaxed);
+}
+uint64_t kvp_get_wait_limit_ns(void) { return kvp::g_wait_limit_ns.load(std::memory_order_relaxed); }
+
+kvp_status kvp_pool_errors(const kvp_pool* pool, uint32_t* bits, void* stream) {
+    if (!pool || !bits) return KVP_ERR_INVALID_ARG;
+    *bits = 0;
+    if (!pool->err_word) return KVP_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t host = 0;
+    if (cudaMemcpyAsync(&host, pool->err_word, sizeof(host), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return KVP_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KVP_ERR_CUDA;
+    *bits = host;
+    return (host & KVP_DEVERR_TIMEOUT) ? KVP_ERR_TIMEOUT : KVP_OK;
+}
 
 const char* kvp_status_string(kvp_status status) {
     switch (status) {
@@ -275,6 +295,8 @@ kvp_status kvp_prefix_attn(const kvp_pool* pool, const void* q, void* out, float
     p.group = g;
     p.q_tiles = static_cast<int32_t>(q_tiles);
     p.num_splits = splits;
+    p.wait_limit_ns = wait_limit_ns();
+    p.stall_test = (launch_flags() & KVP_LAUNCH_STALL_TEST) ? 1 : 0;
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
     p.ws_o = nullptr;
     p.ws_lse = nullptr;
@@ -380,6 +402,8 @@ static kvp_status decode_prepare(const kvp_pool* pool, const kvp_qpool* qpool, c
     p.ws_lse = nullptr;
     p.qpool = qpool ? qview_of(qpool) : QPoolView{nullptr, nullptr, nullptr, nullptr, 0, 0};
     p.qpages = qpool ? qpages : nullptr;
+    p.wait_limit_ns = wait_limit_ns();
+    p.stall_test = (launch_flags() & KVP_LAUNCH_STALL_TEST) ? 1 : 0;
     *pp = p;
     return KVP_OK;
 }

@@ -41,7 +41,7 @@ struct DecodeCfg {
     static constexpr int STG_BYTES = BITS ? STAGE_BYTES : 0;  // per consumer warp: dequantized K and V
     static constexpr int OFF_STG = RING_BYTES;
     static constexpr int OFF_BAR = RING_BYTES + kConsumerWarps * STG_BYTES;
-    static constexpr int SMEM_BYTES = OFF_BAR + 2 * NS * 8 + 16 + 1024;
+    static constexpr int SMEM_BYTES = OFF_BAR + (2 * NS + 1) * 8 + 16 + 1024;
 };
 
 // Two codes -> half2 (1024 + c0, 1024 + c1): exact, since fp16 has unit
@@ -205,7 +205,8 @@ __global__ void __launch_bounds__(kDecodeThreads, BITS ? 4 : 5)
     uint8_t* smem = align1024(smem_raw);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* empty = full + C::NS;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + C::NS);
+    uint64_t* stall = empty + C::NS;  // nothing arrives on it (KVP_LAUNCH_STALL_TEST)
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(stall + 1);
 
     const int sp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -241,6 +242,7 @@ __global__ void __launch_bounds__(kDecodeThreads, BITS ? 4 : 5)
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
         }
+        mbar_init(stall, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -260,9 +262,12 @@ __global__ void __launch_bounds__(kDecodeThreads, BITS ? 4 : 5)
             prefetch_tmap(&tmap_v);
         }
         pdl_wait();  // pool contents from the kernel before are read from here on
+        // Test of the failure path: before any copy is issued, wait on a
+        // barrier nothing arrives on until the limit runs out.
+        const bool stalled = p.stall_test && !stall_wait(stall, abort_flag, err, p.wait_limit_ns);
         int my_blk = 0;
         int issued = 0;
-        for (int i = 0; i < nstages; ++i) {
+        for (int i = 0; i < nstages && !stalled; ++i) {
             const int slot = i % C::NS;
             const int rel = (i * pps) & 31;
             if (rel == 0) {
@@ -276,7 +281,8 @@ __global__ void __launch_bounds__(kDecodeThreads, BITS ? 4 : 5)
                 my_blk = blk;
             }
             int ok = 1;
-            if (lane == 0 && i >= C::NS) ok = mbar_wait(&empty[slot], ((i / C::NS) - 1) & 1, abort_flag, err);
+            if (lane == 0 && i >= C::NS)
+                ok = mbar_wait(&empty[slot], ((i / C::NS) - 1) & 1, abort_flag, err, p.wait_limit_ns);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             const bool qst = BITS > 0 && page0 + i < qp;
@@ -343,7 +349,7 @@ __global__ void __launch_bounds__(kDecodeThreads, BITS ? 4 : 5)
 
         for (int i = warp; i < nstages; i += kConsumerWarps) {
             const int slot = i % C::NS;
-            if (!mbar_wait(&full[slot], (i / C::NS) & 1, abort_flag, err)) break;
+            if (!mbar_wait(&full[slot], (i / C::NS) & 1, abort_flag, err, p.wait_limit_ns)) break;
             uint8_t* kst = smem + slot * C::STAGE_BYTES;
             uint8_t* vst = kst + C::KBYTES;
             const int kbeg = key0 + i * kStageKeys;

@@ -27,7 +27,8 @@ struct PoolView {
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-uint32_t launch_flags();  // kvp_set_launch_options
+uint32_t launch_flags();      // kvp_set_launch_options
+uint64_t wait_limit_ns();     // kvp_set_wait_limit_ns (pipeline waits)
 
 // Launch with the programmatic-stream-serialization attribute when
 // KVP_LAUNCH_PDL is set, a plain launch otherwise.
@@ -73,6 +74,8 @@ struct PrefixParams {
     float scale_log2;  // softmax_scale * log2(e)
     float* ws_o;       // [total_q * Hq][num_splits][head_dim] fp32 (splits > 1)
     float* ws_lse;     // [total_q * Hq][num_splits] fp32, log2 domain
+    uint64_t wait_limit_ns;  // limit of the pipeline waits
+    int32_t stall_test;      // KVP_LAUNCH_STALL_TEST: wait on a barrier nothing arrives on
 };
 
 struct DecodeParams {
@@ -90,6 +93,8 @@ struct DecodeParams {
     float* ws_lse;  // [B * Hq][max_splits * parts], log2 domain
     QPoolView qpool;         // quantized prefix pages (bits 0: none)
     const int32_t* qpages;   // [B]: leading table entries that name qpool blocks
+    uint64_t wait_limit_ns;  // limit of the pipeline waits
+    int32_t stall_test;      // KVP_LAUNCH_STALL_TEST: wait on a barrier nothing arrives on
 };
 
 // Host-side launchers (defined in the kernel .cu files).
@@ -136,6 +141,10 @@ kvp_status decode_workspace_need(const kvp_pool* pool, const void* q, void* out,
                                  const int32_t* context_lens, const int32_t* block_tables, int32_t max_blocks,
                                  int32_t B, int32_t num_q_heads, int32_t max_context_len, float softmax_scale,
                                  int32_t num_splits, size_t* need);
+
+// Give up on any single wait after this long by default; a healthy wait
+// lasts microseconds.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 // Swizzle chunk width (elements of one TMA box row) for a head dimension:
 // 64 elements (128-byte rows, 128B swizzle) when head_dim is a multiple of
@@ -203,14 +212,14 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
     return ok != 0;
 }
 
-// Give up on any single wait after this long; a healthy wait lasts microseconds.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-
 // Bounded wait for the phase with the given parity.  Returns false when the
 // wait gave up (limit reached, or another thread of the CTA already gave up
-// and raised *abort); the caller must then wind down.
+// and raised *abort); the caller must then wind down.  Pipeline waits take
+// the call's limit (kvp_set_wait_limit_ns); the drain waits of a CTA that is
+// winding down -- copies in flight, the last tensor-core commit -- keep the
+// default, so that nothing can land in shared or tensor memory after exit.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint32_t* err_word) {
+                                          uint32_t* err_word, uint64_t limit_ns = kWaitLimitNs) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = global_timer_ns();
@@ -218,11 +227,40 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
         if (mbar_try_wait_sleep(a, parity)) return true;
         if ((it & 63u) == 0) {
             if (*abort) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 *abort = 1;
                 report(err_word, KVP_DEVERR_TIMEOUT);
                 return false;
             }
+        }
+    }
+}
+
+// KVP_LAUNCH_STALL_TEST: the calling threads wait on `bar`, which nothing
+// arrives on, until the pipeline limit runs out; the wait gives up, raises
+// *abort and reports KVP_DEVERR_TIMEOUT, and the CTA winds down along the
+// same paths as after any timed-out wait.  Returns false.
+__device__ __forceinline__ bool stall_wait(uint64_t* bar, volatile int* abort, uint32_t* err_word,
+                                           uint64_t limit_ns) {
+    // test_wait never suspends the thread, and the clock is read on every
+    // pass, so the give-up time is the limit itself.
+    const uint32_t a = smem_u32(bar);
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(a)
+            : "memory");
+        if (done) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            *abort = 1;
+            report(err_word, KVP_DEVERR_TIMEOUT);
+            return false;
         }
     }
 }

@@ -74,7 +74,7 @@ struct PrefixCfg {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = 2 * TILE_BYTES;
     static constexpr int OFF_BAR = OFF_RING + NSLOT * TILE_BYTES;
-    static constexpr int NBARS = 8 + 2 * NSLOT;
+    static constexpr int NBARS = 9 + 2 * NSLOT;
     static constexpr int SMEM_BYTES = OFF_BAR + NBARS * 8 + 16 + 1024;
     static constexpr uint32_t S_COL0 = 0, S_COL1 = 128;
     static constexpr uint32_t O_COL0 = 256, O_COL1 = 256 + D;
@@ -147,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* o_done = bars + 6;                 // [2] last PV_i complete (commit)
     uint64_t* slot_full = bars + 8;              // [NSLOT] ring slot loaded (TMA bytes)
     uint64_t* slot_empty = bars + 8 + C::NSLOT;  // [NSLOT] ring slot released (commit)
+    uint64_t* stall = bars + 8 + 2 * C::NSLOT;   // nothing arrives on it (KVP_LAUNCH_STALL_TEST)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -207,6 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&slot_full[i], 1);
             mbar_init(&slot_empty[i], 1);
         }
+        mbar_init(stall, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -274,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int jj = 0; jj < n_local; ++jj) {
                 const int j = j_begin + jj;
-                if (!mbar_wait(&s_full[wg], jj & 1, abort_flag, err)) { ok = false; break; }
+                if (!mbar_wait(&s_full[wg], jj & 1, abort_flag, err, p.wait_limit_ns)) { ok = false; break; }
                 tc_fence_after();
                 float x[kBN];
                 {
@@ -346,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 
             // ------------------------------ epilogue ------------------------------
-            if (ok) ok = mbar_wait(&o_done[wg], 0, abort_flag, err);
+            if (ok) ok = mbar_wait(&o_done[wg], 0, abort_flag, err, p.wait_limit_ns);
             if (ok) {
                 tc_fence_after();
                 const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -451,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int slot = gl % C::NSLOT;
                 int ok = 1;
                 if (lane == 0 && gl >= C::NSLOT)
-                    ok = mbar_wait(&slot_empty[slot], ((gl / C::NSLOT) - 1) & 1, abort_flag, err);
+                    ok = mbar_wait(&slot_empty[slot], ((gl / C::NSLOT) - 1) & 1, abort_flag, err, p.wait_limit_ns);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) {
                     stop = true;
@@ -485,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t last_par = 0;
         auto slot_addr = [&](int gl) -> uint32_t { return ring + (gl % C::NSLOT) * C::TILE_BYTES; };
         auto wait_slot = [&](int gl) -> bool {
-            return mbar_wait(&slot_full[gl % C::NSLOT], (gl / C::NSLOT) & 1, abort_flag, err);
+            return mbar_wait(&slot_full[gl % C::NSLOT], (gl / C::NSLOT) & 1, abort_flag, err, p.wait_limit_ns);
         };
         auto release = [&](int gl) {
             tc_commit(&slot_empty[gl % C::NSLOT]);
@@ -514,8 +516,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
 
-        bool ok = mbar_wait(&q_full[0], 0, abort_flag, err);
-        if (ok && has1) ok = mbar_wait(&q_full[1], 0, abort_flag, err);
+        // Test of the failure path: before anything is issued to the tensor
+        // core, wait on a barrier nothing arrives on until the limit runs out.
+        bool ok = p.stall_test ? stall_wait(stall, abort_flag, err, p.wait_limit_ns) : true;
+        if (ok) ok = mbar_wait(&q_full[0], 0, abort_flag, err, p.wait_limit_ns);
+        if (ok && has1) ok = mbar_wait(&q_full[1], 0, abort_flag, err, p.wait_limit_ns);
         if (ok) ok = wait_slot(0);
         if (ok) {
             tc_fence_after();
@@ -546,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
             }
             // ---- query tile 0: PV_0(jj), then S_0(jj+1)
-            if (!mbar_wait(&p_full[0], jj & 1, abort_flag, err)) { ok = false; break; }
+            if (!mbar_wait(&p_full[0], jj & 1, abort_flag, err, p.wait_limit_ns)) { ok = false; break; }
             tc_fence_after();
             issue_pv(0, slot_addr(gv), jj > 0);
             if (!more) tc_commit(&o_done[0]);
@@ -557,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // ---- query tile 1: PV_1(jj), then S_1(jj+1)
             if (has1) {
-                if (!mbar_wait(&p_full[1], jj & 1, abort_flag, err)) { ok = false; break; }
+                if (!mbar_wait(&p_full[1], jj & 1, abort_flag, err, p.wait_limit_ns)) { ok = false; break; }
                 tc_fence_after();
                 issue_pv(1, slot_addr(gv), jj > 0);
                 if (!more) tc_commit(&o_done[1]);

@@ -47,3 +47,11 @@ def test_decode_bytes_are_each_contexts_k_and_v_once():
     per_seq = [int(L) * w.num_kv_heads * w.head_dim * 2 * 2 for L in ctx]
     assert bench.decode_kv_bytes(w) == sum(per_seq)
     assert 600e6 < bench.decode_kv_bytes(w) < 700e6  # the mixed batch's ~643 MB
+
+
+def test_long_context_batch_flops_by_hand():
+    # 4 requests x 64 query heads x d 128, prefix 32768, 2048 new tokens each
+    w = wl.make_config(5)
+    by_hand = 4 * 128 * 64 * 4 * (2048 * 32768 + 2048 * 2049 // 2)
+    assert by_hand == 9_071_105_146_880
+    assert bench.prefill_flops(w) == by_hand

@@ -247,9 +247,19 @@ def _sample_rows(w, sub, n, rng):
     return np.unique(toks * w.num_q_heads + heads)
 
 
+_CONFIGS = {}
+
+
+def _config(cfg):
+    """Full-size workloads are generated once per module (seconds each)."""
+    if cfg not in _CONFIGS:
+        _CONFIGS[cfg] = wl.make_config(cfg)
+    return _CONFIGS[cfg]
+
+
 @pytest.mark.parametrize("cfg", [2, 3, 4, 5])
 def test_full_size_configs_sampled_rows(cfg):
-    w = wl.make_config(cfg)
+    w = _config(cfg)
     rng = np.random.default_rng(cfg)
     rows = _sample_rows(w, "prefill", 48, rng) if w.num_prefill else None
     drows = _sample_rows(w, "decode", 48, rng) if w.num_decode else None
@@ -270,6 +280,26 @@ def test_full_size_configs_sampled_rows(cfg):
     if drows is not None:
         _compare_attn(w.dtype, st.out_dec, st.lse_dec, ref["decode_out"], ref["decode_lse"], drows, f"cfg{cfg}-dec")
         assert torch.isfinite(st.out_dec.float()).all()
+
+
+@pytest.mark.parametrize("splits", [2, 4])
+def test_long_context_split_kv_at_full_size(splits):
+    """The long-context batch (4 x 32768 cached + 2048 new tokens) with its
+    key range split: each query tile's keys are cut into `splits` ranges of up
+    to 8 K keys, written as fp32 partials and merged by log-sum-exp.  (The
+    library itself picks one split here: 4 x 8 x 32 = 1024 CTAs already fill
+    the GPU.)  Sampled rows against the oracle, every row finite."""
+    w = _config(5)
+    rng = np.random.default_rng(100 + splits)
+    rows = _sample_rows(w, "prefill", 48, rng)
+    st = _step(w, prefix_splits=splits)
+    assert st.prefix_splits == splits
+    st.run()
+    torch.cuda.synchronize()
+    assert st.pool.errors() == 0
+    ref = oracle.run_step(w, rows=rows)
+    _compare_attn(w.dtype, st.out_pf, st.lse_pf, ref["prefill_out"], ref["prefill_lse"], rows, f"split{splits}")
+    assert torch.isfinite(st.out_pf.float()).all() and torch.isfinite(st.lse_pf).all()
 
 
 # --------------------------------------------------------------------------
