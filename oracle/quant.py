@@ -167,3 +167,58 @@ def decode_attn_q(dtype: str, qpool, bits: int, k_pool, v_pool, q, context_lens,
             out[b, h] = e @ V[h // g] / l
             lse[b, h] = m + np.log(l)
     return out, lse
+
+
+def prefix_attn_q(dtype: str, qpool, bits: int, k_pool, v_pool, q, cu_seqlens_q, context_lens, block_tables,
+                  qpages, scale, rows=None):
+    """Causal attention of each sequence's new tokens over its cached prefix
+    plus its own K/V (kvboost "How it works" step 5), where the cached prefix
+    is held in the quantized pool ("Optional: KV quantization"): the first
+    qpages[s] pages of sequence s are dequantized from ``qpool`` (code * s +
+    min, exactly), the rest read from the 16-bit pool.  New token i of
+    sequence s sits at position context_lens[s] - N_s + i and sees keys 0 ..
+    that position.  fp64 softmax.
+
+    q: bit patterns [T, Hq, d].  Returns (out, lse) for the flat rows
+    t * Hq + h given in ``rows`` (all rows when None): out [n, d], lse [n]
+    (natural log)."""
+    T, Hq, d = q.shape
+    nb16, Hkv, bs, _ = k_pool.shape
+    g = Hq // Hkv
+    cu = np.asarray(cu_seqlens_q, dtype=np.int64)
+    qf = decode_bits(q, dtype).astype(np.float64)
+    if rows is None:
+        rows = np.arange(T * Hq)
+    rows = np.asarray(rows, dtype=np.int64)
+    out = np.zeros((len(rows), d))
+    lse = np.zeros(len(rows))
+    seq_of = np.searchsorted(cu, rows // Hq, side="right") - 1
+    cache = {}
+    for n, r in enumerate(rows):
+        t, h = int(r // Hq), int(r % Hq)
+        s = int(seq_of[n])
+        if s not in cache:
+            L = int(context_lens[s])
+            npg = (L + bs - 1) // bs
+            qp = min(max(int(qpages[s]), 0), npg)
+            Ks, Vs = [], []
+            for p in range(npg):
+                blk = int(block_tables[s][p])
+                if p < qp:
+                    K, V = dequantize_block(qpool, bits, blk, d)
+                else:
+                    K = decode_bits(k_pool[blk], dtype).astype(np.float64)
+                    V = decode_bits(v_pool[blk], dtype).astype(np.float64)
+                Ks.append(K)
+                Vs.append(V)
+            cache = {s: (np.concatenate(Ks, axis=1)[:, :L], np.concatenate(Vs, axis=1)[:, :L], L)}
+        K, V, L = cache[s]
+        N = int(cu[s + 1] - cu[s])
+        pos = L - N + (t - int(cu[s]))
+        x = K[h // g, : pos + 1] @ qf[t, h] * scale
+        m = x.max()
+        e = np.exp(x - m)
+        l = e.sum()
+        out[n] = e @ V[h // g, : pos + 1] / l
+        lse[n] = m + np.log(l)
+    return out, lse

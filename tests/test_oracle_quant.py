@@ -162,3 +162,90 @@ def test_quantize_skips_out_of_range_pairs():
     qp2, bad = quant.quantize_blocks("f16", kb, kb, qp, 8, [[4, 0], [0, 2], [-1, 1], [1, 1]])
     assert bad == 3
     assert not qp2[0][0].any() and qp2[0][1].any()
+
+
+def _prefill_tables(rng, nb, bs, ctx, width):
+    bt = np.full((len(ctx), width), -1, dtype=np.int32)
+    perm = rng.permutation(nb)
+    k = 0
+    for b, L in enumerate(ctx):
+        n = (int(L) + bs - 1) // bs
+        bt[b, :n] = perm[k:k + n]
+        k += n
+    return bt
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quantized_prefill_is_exact_on_grid_inputs(bits):
+    """Prefix attention over a quantized cached prefix: on grid inputs
+    dequant(quant(x)) == x, so it must equal the 16-bit C prefix-attention
+    oracle (a different implementation) on the original pool for any split
+    of the pages between the two pools -- none, part of the prefix, the whole
+    prefix, and pages holding new tokens too (quantized after their append)."""
+    rng = np.random.default_rng(20 + bits)
+    nb, Hkv, bs, d, Hq = 40, 2, 16, 64, 6
+    kb, vb, K, V = _grid_pool(rng, nb, Hkv, bs, d, bits)
+    qp = quant.empty_qpool(nb, Hkv, bs, d, bits)
+    qp, bad = quant.quantize_blocks("bf16", kb, vb, qp, bits, np.stack([np.arange(nb)] * 2, 1))
+    assert bad == 0
+    new = np.array([37, 1, 20], dtype=np.int64)
+    ctx = np.array([150, 16, 260], dtype=np.int32)  # prefixes 113, 15, 240 tokens
+    cu = np.concatenate([[0], np.cumsum(new)]).astype(np.int32)
+    bt = _prefill_tables(rng, nb, bs, ctx, 20)
+    T = int(cu[-1])
+    q = wl.round_to_bits(rng.standard_normal((T, Hq, d)).astype(np.float32) * 0.2, "bf16")
+    want, want_lse, badr = oracle.prefix_attn("bf16", kb, vb, q, cu, ctx, bt, 0.125)
+    assert badr == 0
+    for qpages in ([0, 0, 0], [3, 0, 7], [7, 0, 15], [10, 1, 17]):
+        out, lse = quant.prefix_attn_q("bf16", qp, bits, kb, vb, q, cu, ctx, bt, np.array(qpages), 0.125)
+        np.testing.assert_allclose(out, want, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse, want_lse, rtol=0, atol=1e-12)
+
+
+def test_quantized_prefill_without_quantized_pages_is_16bit_attention():
+    """qpages = 0 everywhere: the quantized pool is never read (it holds only
+    zeros here), and random, off-grid inputs give the 16-bit C oracle's
+    answer; sampled rows equal the corresponding rows of the full answer."""
+    rng = np.random.default_rng(31)
+    nb, Hkv, bs, d, Hq = 30, 2, 16, 128, 8
+    kb = wl.round_to_bits(rng.standard_normal((nb, Hkv, bs, d)).astype(np.float32), "f16")
+    vb = wl.round_to_bits(rng.standard_normal((nb, Hkv, bs, d)).astype(np.float32), "f16")
+    new = np.array([5, 40], dtype=np.int64)
+    ctx = np.array([100, 200], dtype=np.int32)
+    cu = np.concatenate([[0], np.cumsum(new)]).astype(np.int32)
+    bt = _prefill_tables(rng, nb, bs, ctx, 16)
+    q = wl.round_to_bits(rng.standard_normal((45, Hq, d)).astype(np.float32), "f16")
+    qp = quant.empty_qpool(4, Hkv, bs, d, 8)
+    want, want_lse, _ = oracle.prefix_attn("f16", kb, vb, q, cu, ctx, bt, 0.088)
+    out, lse = quant.prefix_attn_q("f16", qp, 8, kb, vb, q, cu, ctx, bt, np.zeros(2, np.int32), 0.088)
+    np.testing.assert_allclose(out, want, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, want_lse, rtol=0, atol=1e-12)
+    rows = np.array([0, 7, 44 * Hq + 3, 20 * Hq + 5])
+    o2, l2 = quant.prefix_attn_q("f16", qp, 8, kb, vb, q, cu, ctx, bt, np.zeros(2, np.int32), 0.088, rows=rows)
+    np.testing.assert_array_equal(o2, out[rows])
+    np.testing.assert_array_equal(l2, lse[rows])
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quantized_prefill_of_one_token_is_quantized_decode(bits):
+    """With one new token per sequence, prefix attention over a partly
+    quantized context is decode attention over it (decode_attn_q, written
+    separately), on off-grid inputs where quantization changes the values."""
+    rng = np.random.default_rng(40 + bits)
+    nb, Hkv, bs, d, Hq = 30, 2, 16, 96, 4
+    kb = wl.round_to_bits(rng.standard_normal((nb, Hkv, bs, d)).astype(np.float32), "bf16")
+    vb = wl.round_to_bits(rng.standard_normal((nb, Hkv, bs, d)).astype(np.float32), "bf16")
+    qp = quant.empty_qpool(nb, Hkv, bs, d, bits)
+    qp, _ = quant.quantize_blocks("bf16", kb, vb, qp, bits, np.stack([np.arange(nb)] * 2, 1))
+    ctx = np.array([77, 16, 130], dtype=np.int32)
+    cu = np.arange(4, dtype=np.int32)
+    bt = _prefill_tables(rng, nb, bs, ctx, 10)
+    q = wl.round_to_bits(rng.standard_normal((3, Hq, d)).astype(np.float32) * 0.3, "bf16")
+    qpages = np.array([4, 1, 6], dtype=np.int32)
+    out, lse = quant.prefix_attn_q("bf16", qp, bits, kb, vb, q, cu, ctx, bt, qpages, 0.1)
+    want, want_lse = quant.decode_attn_q("bf16", qp, bits, kb, vb, q, ctx, bt, qpages, 0.1)
+    np.testing.assert_allclose(out, want.reshape(3 * Hq, d), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, want_lse.reshape(3 * Hq), rtol=0, atol=1e-12)
+    # and quantization did change the answer (the pages are off the grid)
+    plain, _, _ = oracle.prefix_attn("bf16", kb, vb, q, cu, ctx, bt, 0.1)
+    assert np.abs(out - plain).max() > 1e-4
