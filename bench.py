@@ -768,6 +768,109 @@ def run_decode_q(args):
     return 0
 
 
+def run_prefix_q(args):
+    """Prefix attention over a quantized cached prefix: the workload's
+    prefill chunks with every complete page of their cached prefixes moved to
+    an 8- or 4-bit pool (a block shared by several tables is quantized once),
+    timed against the 16-bit prefix attention of the same batch.  The FLOP
+    count is the prefill's (quantization changes where K/V come from, not the
+    work)."""
+    import numpy as np
+    import torch
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    from paged_prefix_reuse_gb300 import build as kvp_build
+
+    kvp_build.build_library()
+    import paged_prefix_reuse_gb300 as kvp
+    from paged_prefix_reuse_gb300.step import DeviceStep
+
+    kvp.load_library()
+    kvp.kvp_set_launch_options(kvp.LAUNCH_PDL if args.pdl else 0)
+    w = wl.make_config(WORKLOADS[args.workload], **WORKLOAD_ARGS.get(args.workload, {}))
+    st = DeviceStep(w, device=dev)
+    st.run_copy()
+    st.run_slots()
+    st.run_append()
+    torch.cuda.synchronize()
+    pool = st.pool
+    bs = pool.block_size
+    npf = st.npf
+    bt = st.bt[:npf].cpu().numpy().copy()
+    prefix = (w.context_lens[:npf] - w.new_lens[:npf]).astype(np.int64)
+    qpages = (prefix // bs).astype(np.int32)
+    qid = {}
+    for s_ in range(npf):
+        for pg in range(int(qpages[s_])):
+            src = int(bt[s_, pg])
+            if src not in qid:
+                qid[src] = len(qid)
+            bt[s_, pg] = qid[src]
+    pairs = np.array(list(qid.items()), dtype=np.int32).reshape(-1, 2)
+    qp = kvp.QuantKVPool.like(pool, max(1, len(qid)), args.bits)
+    for i in range(0, len(pairs), 65535):
+        kvp.kvp_quantize_blocks(pool, qp, torch.from_numpy(pairs[i:i + 65535]).to(dev))
+    torch.cuda.synchronize()
+    tq, tbt = torch.from_numpy(qpages).to(dev), torch.from_numpy(bt).to(dev)
+    q, cu, ctx = st.q[: st.tq], st.cu[: npf + 1], st.ctx[:npf]
+    out = torch.empty_like(q)
+    lse = torch.empty((w.num_q_heads, st.tq), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            ts = []
+            for i in range(args.warmup + args.steps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                e1.synchronize()
+                if i >= args.warmup:
+                    ts.append(e0.elapsed_time(e1) / 1e3)
+        return float(np.mean(ts))
+
+    t16 = timed(lambda: kvp.kvp_prefix_attn(pool, q, cu, ctx, st.bt[:npf], st.max_q_pf, st.max_ctx_pf, st.scale,
+                                            num_splits=st.prefix_splits, out=out, lse=lse, workspace=st.ws_pf,
+                                            stream=stream))
+    tqz = timed(lambda: kvp.kvp_prefix_attn_q(pool, qp, tq, q, cu, ctx, tbt, st.max_q_pf, st.max_ctx_pf, st.scale,
+                                              num_splits=st.prefix_splits, out=out, lse=lse, workspace=st.ws_pf,
+                                              stream=stream))
+    if pool.errors():
+        raise RuntimeError(f"device error word {pool.errors():#x}")
+    flops = prefill_flops(w)
+    peaks, peak_src = load_peaks()
+    peak = _peak_value(peaks, "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops"]
+    hkv, d = pool.num_kv_heads, pool.head_dim
+    page16 = hkv * bs * d * 2 * 2
+    pageq = hkv * (2 * bs * d * args.bits // 8 + 4 * d + 4 * bs)
+    line = {
+        "metric": f"prefix attention over an int{args.bits} cached prefix: TFLOP/s",
+        "value": flops / tqz / 1e12, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tqz * 1e3, "higher_is_better": True, "op": "prefix_q", "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": args.workload, "bits": args.bits, "quantized_pages": int(len(qid)),
+                   "cached_prefix_bytes_16bit": float(len(qid) * page16),
+                   "cached_prefix_bytes_quantized": float(len(qid) * pageq),
+                   "splits": int(st.prefix_splits), "l2": "flushed before every timed call",
+                   "launch": "CUDA graph replay of the one call"},
+        "prefix_16bit_ms": t16 * 1e3, "speed_vs_16bit": t16 / tqz,
+        "gpu_launches": 1 + (1 if st.prefix_splits > 1 else 0),
+        "roofline": {"kernel": "prefix_attn_q", "bound": "tensor", "achieved": flops / tqz / 1e12, "peak": peak,
+                     "unit": "TFLOP/s", "frac": flops / tqz / 1e12 / peak,
+                     "peak_source": f"{peak_src} bf16 dense (burst); the products run in fp16 (same nominal rate)",
+                     "traffic": committed_traffic(f"prefix_q_int{args.bits}", args.workload)},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_blockmgr(args):
     """Host block manager throughput through the public binding: chunk
     hashing (SHA-256 chain) and a request stream -- admit a prompt that shares
@@ -955,11 +1058,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the timed oracle sample")
     ap.add_argument("--preroll-s", type=float, default=0.4,
                     help="seconds of untimed steps before timing, so the clock samples see load")
-    ap.add_argument("--op", choices=["step", "block_swap", "decode_q", "blockmgr", "cacheblend"], default="step",
+    ap.add_argument("--op", choices=["step", "block_swap", "decode_q", "prefix_q", "blockmgr", "cacheblend"],
+                    default="step",
                     help="step: the prefill/decode step (default); block_swap: host <-> device page swap; "
-                         "decode_q: decode over a quantized cached prefix; blockmgr: host block manager; "
+                         "decode_q: decode over a quantized cached prefix; prefix_q: prefix attention over a "
+                         "quantized cached prefix (--workload's prefill); blockmgr: host block manager; "
                          "cacheblend: CacheBlend recompute selection")
-    ap.add_argument("--bits", type=int, choices=[8, 4], default=8, help="quantized pool width for --op decode_q")
+    ap.add_argument("--bits", type=int, choices=[8, 4], default=8,
+                    help="quantized pool width for --op decode_q and --op prefix_q")
     ap.add_argument("--e2e-groups", type=int, default=0,
                     help="sequence groups of the host-buffer (e2e) step, each on its own stream (0: auto)")
     ap.add_argument("--pdl", type=int, choices=[0, 1], default=1,
@@ -971,6 +1077,8 @@ def main():
         return run_swap(args)
     if args.op == "decode_q":
         return run_decode_q(args)
+    if args.op == "prefix_q":
+        return run_prefix_q(args)
     if args.op == "blockmgr":
         return run_blockmgr(args)
     if args.op == "cacheblend":

@@ -175,6 +175,27 @@ kvp_status kvp_decode_attn_q(const kvp_pool *pool, const kvp_qpool *qpool, const
                              float softmax_scale, int32_t num_splits, void *workspace, size_t workspace_bytes,
                              void *stream);
 
+/* Prefix attention over a context whose cached prefix is quantized
+ * (kvboost "Optional: KV quantization" with "How it works" step 5: the
+ * cached chunks are stored in 8 or 4 bits and the live suffix attends to
+ * them): as kvp_prefix_attn, except that for sequence s the first qpages[s]
+ * entries of its block table name blocks of qpool (dequantized inside the
+ * kernel, code * s + z, into the tiles the tensor cores read) and the
+ * remaining entries name blocks of the 16-bit pool (the live suffix, whose
+ * K/V kvp_cache_append wrote).  The tensor-core products of this call run in
+ * fp16 whatever the pool dtype (q and a bf16 pool's suffix pages are
+ * converted to fp16; accumulation, softmax, O and LSE in fp32, O written in
+ * the pool dtype), so K/V values must lie within fp16 range.
+ * qpages: device int32 [B], 0 <= qpages[s] <= pages of s (a larger value is
+ * clamped).  block_size must be 16 (else KVP_ERR_UNSUPPORTED).  Workspace,
+ * splits, outputs and errors as kvp_prefix_attn (kvp_workspace_size op 0);
+ * a table entry outside the pool it names sets KVP_DEVERR_BAD_BLOCK. */
+kvp_status kvp_prefix_attn_q(const kvp_pool *pool, const kvp_qpool *qpool, const int32_t *qpages, const void *q,
+                             void *out, float *lse, const int32_t *cu_seqlens_q, const int32_t *context_lens,
+                             const int32_t *block_tables, int32_t max_blocks, int32_t B, int32_t total_q,
+                             int32_t num_q_heads, int32_t max_q_len, int32_t max_context_len, float softmax_scale,
+                             int32_t num_splits, void *workspace, size_t workspace_bytes, void *stream);
+
 /* CacheBlend recompute selection (kvboost "How it works" > "4. Seam
  * repair": the cacheblend strategy measures per-token cosine deviation
  * between the cached K/V and the K/V with full context in one forward pass

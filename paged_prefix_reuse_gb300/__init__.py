@@ -12,6 +12,7 @@ Functions carry the names of the C entry points declared in
 ``kvp_block_copy``, ``kvp_block_swap``, ``kvp_quantize_blocks``,
 ``kvp_kv_deviation``, ``kvp_select_recompute``, ``kvp_prefix_attn``,
 ``kvp_decode_attn``, ``kvp_decode_attn_noalloc``, ``kvp_decode_attn_q``,
+``kvp_prefix_attn_q``, ``kvp_pool_errors``, ``kvp_set_wait_limit_ns``,
 ``kvp_workspace_size``, the split-count helpers and
 ``kvp_set_launch_options``.  ``BlockManager`` and ``kvp_hash_chunks`` wrap
 the host block manager of ``include/kvp_blockmgr.h``.  ``step`` runs a
@@ -48,6 +49,7 @@ __all__ = [
     "kvp_prefix_attn",
     "kvp_decode_attn",
     "kvp_decode_attn_q",
+    "kvp_prefix_attn_q",
     "kvp_decode_attn_noalloc",
     "kvp_workspace_size",
     "kvp_prefix_num_splits",
@@ -88,6 +90,7 @@ EXPORTED_SYMBOLS = (
     "kvp_prefix_attn",
     "kvp_decode_attn",
     "kvp_decode_attn_q",
+    "kvp_prefix_attn_q",
     "kvp_decode_attn_noalloc",
     "kvp_prefix_num_splits",
     "kvp_decode_num_splits",
@@ -189,6 +192,8 @@ def load_library():
         QP = ctypes.POINTER(_QPool)
         lib.kvp_quantize_blocks.argtypes = [PP, QP, P, i32, P]
         lib.kvp_decode_attn_q.argtypes = [PP, QP, P, P, P, P, P, P, i32, i32, i32, i32, f32, i32, P, sz, P]
+        lib.kvp_prefix_attn_q.argtypes = [PP, QP, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, i32, P, sz,
+                                          P]
         lib.kvp_prefix_attn.argtypes = [PP, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, i32, P, sz, P]
         lib.kvp_decode_attn.argtypes = [PP, P, P, P, P, P, i32, i32, i32, i32, f32, i32, P, sz, P]
         lib.kvp_decode_attn_noalloc.argtypes = [PP, P, P, P, P, P, i32, i32, i32, i32, f32, i32, P]
@@ -215,7 +220,7 @@ def load_library():
             getattr(lib, name).restype = ctypes.c_int
         for name in ("kvp_slot_mapping", "kvp_cache_append", "kvp_block_copy", "kvp_block_swap",
                      "kvp_quantize_blocks", "kvp_kv_deviation", "kvp_select_recompute", "kvp_prefix_attn",
-                     "kvp_decode_attn", "kvp_decode_attn_q",
+                     "kvp_decode_attn", "kvp_decode_attn_q", "kvp_prefix_attn_q",
                      "kvp_decode_attn_noalloc"):
             getattr(lib, name).restype = ctypes.c_int
         lib.kvp_prefix_num_splits.argtypes = [i32, i32, i32, i32, i32, i32]
@@ -495,6 +500,44 @@ def kvp_decode_attn_q(pool: PagedKVPool, qpool: QuantKVPool, qpages: torch.Tenso
                                  _ptr(block_tables), int(block_tables.shape[1]), B, Hq, int(max_context_len),
                                  float(softmax_scale), int(splits), _ptr(workspace), ws_bytes, _stream(stream)),
            "kvp_decode_attn_q")
+    return out, lse
+
+
+def kvp_prefix_attn_q(pool: PagedKVPool, qpool: QuantKVPool, qpages: torch.Tensor, q: torch.Tensor,
+                      cu_seqlens_q: torch.Tensor, context_lens: torch.Tensor, block_tables: torch.Tensor,
+                      max_q_len: int, max_context_len: int, softmax_scale: float, num_splits: int = 0,
+                      out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None, want_lse: bool = True, stream=None):
+    """Prefix attention where the first ``qpages[s]`` table entries of each
+    sequence name blocks of the quantized pool (the cached prefix) and the
+    rest blocks of the 16-bit pool.  Returns (out [T, Hq, d], lse [Hq, T]
+    float32 or None)."""
+    _arg(q, "q", pool.dtype, 3, (pool.head_dim,))
+    _arg(qpages, "qpages", torch.int32, 1)
+    _arg(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _arg(context_lens, "context_lens", torch.int32, 1)
+    _arg(block_tables, "block_tables", torch.int32, 2)
+    _arg(out, "out", pool.dtype, 3, tuple(q.shape), optional=True)
+    _arg(lse, "lse", torch.float32, 2, (q.shape[1], q.shape[0]), optional=True)
+    _on_device(q=q, qpages=qpages, cu_seqlens_q=cu_seqlens_q, context_lens=context_lens, block_tables=block_tables,
+               out=out, lse=lse)
+    lib = load_library()
+    T, Hq, d = (int(x) for x in q.shape)
+    B = int(context_lens.shape[0])
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
+    splits = num_splits or kvp_prefix_num_splits(B, Hq, pool.num_kv_heads, d, max_q_len, max_context_len)
+    need = kvp_workspace_size(0, T, Hq, d, splits)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.kvp_prefix_attn_q(pool.c, qpool.c, _ptr(qpages), _ptr(q), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q),
+                                 _ptr(context_lens), _ptr(block_tables), int(block_tables.shape[1]), B, T, Hq,
+                                 int(max_q_len), int(max_context_len), float(softmax_scale), int(splits),
+                                 _ptr(workspace), ws_bytes, _stream(stream)),
+           "kvp_prefix_attn_q")
     return out, lse
 
 

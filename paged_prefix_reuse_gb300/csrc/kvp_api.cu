@@ -257,17 +257,26 @@ kvp_status kvp_select_recompute(const float* deviation, const int64_t* slots, co
                                              static_cast<cudaStream_t>(stream)));
 }
 
-kvp_status kvp_prefix_attn(const kvp_pool* pool, const void* q, void* out, float* lse, const int32_t* cu_seqlens_q,
-                           const int32_t* context_lens, const int32_t* block_tables, int32_t max_blocks, int32_t B,
-                           int32_t total_q, int32_t num_q_heads, int32_t max_q_len, int32_t max_context_len,
-                           float softmax_scale, int32_t num_splits, void* workspace, size_t workspace_bytes,
-                           void* stream) {
+static kvp_status check_qpool(const kvp_pool* pool, const kvp_qpool* qp);
+static QPoolView qview_of(const kvp_qpool* qp);
+
+// Prefix attention, with (qpool != nullptr) or without a quantized prefix.
+static kvp_status prefix_common(const kvp_pool* pool, const kvp_qpool* qpool, const int32_t* qpages, const void* q,
+                                void* out, float* lse, const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                                const int32_t* block_tables, int32_t max_blocks, int32_t B, int32_t total_q,
+                                int32_t num_q_heads, int32_t max_q_len, int32_t max_context_len, float softmax_scale,
+                                int32_t num_splits, void* workspace, size_t workspace_bytes, void* stream) {
     kvp_status st = check_pool(pool);
     if (st != KVP_OK) return st;
+    if (qpool) {
+        if ((st = check_qpool(pool, qpool)) != KVP_OK) return st;
+        if (pool->block_size != 16) return KVP_ERR_UNSUPPORTED;
+    }
     if (B < 0 || total_q < 0 || max_blocks < 0 || num_splits < 0 || max_q_len < 0 || max_context_len < 0)
         return KVP_ERR_INVALID_ARG;
     if (B == 0 || total_q == 0) return KVP_OK;
     if (!q || !out || !cu_seqlens_q || !context_lens || !block_tables || max_blocks == 0) return KVP_ERR_INVALID_ARG;
+    if (qpool && !qpages) return KVP_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(out)) return KVP_ERR_INVALID_ARG;
     if (num_q_heads < 1 || num_q_heads % pool->num_kv_heads != 0) return KVP_ERR_INVALID_ARG;
     if (max_q_len < 1 || max_context_len < 1) return KVP_ERR_INVALID_ARG;
@@ -297,6 +306,8 @@ kvp_status kvp_prefix_attn(const kvp_pool* pool, const void* q, void* out, float
     p.num_splits = splits;
     p.wait_limit_ns = wait_limit_ns();
     p.stall_test = (launch_flags() & KVP_LAUNCH_STALL_TEST) ? 1 : 0;
+    p.qpool = qpool ? qview_of(qpool) : QPoolView{nullptr, nullptr, nullptr, nullptr, 0, 0};
+    p.qpages = qpool ? qpages : nullptr;
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
     p.ws_o = nullptr;
     p.ws_lse = nullptr;
@@ -312,12 +323,33 @@ kvp_status kvp_prefix_attn(const kvp_pool* pool, const void* q, void* out, float
     if ((st = make_pool_map(&tk, pool->k_pool, pool, pcw)) != KVP_OK) return st;
     if ((st = make_pool_map(&tv, pool->v_pool, pool, pcw)) != KVP_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_prefix_attn(p, tk, tv, s);
+    cudaError_t e = qpool ? launch_prefix_attn_q(p, tk, tv, s) : launch_prefix_attn(p, tk, tv, s);
     if (e != cudaSuccess) return KVP_ERR_CUDA;
     if (splits > 1)
         e = launch_merge(p.ws_o, p.ws_lse, total_q * num_q_heads, num_q_heads, pool->head_dim, splits, pool->dtype,
                          out, lse, total_q, nullptr, pool->block_size, 0, 1, s);
     return from_cuda(e);
+}
+
+kvp_status kvp_prefix_attn(const kvp_pool* pool, const void* q, void* out, float* lse, const int32_t* cu_seqlens_q,
+                           const int32_t* context_lens, const int32_t* block_tables, int32_t max_blocks, int32_t B,
+                           int32_t total_q, int32_t num_q_heads, int32_t max_q_len, int32_t max_context_len,
+                           float softmax_scale, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+    return prefix_common(pool, nullptr, nullptr, q, out, lse, cu_seqlens_q, context_lens, block_tables, max_blocks, B,
+                         total_q, num_q_heads, max_q_len, max_context_len, softmax_scale, num_splits, workspace,
+                         workspace_bytes, stream);
+}
+
+kvp_status kvp_prefix_attn_q(const kvp_pool* pool, const kvp_qpool* qpool, const int32_t* qpages, const void* q,
+                             void* out, float* lse, const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                             const int32_t* block_tables, int32_t max_blocks, int32_t B, int32_t total_q,
+                             int32_t num_q_heads, int32_t max_q_len, int32_t max_context_len, float softmax_scale,
+                             int32_t num_splits, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!qpool) return KVP_ERR_INVALID_ARG;
+    return prefix_common(pool, qpool, qpages, q, out, lse, cu_seqlens_q, context_lens, block_tables, max_blocks, B,
+                         total_q, num_q_heads, max_q_len, max_context_len, softmax_scale, num_splits, workspace,
+                         workspace_bytes, stream);
 }
 
 static kvp_status check_qpool(const kvp_pool* pool, const kvp_qpool* qp) {

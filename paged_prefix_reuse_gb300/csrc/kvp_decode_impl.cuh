@@ -44,45 +44,6 @@ struct DecodeCfg {
     static constexpr int SMEM_BYTES = OFF_BAR + (2 * NS + 1) * 8 + 16 + 1024;
 };
 
-// Two codes -> half2 (1024 + c0, 1024 + c1): exact, since fp16 has unit
-// spacing on [1024, 2048).  The codes sit in bytes i and j of w; every byte
-// of the constant source is 0x64, the high byte of 1024.0 in fp16.
-__device__ __forceinline__ uint32_t magic_pair(uint32_t w, uint32_t sel) {
-    return __byte_perm(w, 0x64646464u, sel);
-}
-
-// Dequantize one 8-channel unit: codes -> fp16 (1024 + c) - 1024, then
-// c * s + z in one fp16 fused multiply-add per pair (a single rounding).
-// 8 bits: 8 code bytes; 4 bits: 8 nibbles, the even channel in the low one.
-template <int BITS>
-__device__ __forceinline__ uint4 dequant_unit(const uint8_t* codes, const uint32_t (&s2)[4], const uint32_t (&z2)[4]) {
-    uint32_t h[4];
-    if constexpr (BITS == 8) {
-        const uint2 w = *reinterpret_cast<const uint2*>(codes);
-        h[0] = magic_pair(w.x, 0x4140);
-        h[1] = magic_pair(w.x, 0x4342);
-        h[2] = magic_pair(w.y, 0x4140);
-        h[3] = magic_pair(w.y, 0x4342);
-    } else {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(codes);
-        const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;  // even / odd channels
-        const uint32_t t = __byte_perm(lo, hi, 0x5140), u = __byte_perm(lo, hi, 0x7362);  // c0..c3, c4..c7
-        h[0] = magic_pair(t, 0x4140);
-        h[1] = magic_pair(t, 0x4342);
-        h[2] = magic_pair(u, 0x4140);
-        h[3] = magic_pair(u, 0x4342);
-    }
-    const __half2 k1024 = __float2half2_rn(1024.f);
-    uint32_t o[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const __half2 c = __hsub2(*reinterpret_cast<const __half2*>(&h[j]), k1024);
-        const __half2 x = __hfma2(c, *reinterpret_cast<const __half2*>(&s2[j]), *reinterpret_cast<const __half2*>(&z2[j]));
-        o[j] = *reinterpret_cast<const uint32_t*>(&x);
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
 // Dequantize one quantized stage (SK keys of one kv head) into the warp's
 // fp16 K and V tiles, in the chunked, swizzled layout the TMA path gives.
 // K scale/min are per channel (a lane's channels are fixed across its keys

@@ -76,6 +76,8 @@ struct PrefixParams {
     float* ws_lse;     // [total_q * Hq][num_splits] fp32, log2 domain
     uint64_t wait_limit_ns;  // limit of the pipeline waits
     int32_t stall_test;      // KVP_LAUNCH_STALL_TEST: wait on a barrier nothing arrives on
+    QPoolView qpool;         // quantized prefix pages (bits 0: none)
+    const int32_t* qpages;   // [B]: leading table entries that name qpool blocks
 };
 
 struct DecodeParams {
@@ -118,6 +120,9 @@ cudaError_t launch_block_swap(const PoolView& pool, void* k_pool, void* v_pool, 
                               cudaStream_t stream);
 cudaError_t launch_prefix_attn(const PrefixParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                cudaStream_t stream);
+// The same over a partly quantized context (p.qpool, p.qpages; block_size 16).
+cudaError_t launch_prefix_attn_q(const PrefixParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                                 cudaStream_t stream);
 // Query rows (token, head-of-group pairs) one prefix CTA covers.
 int prefix_rows_per_cta();
 // Columns of one TMA box of the prefix kernel's K/V tiles (64 at head_dim 96:
@@ -454,6 +459,46 @@ __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// ---- dequantization of 8/4-bit codes (the quantized pool) ----
+// Two codes -> half2 (1024 + c0, 1024 + c1): exact, since fp16 has unit
+// spacing on [1024, 2048).  The codes sit in bytes i and j of w; every byte
+// of the constant source is 0x64, the high byte of 1024.0 in fp16.
+__device__ __forceinline__ uint32_t magic_pair(uint32_t w, uint32_t sel) {
+    return __byte_perm(w, 0x64646464u, sel);
+}
+
+// Dequantize one 8-channel unit: codes -> fp16 (1024 + c) - 1024, then
+// c * s + z in one fp16 fused multiply-add per pair (a single rounding).
+// 8 bits: 8 code bytes; 4 bits: 8 nibbles, the even channel in the low one.
+template <int BITS>
+__device__ __forceinline__ uint4 dequant_unit(const uint8_t* codes, const uint32_t (&s2)[4], const uint32_t (&z2)[4]) {
+    uint32_t h[4];
+    if constexpr (BITS == 8) {
+        const uint2 w = *reinterpret_cast<const uint2*>(codes);
+        h[0] = magic_pair(w.x, 0x4140);
+        h[1] = magic_pair(w.x, 0x4342);
+        h[2] = magic_pair(w.y, 0x4140);
+        h[3] = magic_pair(w.y, 0x4342);
+    } else {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(codes);
+        const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;  // even / odd channels
+        const uint32_t t = __byte_perm(lo, hi, 0x5140), u = __byte_perm(lo, hi, 0x7362);  // c0..c3, c4..c7
+        h[0] = magic_pair(t, 0x4140);
+        h[1] = magic_pair(t, 0x4342);
+        h[2] = magic_pair(u, 0x4140);
+        h[3] = magic_pair(u, 0x4342);
+    }
+    const __half2 k1024 = __float2half2_rn(1024.f);
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const __half2 c = __hsub2(*reinterpret_cast<const __half2*>(&h[j]), k1024);
+        const __half2 x = __hfma2(c, *reinterpret_cast<const __half2*>(&s2[j]), *reinterpret_cast<const __half2*>(&z2[j]));
+        o[j] = *reinterpret_cast<const uint32_t*>(&x);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 template <bool kBF16>

@@ -196,6 +196,18 @@ def test_quantized_pool_validation(lib):
     assert lib.kvp_decode_attn_q(ctypes.byref(pool32), ctypes.byref(q32), 0x60000, 0x30000, 0x40000, None, 0x50000,
                                  0x70000, 8, 2, hkv * 2, 100, 0.1, 1, None, 0, None) == KVP_ERR_UNSUPPORTED
 
+    def pq(qpool, qpages=0x60000, B=1, P_=P, splits=1, ws=None, ws_bytes=0):
+        return lib.kvp_prefix_attn_q(P_, qpool, qpages, 0x30000, 0x40000, None, 0x50000, 0x60000, 0x70000, 8, B,
+                                     16, hkv * 2, 16, 100, 0.1, splits, ws, ws_bytes, None)
+
+    assert pq(ctypes.byref(good), B=0) == KVP_OK
+    assert pq(None) == KVP_ERR_INVALID_ARG
+    assert pq(ctypes.byref(good), qpages=None) == KVP_ERR_INVALID_ARG
+    assert pq(ctypes.byref(qp(bits=3))) == KVP_ERR_UNSUPPORTED
+    assert pq(ctypes.byref(qp(num_kv_heads=hkv + 1))) == KVP_ERR_INVALID_ARG
+    assert pq(ctypes.byref(q32), P_=ctypes.byref(pool32)) == KVP_ERR_UNSUPPORTED
+    assert pq(ctypes.byref(good), splits=3) == KVP_ERR_WORKSPACE
+
 
 def test_cacheblend_validation(lib):
     pool = _pool()

@@ -203,3 +203,120 @@ def test_quantized_range_overflow_is_flagged():
     kvp.kvp_quantize_blocks(pool, qp, torch.tensor([[0, 1]], dtype=torch.int32, device="cuda"))
     torch.cuda.synchronize()
     assert pool.errors() & 0x20
+
+
+# --------------------------------------------------------------------------
+# prefix attention over a quantized cached prefix (kvp_prefix_attn_q)
+# --------------------------------------------------------------------------
+def _prefill_q_case(w, bits, qfrac, into_new=False, seed=0):
+    """Append the new tokens' K/V (16-bit pool), then move the first pages of
+    every sequence to a quantized pool (scattered block ids; a block shared by
+    several tables is quantized once).  qfrac[s] of the full cached pages
+    (or, with into_new, of all pages: pages holding new tokens too)."""
+    import paged_prefix_reuse_gb300 as kvp
+    from paged_prefix_reuse_gb300.step import DeviceStep
+
+    st = DeviceStep(w)
+    st.run_slots()
+    st.run_append()
+    torch.cuda.synchronize()
+    kb, vb = _bits(st.pool.k), _bits(st.pool.v)
+    bs = w.block_size
+    bt = st.bt.cpu().numpy().copy()
+    ctx = st.ctx.cpu().numpy()
+    new = np.diff(st.cu.cpu().numpy())
+    qpages, qid = [], {}
+    for s in range(w.B):
+        full = (int(ctx[s]) + bs - 1) // bs if into_new else (int(ctx[s]) - int(new[s])) // bs
+        k = int(round(qfrac[s % len(qfrac)] * full))
+        qpages.append(k)
+        for p in range(k):
+            src = int(bt[s, p])
+            if src not in qid:
+                qid[src] = len(qid)
+            bt[s, p] = qid[src]
+    nq = max(1, len(qid))
+    perm = np.random.default_rng(seed).permutation(nq)
+    for s, k in enumerate(qpages):
+        bt[s, :k] = perm[bt[s, :k]]
+    pairs = np.array([(src, perm[i]) for src, i in qid.items()], dtype=np.int32).reshape(-1, 2)
+    qp = kvp.QuantKVPool.like(st.pool, nq, bits)
+    if len(pairs):
+        kvp.kvp_quantize_blocks(st.pool, qp, torch.from_numpy(pairs).cuda())
+    torch.cuda.synchronize()
+    assert st.pool.errors() == 0
+    oq, _ = quant.quantize_blocks(w.dtype, kb, vb, _qarrays(qp), bits, pairs)
+    return st, qp, oq, bt, np.array(qpages, dtype=np.int32), kb, vb
+
+
+def _run_prefill_q(st, qp, bt, qpages, w, splits=0):
+    import paged_prefix_reuse_gb300 as kvp
+
+    out, lse = kvp.kvp_prefix_attn_q(st.pool, qp, torch.from_numpy(qpages).cuda(), st.q[: st.tq],
+                                     st.cu[: st.npf + 1], st.ctx[: st.npf], torch.from_numpy(bt[: st.npf]).cuda(),
+                                     st.max_q_pf, st.max_ctx_pf, w.softmax_scale, num_splits=splits)
+    torch.cuda.synchronize()
+    assert st.pool.errors() == 0
+    return out, lse
+
+
+PREFILL_Q = [
+    # dtype, d, bits, splits, Hq, Hkv, qfrac, into_new
+    ("bf16", 128, 8, 1, 8, 2, [1.0, 0.5, 0.0], False),
+    ("bf16", 128, 4, 2, 8, 2, [1.0, 0.7, 1.0], True),
+    ("f16", 96, 8, 1, 4, 4, [1.0, 1.0, 0.3], False),
+    ("f16", 64, 4, 0, 6, 3, [0.6, 1.0, 1.0], True),
+    ("bf16", 96, 4, 3, 5, 1, [1.0, 0.0, 1.0], False),
+    ("f16", 128, 8, 1, 16, 1, [1.0, 1.0, 1.0], False),
+]
+
+
+@pytest.mark.parametrize("dtype,d,bits,splits,Hq,Hkv,qfrac,into_new", PREFILL_Q)
+def test_quantized_prefill_matches_oracle(dtype, d, bits, splits, Hq, Hkv, qfrac, into_new):
+    """Ragged new-token counts (one chunk of 1 token, one crossing several
+    query tiles), prefixes not a multiple of the block, a tile boundary inside
+    the quantized range, splits over the key range."""
+    w = wl.make_random(200 + d + bits + splits, [300, 77, 650], [131, 1, 40], Hq=Hq, Hkv=Hkv, d=d, dtype=dtype)
+    st, qp, oq, bt, qpages, kb, vb = _prefill_q_case(w, bits, qfrac, into_new, seed=d)
+    out, lse = _run_prefill_q(st, qp, bt, qpages, w, splits)
+    want, want_lse = quant.prefix_attn_q(dtype, oq, bits, kb, vb, w.q, w.cu_seqlens_q, w.context_lens, bt, qpages,
+                                         w.softmax_scale)
+    o = out.float().cpu().numpy().astype(np.float64).reshape(want.shape)
+    l = lse.cpu().numpy().astype(np.float64).T.reshape(-1)
+    assert np.isfinite(o).all()
+    assert np.abs(o - want).max() <= TOL[dtype], np.abs(o - want).max()
+    assert np.abs(l - want_lse).max() <= LSE_TOL, np.abs(l - want_lse).max()
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quantized_prefill_rag_chunks_at_full_size(bits):
+    """The RAG chunk-reuse batch at full size (16 requests x 8 shared 256-token
+    chunks, 32 kv heads, d = 96, fp16) with every cached chunk page stored
+    quantized: sampled rows against the oracle, every output finite."""
+    w = wl.make_config(3)
+    st, qp, oq, bt, qpages, kb, vb = _prefill_q_case(w, bits, [1.0], seed=bits)
+    assert (qpages == w.prefix_lens // 16).all()
+    out, lse = _run_prefill_q(st, qp, bt, qpages, w)
+    rng = np.random.default_rng(bits)
+    T = int(w.cu_seqlens_q[-1])
+    rows = np.unique(np.concatenate([rng.integers(0, T * w.num_q_heads, 40), [0, T * w.num_q_heads - 1]]))
+    want, want_lse = quant.prefix_attn_q(w.dtype, oq, bits, kb, vb, w.q, w.cu_seqlens_q, w.context_lens, bt,
+                                         qpages, w.softmax_scale, rows=rows)
+    o = out.float().cpu().numpy().astype(np.float64).reshape(T * w.num_q_heads, -1)[rows]
+    l = lse.cpu().numpy().astype(np.float64).T.reshape(-1)[rows]
+    assert torch.isfinite(out.float()).all()
+    assert np.abs(o - want).max() <= TOL[w.dtype]
+    assert np.abs(l - want_lse).max() <= LSE_TOL
+
+
+def test_quantized_prefill_bad_quantized_block_is_flagged():
+    import paged_prefix_reuse_gb300 as kvp
+
+    w = wl.make_random(250, [200], [30], Hq=4, Hkv=2, d=128, dtype="bf16")
+    st, qp, oq, bt, qpages, kb, vb = _prefill_q_case(w, 8, [1.0])
+    bt = bt.copy()
+    bt[0, 1] = qp.num_blocks + 5  # outside the quantized pool (it is inside the 16-bit one)
+    out, lse = kvp.kvp_prefix_attn_q(st.pool, qp, torch.from_numpy(qpages).cuda(), st.q, st.cu, st.ctx,
+                                     torch.from_numpy(bt).cuda(), st.max_q_pf, st.max_ctx_pf, w.softmax_scale)
+    torch.cuda.synchronize()
+    assert st.pool.errors() & kvp.DEVERR["bad_block"]
