@@ -71,8 +71,11 @@ __global__ void slot_mapping_kernel(PoolView pool, const int32_t* __restrict__ c
 // Append.  A token's K (and V) rows for all kv heads are vpt = Hkv * d / 8
 // 16-byte vectors.  A 256-thread block covers tpb = max(1, 256 / vpt) tokens
 // per step; thread i owns vector i % vpt of token i / vpt (computed once, in
-// 32-bit arithmetic) and walks tokens with a grid stride, keeping kUnroll
-// tokens' loads in flight before their stores.
+// 32-bit arithmetic) and walks tokens with a grid stride, kUnroll tokens per
+// pass.  The new K/V rows do not depend on the slot, so each pass issues the
+// data loads together with the slot loads -- one memory round trip, not two
+// -- and stores once both have arrived.  (A token whose slot is -1 has its
+// rows read for nothing; padding tokens are rare.)
 constexpr int kUnroll = 4;
 
 __global__ void __launch_bounds__(kThreads) append_kernel(PoolView pool, uint4* __restrict__ k_pool,
@@ -93,29 +96,28 @@ __global__ void __launch_bounds__(kThreads) append_kernel(PoolView pool, uint4* 
         const int64_t step = static_cast<int64_t>(gridDim.x) * tpb;
         for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * tpb + tok_local; t0 < T; t0 += step * kUnroll) {
             uint4 kv[kUnroll], vv[kUnroll];
-            int64_t dst[kUnroll];
+            int64_t sl[kUnroll];
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int64_t t = t0 + u * step;
-                dst[u] = -1;
+                sl[u] = -1;
                 if (t < T) {
-                    const int64_t slot = __ldg(slots + t);
-                    if (slot >= 0 && slot < num_slots) {
-                        const int64_t blk = slot / pool.block_size;
-                        const int64_t row = slot - blk * pool.block_size;
-                        dst[u] = ((blk * pool.num_kv_heads + h) * pool.block_size + row) * vph + c;
-                        kv[u] = __ldcs(k_new + t * vpt + j);
-                        vv[u] = __ldcs(v_new + t * vpt + j);
-                    } else if (slot != -1 && j == 0) {
-                        report(pool.err_word, KVP_DEVERR_BAD_SLOT);
-                    }
+                    sl[u] = __ldg(slots + t);
+                    kv[u] = __ldcs(k_new + t * vpt + j);
+                    vv[u] = __ldcs(v_new + t * vpt + j);
                 }
             }
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
-                if (dst[u] >= 0) {
-                    k_pool[dst[u]] = kv[u];
-                    v_pool[dst[u]] = vv[u];
+                const int64_t slot = sl[u];
+                if (slot >= 0 && slot < num_slots) {
+                    const int64_t blk = slot / pool.block_size;
+                    const int64_t row = slot - blk * pool.block_size;
+                    const int64_t dst = ((blk * pool.num_kv_heads + h) * pool.block_size + row) * vph + c;
+                    k_pool[dst] = kv[u];
+                    v_pool[dst] = vv[u];
+                } else if (slot != -1 && j == 0) {
+                    report(pool.err_word, KVP_DEVERR_BAD_SLOT);
                 }
             }
         }

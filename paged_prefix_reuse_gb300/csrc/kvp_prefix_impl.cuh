@@ -57,6 +57,8 @@
 //  * the products run in fp16 whatever the pool dtype (Q is converted when
 //    it is staged, P is written as fp16), as in the quantized decode.
 #pragma once
+#include <type_traits>
+
 #include "kvp_internal.cuh"
 
 namespace kvp {
@@ -185,57 +187,90 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 a) {
 // V[t][c] = code * s_t + z_t (per token), one fp16 fused multiply-add per
 // pair; columns past the head dimension are zeros.  The other pages already
 // hold 16-bit values from TMA and, for a bf16 pool, are converted in place.
+// All of a page's code and scale loads are issued before its stores (the
+// staging and the slot are both shared memory, so a store could otherwise
+// not be moved past the next load), and the next page's loads before the
+// current page's arithmetic.
 template <bool kBF16, int D, int BITS>
-__device__ __forceinline__ void prefix_fill_rows(const uint8_t* stage, uint8_t* dst, int kv, int dw, int nq,
-                                                 int lane) {
+__device__ __forceinline__ void prefix_fill_rows(const uint8_t* __restrict__ stage, uint8_t* __restrict__ dst,
+                                                 int kv, int dw, int nq, int lane) {
     constexpr int DP = prefix_width(D);
     using QC = PrefixQCfg<D, BITS>;
     using L = PrefixCfg<DP>;         // layout of a slot (chunks of CW columns)
     constexpr int U = DP / 8;        // 16-byte units per row of the slot
     constexpr int UD = D / 8;        // units that hold data
     constexpr int RPP = 32 / U;      // rows per pass of the warp
+    constexpr int IT = 16 / RPP;     // passes per page
     constexpr int CROW = D * BITS / 8;
+    using CodeT = typename std::conditional<BITS == 8, uint2, uint32_t>::type;
     const int u = lane % U;
     const int r_in = lane / U;
+    const bool has = u < UD;
     const uint32_t ubase = (u / (L::CW / 8)) * L::CHUNK_BYTES;
     const int uc = u % (L::CW / 8);
-#pragma unroll
-    for (int pg = 0; pg < 4; ++pg) {
-        const int i = 4 * dw + pg;  // page of the tile
-        if (i < nq) {
+    auto slot_ptr = [&](int r) -> uint4* { return reinterpret_cast<uint4*>(dst + ubase + swz_offset(r, uc, L::ROWB)); };
+    const int i0 = 4 * dw;
+    const int nmine = min(max(nq - i0, 0), 4);  // quantized pages among this warp's four
+    if (nmine > 0) {
+        // Loads of one page: its codes for this lane's unit in every pass,
+        // and its scales (K: this unit's 8 channels; V: each pass's token).
+        CodeT c[2][IT];
+        uint32_t m0[2][IT > 4 ? IT : 4], m1[2][4];
+        auto load_page = [&](int b, int i) {
             const uint8_t* codes = stage + i * QC::CODE + u * BITS;
             const uint8_t* meta = stage + QC::OFF_META + i * (kv ? QC::VMETA : QC::KMETA);
-            uint32_t ks[4] = {0, 0, 0, 0}, kz[4] = {0, 0, 0, 0};
-            if (kv == 0 && u < UD) {
-                const uint4 a = *reinterpret_cast<const uint4*>(meta + u * 16);
-                const uint4 b = *reinterpret_cast<const uint4*>(meta + 2 * D + u * 16);
-                ks[0] = a.x; ks[1] = a.y; ks[2] = a.z; ks[3] = a.w;
-                kz[0] = b.x; kz[1] = b.y; kz[2] = b.z; kz[3] = b.w;
-            }
 #pragma unroll
-            for (int it = 0; it < 16 / RPP; ++it) {
-                const int t = it * RPP + r_in;  // token of the page
-                const int r = 16 * i + t;       // row of the slot
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (u < UD) {
-                    if (kv == 0) {
-                        v = dequant_unit<BITS>(codes + t * CROW, ks, kz);
-                    } else {
-                        const uint32_t sz = *reinterpret_cast<const uint32_t*>(meta + 4 * t);  // (s_t, z_t)
-                        const uint32_t s1 = __byte_perm(sz, 0, 0x1010), z1 = __byte_perm(sz, 0, 0x3232);
-                        const uint32_t vs[4] = {s1, s1, s1, s1}, vz[4] = {z1, z1, z1, z1};
-                        v = dequant_unit<BITS>(codes + t * CROW, vs, vz);
-                    }
+            for (int it = 0; it < IT; ++it)
+                c[b][it] = has ? *reinterpret_cast<const CodeT*>(codes + (it * RPP + r_in) * CROW) : CodeT{};
+            if (kv == 0) {
+                uint4 a = make_uint4(0, 0, 0, 0), z = make_uint4(0, 0, 0, 0);
+                if (has) {
+                    a = *reinterpret_cast<const uint4*>(meta + u * 16);
+                    z = *reinterpret_cast<const uint4*>(meta + 2 * D + u * 16);
                 }
-                *reinterpret_cast<uint4*>(dst + ubase + swz_offset(r, uc, L::ROWB)) = v;
-            }
-        } else if constexpr (kBF16) {
+                m0[b][0] = a.x; m0[b][1] = a.y; m0[b][2] = a.z; m0[b][3] = a.w;
+                m1[b][0] = z.x; m1[b][1] = z.y; m1[b][2] = z.z; m1[b][3] = z.w;
+            } else {
 #pragma unroll
-            for (int it = 0; it < 16 / RPP; ++it) {
-                const int r = 16 * i + it * RPP + r_in;
-                uint4* a = reinterpret_cast<uint4*>(dst + ubase + swz_offset(r, uc, L::ROWB));
-                *a = bf16x8_to_f16x8(*a);
+                for (int it = 0; it < IT; ++it)
+                    m0[b][it] = *reinterpret_cast<const uint32_t*>(meta + 4 * (it * RPP + r_in));  // (s_t, z_t)
             }
+        };
+        load_page(0, i0);
+#pragma unroll
+        for (int pg = 0; pg < 4; ++pg) {
+            if (pg >= nmine) break;
+            const int b = pg & 1;
+            if (pg + 1 < nmine) load_page(b ^ 1, i0 + pg + 1);
+            uint4 v[IT];
+#pragma unroll
+            for (int it = 0; it < IT; ++it) {
+                if (kv == 0) {
+                    const uint32_t ks[4] = {m0[b][0], m0[b][1], m0[b][2], m0[b][3]};
+                    const uint32_t kz[4] = {m1[b][0], m1[b][1], m1[b][2], m1[b][3]};
+                    v[it] = dequant_unit<BITS>(reinterpret_cast<const uint8_t*>(&c[b][it]), ks, kz);
+                } else {
+                    const uint32_t sz = m0[b][it];
+                    const uint32_t s1 = __byte_perm(sz, 0, 0x1010), z1 = __byte_perm(sz, 0, 0x3232);
+                    const uint32_t vs[4] = {s1, s1, s1, s1}, vz[4] = {z1, z1, z1, z1};
+                    v[it] = dequant_unit<BITS>(reinterpret_cast<const uint8_t*>(&c[b][it]), vs, vz);
+                }
+                if (!has) v[it] = make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int it = 0; it < IT; ++it) *slot_ptr(16 * (i0 + pg) + it * RPP + r_in) = v[it];
+        }
+    }
+    if constexpr (kBF16) {
+        // This warp's 16-bit pages (the live suffix): bf16 -> fp16 in place.
+#pragma unroll
+        for (int pg = 0; pg < 4; ++pg) {
+            if (pg < nmine) continue;
+            uint4 a[IT];
+#pragma unroll
+            for (int it = 0; it < IT; ++it) a[it] = *slot_ptr(16 * (i0 + pg) + it * RPP + r_in);
+#pragma unroll
+            for (int it = 0; it < IT; ++it) *slot_ptr(16 * (i0 + pg) + it * RPP + r_in) = bf16x8_to_f16x8(a[it]);
         }
     }
 }
