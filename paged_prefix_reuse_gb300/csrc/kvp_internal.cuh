@@ -471,19 +471,18 @@ __device__ __forceinline__ uint32_t magic_pair(uint32_t w, uint32_t sel) {
 
 // Dequantize one 8-channel unit: codes -> fp16 (1024 + c) - 1024, then
 // c * s + z in one fp16 fused multiply-add per pair (a single rounding).
-// 8 bits: 8 code bytes; 4 bits: 8 nibbles, the even channel in the low one.
+// 8 bits: 8 code bytes in w.x, w.y; 4 bits: 8 nibbles in w.x, the even
+// channel in the low one.
 template <int BITS>
-__device__ __forceinline__ uint4 dequant_unit(const uint8_t* codes, const uint32_t (&s2)[4], const uint32_t (&z2)[4]) {
+__device__ __forceinline__ uint4 dequant_words(uint2 w, const uint32_t (&s2)[4], const uint32_t (&z2)[4]) {
     uint32_t h[4];
     if constexpr (BITS == 8) {
-        const uint2 w = *reinterpret_cast<const uint2*>(codes);
         h[0] = magic_pair(w.x, 0x4140);
         h[1] = magic_pair(w.x, 0x4342);
         h[2] = magic_pair(w.y, 0x4140);
         h[3] = magic_pair(w.y, 0x4342);
     } else {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(codes);
-        const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;  // even / odd channels
+        const uint32_t lo = w.x & 0x0F0F0F0Fu, hi = (w.x >> 4) & 0x0F0F0F0Fu;  // even / odd channels
         const uint32_t t = __byte_perm(lo, hi, 0x5140), u = __byte_perm(lo, hi, 0x7362);  // c0..c3, c4..c7
         h[0] = magic_pair(t, 0x4140);
         h[1] = magic_pair(t, 0x4342);
@@ -499,6 +498,40 @@ __device__ __forceinline__ uint4 dequant_unit(const uint8_t* codes, const uint32
         o[j] = *reinterpret_cast<const uint32_t*>(&x);
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// The same, reading the unit's codes through a pointer.
+template <int BITS>
+__device__ __forceinline__ uint4 dequant_unit(const uint8_t* codes, const uint32_t (&s2)[4], const uint32_t (&z2)[4]) {
+    uint2 w;
+    if constexpr (BITS == 8) {
+        w = *reinterpret_cast<const uint2*>(codes);
+    } else {
+        w = make_uint2(*reinterpret_cast<const uint32_t*>(codes), 0u);
+    }
+    return dequant_words<BITS>(w, s2, z2);
+}
+
+// ---- explicit shared-memory accesses (32-bit shared addresses) ----
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
 }
 
 template <bool kBF16>

@@ -104,9 +104,36 @@ SMALL = {
 }
 
 
+# A CTA with one live query tile and at least two key tiles splits the key
+# range between its two softmax warpgroups and merges their partial results:
+# odd and even tile counts, a one-token chunk over a long prefix, a chunk of
+# exactly one tile with no prefix (no split), one just over a tile (two
+# query tiles, no split), logits large enough that the two halves' maxima
+# differ by far more than 2^8.
+SMALL.update({
+    "key_split_g1_bf16": lambda: wl.make_random(81, [500, 1000, 0, 37], [100, 3, 128, 129], Hq=4, Hkv=4, d=128,
+                                                dtype="bf16"),
+    "key_split_g2_f16_d64": lambda: wl.make_random(82, [700, 260, 5], [60, 17, 64], Hq=4, Hkv=2, d=64,
+                                                   dtype="f16"),
+    "key_split_d96_large_logits": lambda: wl.make_random(83, [900, 1], [70, 120], Hq=3, Hkv=3, d=96, dtype="f16",
+                                                         q_std=6.0),
+    "key_split_bs8_gqa5": lambda: wl.make_random(84, [333, 2000], [25, 1], Hq=10, Hkv=2, d=128, dtype="bf16",
+                                                 bs=8),
+})
+
+
 @pytest.mark.parametrize("name", sorted(SMALL))
 def test_small_workloads_match_oracle(name):
     _check_step(SMALL[name]())
+
+
+@pytest.mark.parametrize("splits", [2, 3])
+def test_key_split_within_cta_combined_with_split_kv(splits):
+    """Single-tile CTAs whose key range is also cut across CTAs: each CTA's
+    share is again split between its warpgroups and merged, then the CTAs'
+    partials are merged by log-sum-exp."""
+    w = wl.make_random(85, [1500, 777], [90, 40], Hq=6, Hkv=6, d=128, dtype="bf16")
+    _check_step(w, prefix_splits=splits)
 
 
 @pytest.mark.parametrize("splits", [1, 2, 3, 7])
