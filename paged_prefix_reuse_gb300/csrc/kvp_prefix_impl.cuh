@@ -278,9 +278,6 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
     uint64_t* qempty = qfull + QC::NQS;          // [NQS] staging slot dequantized (2 warp arrivals)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    // The key-split mode, kept in shared memory so that the softmax warps do
-    // not hold it in a register through their loop (read again after it).
-    volatile int* split_flag = abort_flag + 1;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_trigger();
@@ -317,22 +314,6 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
     const int per = (n_tiles + p.num_splits - 1) / p.num_splits;
     const int j_begin = min(n_tiles, split * per);
     const int n_local = min(n_tiles, j_begin + per) - j_begin;
-    // A CTA with one live query tile and at least two key tiles splits that
-    // tile's key range between its two softmax warpgroups -- warpgroup 0 the
-    // first ceil(n/2) tiles, warpgroup 1 the rest -- so that the tensor core
-    // alternates between two softmax chains as it does for two query tiles;
-    // warpgroup 0 merges the two partial results (O, max, sum) at the end.
-    const bool kv_split = !has1 && n_local >= 2;
-    const int n_w0 = kv_split ? (n_local + 1) / 2 : n_local;  // tiles of warpgroup 0
-    const int n_w1 = kv_split ? n_local - n_w0 : n_local;      // tiles of warpgroup 1
-    // The K/V tiles in ring order (visit v loads K then V of one tile): in
-    // order without a split; with one, warpgroup 0's and 1's tiles alternate,
-    // warpgroup 0's last one alone when it has one more.
-    auto visit_tile = [&](int v) -> int {
-        if (!kv_split) return j_begin + v;
-        if (v < 2 * n_w1) return j_begin + (v & 1) * n_w0 + (v >> 1);
-        return j_begin + n_w1 + (v - 2 * n_w1);
-    };
 
     if (n_local <= 0) {
         // This split's key range is empty for the whole CTA: empty partials.
@@ -364,7 +345,6 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
         }
         mbar_init(stall, 1);
         *abort_flag = 0;
-        *split_flag = kv_split ? 1 : 0;
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -379,17 +359,15 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
     if (warp < kSoftmaxWarps) {
         // =========================== softmax warpgroups ===========================
         const int wg = warp >> 2;
-        if (wg == 0 || has1 || kv_split) {
+        if (wg == 0 || has1) {
             const int row = tid & (kBM - 1);
-            const int qt_wg = kv_split ? 0 : wg;  // the query tile this warpgroup works on
-            const int rtile = r0 + qt_wg * kBM;    // its first row
-            const int rg = rtile + row;
+            const int rg = r0 + wg * kBM + row;
             const bool valid = rg < rows_total;
             const int token = valid ? rg / g : 0;
             const int head = h * g + (valid ? rg % g : 0);
             const int qpos = valid ? P + token : L - 1;
 
-            if (qt_wg == wg) {  // Q tile wg -> swizzled shared memory (K-major A operand)
+            {  // Q tile wg -> swizzled shared memory (K-major A operand)
                 // All of this thread's 16-byte loads are issued before any store,
                 // so their latencies overlap instead of adding up.
                 constexpr int V16 = D / 8;
@@ -432,10 +410,8 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
             const float sl2 = p.scale_log2;
             float m = -INFINITY, l = 0.f;
             bool ok = true;
-            const int n_mine = wg ? n_w1 : n_w0;
-            const int j_first = j_begin + (kv_split && wg ? n_w0 : 0);
-            for (int jj = 0; jj < n_mine; ++jj) {
-                const int j = j_first + jj;
+            for (int jj = 0; jj < n_local; ++jj) {
+                const int j = j_begin + jj;
                 if (!mbar_wait(&s_full[wg], jj & 1, abort_flag, err, p.wait_limit_ns)) { ok = false; break; }
                 tc_fence_after();
                 float x[kBN];
@@ -509,46 +485,10 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
 
             // ------------------------------ epilogue ------------------------------
             if (ok) ok = mbar_wait(&o_done[wg], 0, abort_flag, err, p.wait_limit_ns);
-            const bool merged = *split_flag != 0;  // kv_split, from shared memory
-            // Output scale factors: O = O_wg * f0 (+ O_1 * f1 when the key range
-            // was split), lse2 in the log2 domain.
-            float f0 = 0.f, f1 = 0.f, lse2 = -INFINITY;
-            if (merged) {
-                // Warpgroup 1 hands its row maximum and sum to warpgroup 0 through
-                // its unused Q region; both warpgroups always reach the barrier.
-                float2* stats = reinterpret_cast<float2*>(smem + C::OFF_Q + C::TILE_BYTES);
-                if (wg == 1 && ok) stats[row] = make_float2(m, l);
-                asm volatile("bar.sync 3, 256;" ::: "memory");
-                if (wg == 1 || *abort_flag) ok = false;
-                if (ok) {
-                    const float2 st1 = stats[row];
-                    const float M = fmaxf(m, st1.x);
-                    const float a0 = m == -INFINITY ? 0.f : fast_exp2(m - M);
-                    const float a1 = st1.x == -INFINITY ? 0.f : fast_exp2(st1.x - M);
-                    const float lsum = l * a0 + st1.y * a1;
-                    const float iv = lsum > 0.f ? 1.f / lsum : 0.f;
-                    f0 = a0 * iv;
-                    f1 = a1 * iv;
-                    lse2 = lsum > 0.f ? M + __log2f(lsum) : -INFINITY;
-                }
-            } else if (ok) {
-                f0 = l > 0.f ? 1.f / l : 0.f;
-                lse2 = l > 0.f ? m + __log2f(l) : -INFINITY;
-            }
-            // Columns [16 cb, 16 cb + 16) of this row's output, scaled (fp32).
-            auto load_o = [&](int cb, float (&o)[16]) {
-                uint32_t r[16];
-                tmem_ld16_sync(lane_base + ocol + 16 * cb, r);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) o[i] = __uint_as_float(r[i]) * f0;
-                if (merged) {
-                    tmem_ld16_sync(lane_base + C::O_COL1 + 16 * cb, r);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) o[i] = fmaf(__uint_as_float(r[i]), f1, o[i]);
-                }
-            };
             if (ok) {
                 tc_fence_after();
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const float lse2 = l > 0.f ? m + __log2f(l) : -INFINITY;
                 const int64_t orow = static_cast<int64_t>(cu0 + token) * p.num_q_heads + head;
                 if (p.num_splits == 1) {
                     // Stage the bf16/fp16 O tile in this warpgroup's Q region (the
@@ -559,17 +499,17 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
                     uint4* stg = reinterpret_cast<uint4*>(smem + C::OFF_Q + wg * C::TILE_BYTES);
 #pragma unroll 1
                     for (int cb = 0; cb < D / 16; ++cb) {
-                        float o[16];
-                        load_o(cb, o);
+                        uint32_t r[16];
+                        tmem_ld16_sync(lane_base + ocol + 16 * cb, r);
                         uint4 a0, a1;
-                        a0.x = pack2<kBF16>(o[0], o[1]);
-                        a0.y = pack2<kBF16>(o[2], o[3]);
-                        a0.z = pack2<kBF16>(o[4], o[5]);
-                        a0.w = pack2<kBF16>(o[6], o[7]);
-                        a1.x = pack2<kBF16>(o[8], o[9]);
-                        a1.y = pack2<kBF16>(o[10], o[11]);
-                        a1.z = pack2<kBF16>(o[12], o[13]);
-                        a1.w = pack2<kBF16>(o[14], o[15]);
+                        a0.x = pack2<kBF16>(__uint_as_float(r[0]) * inv, __uint_as_float(r[1]) * inv);
+                        a0.y = pack2<kBF16>(__uint_as_float(r[2]) * inv, __uint_as_float(r[3]) * inv);
+                        a0.z = pack2<kBF16>(__uint_as_float(r[4]) * inv, __uint_as_float(r[5]) * inv);
+                        a0.w = pack2<kBF16>(__uint_as_float(r[6]) * inv, __uint_as_float(r[7]) * inv);
+                        a1.x = pack2<kBF16>(__uint_as_float(r[8]) * inv, __uint_as_float(r[9]) * inv);
+                        a1.y = pack2<kBF16>(__uint_as_float(r[10]) * inv, __uint_as_float(r[11]) * inv);
+                        a1.z = pack2<kBF16>(__uint_as_float(r[12]) * inv, __uint_as_float(r[13]) * inv);
+                        a1.w = pack2<kBF16>(__uint_as_float(r[14]) * inv, __uint_as_float(r[15]) * inv);
                         stg[row * V16 + (2 * cb + row) % V16] = a0;
                         stg[row * V16 + (2 * cb + 1 + row) % V16] = a1;
                     }
@@ -584,7 +524,7 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
 #pragma unroll 1
                     for (int e = row; e < kBM * V16; e += kBM) {
                         const int rr = e / V16, c = e % V16;
-                        const int rgl = rtile + rr;
+                        const int rgl = r0 + wg * kBM + rr;
                         if (rgl < rows_total) {
                             const int64_t grow =
                                 static_cast<int64_t>(cu0 + rgl / g) * p.num_q_heads + h * g + rgl % g;
@@ -595,13 +535,14 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
                     float* dst = p.ws_o + (orow * p.num_splits + split) * D;
 #pragma unroll
                     for (int cb = 0; cb < D / 16; ++cb) {
-                        float o[16];
-                        load_o(cb, o);
+                        uint32_t r[16];
+                        tmem_ld16_sync(lane_base + ocol + 16 * cb, r);
                         if (valid) {
 #pragma unroll
                             for (int i = 0; i < 16; i += 4)
                                 *reinterpret_cast<float4*>(dst + 16 * cb + i) =
-                                    make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+                                    make_float4(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv,
+                                                __uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv);
                         }
                     }
                     if (valid) p.ws_lse[orow * p.num_splits + split] = lse2;
@@ -615,42 +556,29 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
             prefetch_tmap(&tmap_v);
         }
         const int pages_per_tile = kBN / BS;  // 4, 8 or 16: a tile never straddles a 32-page batch
+        const int page_first = j_begin * pages_per_tile;
         const int32_t* table = p.block_tables + static_cast<int64_t>(s) * p.max_blocks;
-        // The tiles come from one contiguous page range, or (key split) two:
-        // warpgroup 0's from base0, warpgroup 1's from base1.  Per range, lane
-        // i holds the block id of page (base + batch * 32 + i); the next batch
-        // is requested 32 pages ahead so its latency hides behind the tiles in
-        // flight.
-        const int base0 = j_begin * pages_per_tile;
-        const int base1 = (j_begin + n_w0) * pages_per_tile;
-        auto load_pg = [&](int pg) -> int { return __ldg(table + min(pg, npages - 1)); };
-        int cur0 = load_pg(base0 + lane), nxt0 = load_pg(base0 + 32 + lane), bat0 = 0;
-        int cur1 = 0, nxt1 = 0, bat1 = 0;
-        if (kv_split) {
-            cur1 = load_pg(base1 + lane);
-            nxt1 = load_pg(base1 + 32 + lane);
-        }
+        // Lane i holds the block id of page (batch * 32 + i); the next batch is
+        // requested 32 pages ahead so its latency hides behind the tiles in flight.
+        auto load_batch = [&](int batch) -> int {
+            const int pg = min(page_first + batch * 32 + lane, npages - 1);
+            return __ldg(table + pg);
+        };
+        int blk_cur = load_batch(0);
+        int blk_nxt = load_batch(1);
         pdl_wait();  // pool contents from the kernel before (the append) are read from here on
-        int loads = 0;   // ring loads issued: visit v loads K as 2v, V as 2v + 1
-        int staged = 0;  // quantized half-tiles staged, in ring order
+        int loads = 0;   // ring loads issued: K_j is load 2j, V_j is load 2j+1
+        int staged = 0;  // quantized half-tiles staged (they come first)
         bool stop = false;
         for (int jj = 0; jj < n_local && !stop; ++jj) {
-            const int range = (kv_split && jj < 2 * n_w1) ? (jj & 1) : 0;
-            const int j = visit_tile(jj);
-            const int rbase = range ? base1 : base0;
-            const int rel = j * pages_per_tile - rbase;  // page of the tile within its range
-            if (range == 0 && (rel >> 5) != bat0) {
-                cur0 = nxt0;
-                nxt0 = load_pg(base0 + ((rel >> 5) + 1) * 32 + lane);
-                bat0 = rel >> 5;
-            } else if (range == 1 && (rel >> 5) != bat1) {
-                cur1 = nxt1;
-                nxt1 = load_pg(base1 + ((rel >> 5) + 1) * 32 + lane);
-                bat1 = rel >> 5;
+            const int rel = jj * pages_per_tile;
+            if ((rel & 31) == 0 && jj > 0) {
+                blk_cur = blk_nxt;
+                blk_nxt = load_batch((rel >> 5) + 1);
             }
-            int my_blk = range ? cur1 : cur0;
+            int my_blk = blk_cur;
             // Pages before qp name blocks of the quantized pool.
-            const int my_pg = min(rbase + (rel & ~31) + lane, npages - 1);
+            const int my_pg = min(page_first + (rel & ~31) + lane, npages - 1);
             const int64_t my_lim = (BITS > 0 && my_pg < qp) ? p.qpool.num_blocks : p.pool.num_blocks;
             if (my_blk < 0 || my_blk >= my_lim) {
                 report(err, KVP_DEVERR_BAD_BLOCK);
@@ -661,19 +589,18 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
             const int blk_q = __shfl_sync(0xffffffffu, my_blk, ((rel & 31) + lane) & 31);
             const int32_t y = (blk_q * Hkv + h) * BS;
             // Quantized pages of this tile: its first nq pages (BITS > 0: 16-token pages).
-            const int nq = BITS ? min(max(qp - j * pages_per_tile, 0), pages_per_tile) : 0;
+            const int nq = BITS ? min(max(qp - (page_first + rel), 0), pages_per_tile) : 0;
             for (int kv = 0; kv < 2; ++kv) {
                 const int gl = 2 * jj + kv;
                 const int slot = gl % C::NSLOT;
                 if constexpr (BITS > 0) {
                     if (nq > 0) {
-                        // Stage the quantized pages' codes and scales (staging slots
-                        // are used in ring order by the half-tiles that need them).
-                        const int qs = staged % QC::NQS;
+                        // Stage the quantized pages' codes and scales.  Half-tiles with
+                        // quantized pages come first, so the staging index is gl.
+                        const int qs = gl % QC::NQS;
                         int okq = 1;
-                        if (lane == 0 && staged >= QC::NQS)
-                            okq = mbar_wait(&qempty[qs], ((staged / QC::NQS) - 1) & 1, abort_flag, err,
-                                            p.wait_limit_ns);
+                        if (lane == 0 && gl >= QC::NQS)
+                            okq = mbar_wait(&qempty[qs], ((gl / QC::NQS) - 1) & 1, abort_flag, err, p.wait_limit_ns);
                         okq = __shfl_sync(0xffffffffu, okq, 0);
                         if (!okq) {
                             stop = true;
@@ -690,7 +617,7 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
                             const __half* msrc = kv ? p.qpool.v_meta + ph * 32 : p.qpool.k_meta + ph * 2 * D;
                             bulk_load(st + QC::OFF_META + lane * meta, msrc, meta, &qfull[qs]);
                         }
-                        ++staged;
+                        staged = gl + 1;
                     }
                 }
                 int ok = 1;
@@ -756,7 +683,8 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
             last_par = (gl / C::NSLOT) & 1;
         };
         // The whole warp runs these (the MMA and commit wrappers elect one lane).
-        auto issue_s_q = [&](int i, uint32_t qb, uint32_t kbase) {
+        auto issue_s = [&](int i, uint32_t kbase) {
+            const uint32_t qb = i ? qb1 : qb0;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = ((kk * 16) / C::CW) * C::CHUNK_BYTES + ((kk * 16) % C::CW) * 2;
@@ -766,7 +694,6 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
             }
             tc_commit(&s_full[i]);
         };
-        auto issue_s = [&](int i, uint32_t kbase) { issue_s_q(i, i ? qb1 : qb0, kbase); };
         auto issue_pv = [&](int i, uint32_t vbase, bool accumulate) {
             const uint32_t scol = i ? C::S_COL1 : C::S_COL0;
 #pragma unroll
@@ -782,11 +709,22 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
         bool ok = p.stall_test ? stall_wait(stall, abort_flag, err, p.wait_limit_ns) : true;
         if (ok) ok = mbar_wait(&q_full[0], 0, abort_flag, err, p.wait_limit_ns);
         if (ok && has1) ok = mbar_wait(&q_full[1], 0, abort_flag, err, p.wait_limit_ns);
-        // Rows past the context may hold any bytes (even NaN); P is 0 there,
-        // but 0 * NaN is NaN, so clear those V rows of tile j in ring load gv.
-        auto zero_v_tail = [&](int gv, int j) {
-            const int nvalid = L - j * kBN;
+        if (ok) ok = wait_slot(0);
+        if (ok) {
+            tc_fence_after();
+            issue_s(0, slot_addr(0));
+            if (has1) issue_s(1, slot_addr(0));
+            release(0);
+            __syncwarp();
+        }
+        for (int jj = 0; ok && jj < n_local; ++jj) {
+            const int gv = 2 * jj + 1, gk = 2 * jj + 2;
+            const bool more = jj + 1 < n_local;
+            if (!wait_slot(gv)) { ok = false; break; }
+            const int nvalid = L - (j_begin + jj) * kBN;
             if (nvalid < kBN) {
+                // Rows past the context may hold any bytes (even NaN); P is 0
+                // there, but 0 * NaN is NaN, so clear those V rows.
                 uint8_t* vt = smem + C::OFF_RING + (gv % C::NSLOT) * C::TILE_BYTES;
                 const int first = max(nvalid, 0);
                 const int per_row = C::ROWB / 16;
@@ -800,84 +738,29 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
                 fence_proxy_async_smem();
                 __syncwarp();
             }
-        };
-        if (!kv_split) {
-            if (ok) ok = wait_slot(0);
-            if (ok) {
+            // ---- query tile 0: PV_0(jj), then S_0(jj+1)
+            if (!mbar_wait(&p_full[0], jj & 1, abort_flag, err, p.wait_limit_ns)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv(0, slot_addr(gv), jj > 0);
+            if (!more) tc_commit(&o_done[0]);
+            if (more) {
+                if (!wait_slot(gk)) { ok = false; break; }
                 tc_fence_after();
-                issue_s(0, slot_addr(0));
-                if (has1) issue_s(1, slot_addr(0));
-                release(0);
-                __syncwarp();
+                issue_s(0, slot_addr(gk));
             }
-            for (int jj = 0; ok && jj < n_local; ++jj) {
-                const int gv = 2 * jj + 1, gk = 2 * jj + 2;
-                const bool more = jj + 1 < n_local;
-                if (!wait_slot(gv)) { ok = false; break; }
-                zero_v_tail(gv, j_begin + jj);
-                // ---- query tile 0: PV_0(jj), then S_0(jj+1)
-                if (!mbar_wait(&p_full[0], jj & 1, abort_flag, err, p.wait_limit_ns)) { ok = false; break; }
+            // ---- query tile 1: PV_1(jj), then S_1(jj+1)
+            if (has1) {
+                if (!mbar_wait(&p_full[1], jj & 1, abort_flag, err, p.wait_limit_ns)) { ok = false; break; }
                 tc_fence_after();
-                issue_pv(0, slot_addr(gv), jj > 0);
-                if (!more) tc_commit(&o_done[0]);
-                if (more) {
-                    if (!wait_slot(gk)) { ok = false; break; }
-                    tc_fence_after();
-                    issue_s(0, slot_addr(gk));
-                }
-                // ---- query tile 1: PV_1(jj), then S_1(jj+1)
-                if (has1) {
-                    if (!mbar_wait(&p_full[1], jj & 1, abort_flag, err, p.wait_limit_ns)) { ok = false; break; }
-                    tc_fence_after();
-                    issue_pv(1, slot_addr(gv), jj > 0);
-                    if (!more) tc_commit(&o_done[1]);
-                }
-                release(gv);
-                if (more) {
-                    if (has1) issue_s(1, slot_addr(gk));
-                    release(gk);
-                }
-                __syncwarp();
+                issue_pv(1, slot_addr(gv), jj > 0);
+                if (!more) tc_commit(&o_done[1]);
             }
-        } else {
-            // Key split: both warpgroups multiply query tile 0; warpgroup w's
-            // step i takes ring loads kidx(w, i) (K) and kidx(w, i) + 1 (V),
-            // in the producer's visiting order.  Every slot is released right
-            // after its last product is issued, so the producer (which fills
-            // slots in ring order) never waits on a slot the MMA still needs.
-            auto kidx = [&](int w, int i) -> int { return 2 * (i < n_w1 ? 2 * i + w : 2 * n_w1 + (i - n_w1)); };
-#pragma unroll 1
-            for (int w = 0; w < 2 && ok; ++w) {
-                if (!wait_slot(kidx(w, 0))) { ok = false; break; }
-                tc_fence_after();
-                issue_s_q(w, qb0, slot_addr(kidx(w, 0)));
-                release(kidx(w, 0));
+            release(gv);
+            if (more) {
+                if (has1) issue_s(1, slot_addr(gk));
+                release(gk);
             }
             __syncwarp();
-            for (int i = 0; ok && i < n_w0; ++i) {
-#pragma unroll 1
-                for (int w = 0; w < 2; ++w) {
-                    const int nw = w ? n_w1 : n_w0;
-                    if (i >= nw) continue;
-                    const int gv = kidx(w, i) + 1;
-                    if (!wait_slot(gv)) { ok = false; break; }
-                    zero_v_tail(gv, j_begin + (w ? n_w0 : 0) + i);
-                    if (!mbar_wait(&p_full[w], i & 1, abort_flag, err, p.wait_limit_ns)) { ok = false; break; }
-                    tc_fence_after();
-                    issue_pv(w, slot_addr(gv), i > 0);
-                    release(gv);
-                    if (i + 1 < nw) {
-                        const int gk = kidx(w, i + 1);
-                        if (!wait_slot(gk)) { ok = false; break; }
-                        tc_fence_after();
-                        issue_s_q(w, qb0, slot_addr(gk));
-                        release(gk);
-                    } else {
-                        tc_commit(&o_done[w]);
-                    }
-                }
-                __syncwarp();
-            }
         }
         // Let every issued MMA finish before tensor memory is released.
         if (lane == 0 && last_bar) {
@@ -889,17 +772,16 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
         // ====================== dequantizing warps (BITS > 0) ======================
         if constexpr (BITS > 0) {
             const int dw = warp - kDequantWarp0;  // owns rows [64 dw, 64 dw + 64) of every slot
-            int sidx = 0;                          // staging slots consumed, in ring order
             for (int gl = 0; gl < 2 * n_local; ++gl) {
                 const int slot = gl % C::NSLOT;
                 // The slot is ours once the producer has armed it (after the MMA
                 // released it) and its 16-bit pages have landed.
                 if (!mbar_wait(&tfull[slot], (gl / C::NSLOT) & 1, abort_flag, err, p.wait_limit_ns)) break;
-                const int nq = min(max(qp - visit_tile(gl >> 1) * QC::PAGES, 0), QC::PAGES);
+                const int nq = min(max(qp - (j_begin + (gl >> 1)) * QC::PAGES, 0), QC::PAGES);
                 uint8_t* dst = smem + C::OFF_RING + slot * C::TILE_BYTES;
-                const int qs = sidx % QC::NQS;
                 if (nq > 0) {
-                    if (!mbar_wait(&qfull[qs], (sidx / QC::NQS) & 1, abort_flag, err, p.wait_limit_ns)) break;
+                    const int qs = gl % QC::NQS;
+                    if (!mbar_wait(&qfull[qs], (gl / QC::NQS) & 1, abort_flag, err, p.wait_limit_ns)) break;
                     prefix_fill_rows<kBF16, D, BITS>(smem_u32(smem + C::OFF_QST + qs * QC::SLOT), smem_u32(dst),
                                                      gl & 1, dw, nq, lane);
                 } else if constexpr (kBF16) {
@@ -909,10 +791,9 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    if (nq > 0) mbar_arrive(&qempty[qs]);
+                    if (nq > 0) mbar_arrive(&qempty[gl % QC::NQS]);
                     mbar_arrive(&slot_full[slot]);
                 }
-                if (nq > 0) ++sidx;
             }
         }
     }

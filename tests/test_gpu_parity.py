@@ -104,12 +104,10 @@ SMALL = {
 }
 
 
-# A CTA with one live query tile and at least two key tiles splits the key
-# range between its two softmax warpgroups and merges their partial results:
-# odd and even tile counts, a one-token chunk over a long prefix, a chunk of
-# exactly one tile with no prefix (no split), one just over a tile (two
-# query tiles, no split), logits large enough that the two halves' maxima
-# differ by far more than 2^8.
+# CTAs with one live query tile over long key ranges (odd and even tile
+# counts), a one-token chunk over a long prefix, a chunk of exactly one tile
+# with no prefix, one just over a tile, and logits large enough that row
+# maxima jump by far more than 2^8 between distant tiles.
 SMALL.update({
     "key_split_g1_bf16": lambda: wl.make_random(81, [500, 1000, 0, 37], [100, 3, 128, 129], Hq=4, Hkv=4, d=128,
                                                 dtype="bf16"),
@@ -128,10 +126,9 @@ def test_small_workloads_match_oracle(name):
 
 
 @pytest.mark.parametrize("splits", [2, 3])
-def test_key_split_within_cta_combined_with_split_kv(splits):
-    """Single-tile CTAs whose key range is also cut across CTAs: each CTA's
-    share is again split between its warpgroups and merged, then the CTAs'
-    partials are merged by log-sum-exp."""
+def test_single_tile_ctas_with_split_kv(splits):
+    """Single-tile CTAs whose key range is cut across CTAs, the partials
+    merged by log-sum-exp."""
     w = wl.make_random(85, [1500, 777], [90, 40], Hq=6, Hkv=6, d=128, dtype="bf16")
     _check_step(w, prefix_splits=splits)
 
