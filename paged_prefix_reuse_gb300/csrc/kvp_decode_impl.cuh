@@ -48,51 +48,70 @@ struct DecodeCfg {
 // fp16 K and V tiles, in the chunked, swizzled layout the TMA path gives.
 // K scale/min are per channel (a lane's channels are fixed across its keys
 // when 32 is a multiple of the units per row), V's per token.  Keys at or
-// past nvalid become zeros.
+// past nvalid become zeros.  All addresses are shared-memory addresses; the
+// accesses are explicit shared loads and stores, and each half of the
+// lane's units has all its code and scale loads issued before its
+// arithmetic and stores.
 template <int D, int SK, int BITS>
-__device__ __forceinline__ void dequant_stage(const uint8_t* qs, uint8_t* stk, uint8_t* stv, int nvalid, int lane) {
+__device__ __forceinline__ void dequant_stage(uint32_t qs, uint32_t stk, uint32_t stv, int nvalid, int lane) {
     using C = DecodeCfg<D, SK, BITS>;
     constexpr int U = D / 8;            // 16-byte output units per row
     constexpr int CROW = D * BITS / 8;  // code bytes per row
-    const uint8_t* kc = qs;
-    const uint8_t* vc = qs + C::QOFF_V;
-    const __half* km = reinterpret_cast<const __half*>(qs + C::QOFF_KM);
-    const __half2* vm = reinterpret_cast<const __half2*>(qs + C::QOFF_VM);
+    constexpr int IT = SK * U / 32;     // units per lane
+    constexpr int H = IT % 2 == 0 ? IT / 2 : IT;  // units per batch of loads
+    static_assert((SK * U) % 32 == 0, "whole units per lane");
+    const uint32_t kc = qs, vc = qs + C::QOFF_V, km = qs + C::QOFF_KM, vm = qs + C::QOFF_VM;
+    constexpr bool kFixedUnit = (32 % U) == 0;
     uint32_t ks[4], kz[4];
     auto load_kmeta = [&](int u) {
-        const uint4 a = *reinterpret_cast<const uint4*>(km + u * 8);
-        const uint4 b = *reinterpret_cast<const uint4*>(km + D + u * 8);
+        const uint4 a = lds128(km + u * 16);
+        const uint4 b = lds128(km + 2 * D + u * 16);
         ks[0] = a.x; ks[1] = a.y; ks[2] = a.z; ks[3] = a.w;
         kz[0] = b.x; kz[1] = b.y; kz[2] = b.z; kz[3] = b.w;
     };
-    constexpr bool kFixedUnit = (32 % U) == 0;
     if constexpr (kFixedUnit) load_kmeta(lane % U);
-    static_assert((SK * U) % 32 == 0, "whole units per lane");
 #pragma unroll
-    for (int it = 0; it < SK * U / 32; ++it) {
-        const int e = lane + 32 * it;
-        const int key = e / U, u = e - (e / U) * U;
-        if constexpr (!kFixedUnit) load_kmeta(u);
-        uint4 ko = make_uint4(0, 0, 0, 0), vo = make_uint4(0, 0, 0, 0);
-        if (key < nvalid) {
-            ko = dequant_unit<BITS>(kc + key * CROW + u * BITS, ks, kz);
-            const __half2 sz = vm[key];  // (scale, min) of this token
-            const __half2 s = __low2half2(sz), z = __high2half2(sz);
-            const uint32_t s1 = *reinterpret_cast<const uint32_t*>(&s), z1 = *reinterpret_cast<const uint32_t*>(&z);
-            const uint32_t vs[4] = {s1, s1, s1, s1}, vz[4] = {z1, z1, z1, z1};
-            vo = dequant_unit<BITS>(vc + key * CROW + u * BITS, vs, vz);
+    for (int h0 = 0; h0 < IT; h0 += H) {
+        uint2 kw[H], vw[H];
+        uint32_t sz[H];
+#pragma unroll
+        for (int k = 0; k < H; ++k) {
+            const int e = lane + 32 * (h0 + k);
+            const int key = e / U, u = e - (e / U) * U;
+            const uint32_t off = key * CROW + u * BITS;
+            if constexpr (BITS == 8) {
+                kw[k] = lds64(kc + off);
+                vw[k] = lds64(vc + off);
+            } else {
+                kw[k] = make_uint2(lds32(kc + off), 0u);
+                vw[k] = make_uint2(lds32(vc + off), 0u);
+            }
+            sz[k] = lds32(vm + 4 * key);  // (scale, min) of this token
         }
-        const int off = (u / (C::CW / 8)) * C::REGION + swz_offset(key, u % (C::CW / 8), C::ROWB);
-        *reinterpret_cast<uint4*>(stk + off) = ko;
-        *reinterpret_cast<uint4*>(stv + off) = vo;
+#pragma unroll
+        for (int k = 0; k < H; ++k) {
+            const int e = lane + 32 * (h0 + k);
+            const int key = e / U, u = e - (e / U) * U;
+            if constexpr (!kFixedUnit) load_kmeta(u);
+            uint4 ko = make_uint4(0, 0, 0, 0), vo = make_uint4(0, 0, 0, 0);
+            if (key < nvalid) {
+                ko = dequant_words<BITS>(kw[k], ks, kz);
+                const uint32_t s1 = __byte_perm(sz[k], 0, 0x1010), z1 = __byte_perm(sz[k], 0, 0x3232);
+                const uint32_t vs[4] = {s1, s1, s1, s1}, vz[4] = {z1, z1, z1, z1};
+                vo = dequant_words<BITS>(vw[k], vs, vz);
+            }
+            const uint32_t off = (u / (C::CW / 8)) * C::REGION + swz_offset(key, u % (C::CW / 8), C::ROWB);
+            sts128(stk + off, ko);
+            sts128(stv + off, vo);
+        }
     }
 }
 
 // A 16-bit bf16 stage (the live suffix of a bf16 pool) converted to fp16 for
 // the fp16 products of the quantized-prefix kernel; keys at or past nvalid
-// become zeros.  Same swizzled layout in and out.
+// become zeros.  Same swizzled layout in and out; shared-memory addresses.
 template <int D, int SK, int BITS>
-__device__ __forceinline__ void bf16_stage_to_f16(const uint8_t* kin, const uint8_t* vin, uint8_t* stk, uint8_t* stv,
+__device__ __forceinline__ void bf16_stage_to_f16(uint32_t kin, uint32_t vin, uint32_t stk, uint32_t stv,
                                                   int nvalid, int lane) {
     using C = DecodeCfg<D, SK, BITS>;
     constexpr int U = D / 8;
@@ -100,10 +119,10 @@ __device__ __forceinline__ void bf16_stage_to_f16(const uint8_t* kin, const uint
     for (int it = 0; it < SK * U / 32; ++it) {
         const int e = lane + 32 * it;
         const int key = e / U, u = e - (e / U) * U;
-        const int off = (u / (C::CW / 8)) * C::REGION + swz_offset(key, u % (C::CW / 8), C::ROWB);
+        const uint32_t off = (u / (C::CW / 8)) * C::REGION + swz_offset(key, u % (C::CW / 8), C::ROWB);
         uint4 ko = make_uint4(0, 0, 0, 0), vo = make_uint4(0, 0, 0, 0);
         if (key < nvalid) {
-            const uint4 a = *reinterpret_cast<const uint4*>(kin + off), b = *reinterpret_cast<const uint4*>(vin + off);
+            const uint4 a = lds128(kin + off), b = lds128(vin + off);
             ko = make_uint4(pack2<false>(unpack2<true>(a.x).x, unpack2<true>(a.x).y),
                             pack2<false>(unpack2<true>(a.y).x, unpack2<true>(a.y).y),
                             pack2<false>(unpack2<true>(a.z).x, unpack2<true>(a.z).y),
@@ -113,8 +132,8 @@ __device__ __forceinline__ void bf16_stage_to_f16(const uint8_t* kin, const uint
                             pack2<false>(unpack2<true>(b.z).x, unpack2<true>(b.z).y),
                             pack2<false>(unpack2<true>(b.w).x, unpack2<true>(b.w).y));
         }
-        *reinterpret_cast<uint4*>(stk + off) = ko;
-        *reinterpret_cast<uint4*>(stv + off) = vo;
+        sts128(stk + off, ko);
+        sts128(stv + off, vo);
     }
 }
 
@@ -322,10 +341,12 @@ __global__ void __launch_bounds__(kDecodeThreads, BITS ? 4 : 5)
             if constexpr (BITS > 0) {
                 if (staged) {
                     uint8_t* stk = smem + C::OFF_STG + warp * C::STG_BYTES;
+                    const uint32_t stk_a = smem_u32(stk);
                     if (qst)
-                        dequant_stage<D, SK, BITS>(kst, stk, stk + C::KBYTES, nvalid, lane);
+                        dequant_stage<D, SK, BITS>(smem_u32(kst), stk_a, stk_a + C::KBYTES, nvalid, lane);
                     else
-                        bf16_stage_to_f16<D, SK, BITS>(kst, vst, stk, stk + C::KBYTES, nvalid, lane);
+                        bf16_stage_to_f16<D, SK, BITS>(smem_u32(kst), smem_u32(vst), stk_a, stk_a + C::KBYTES, nvalid,
+                                                       lane);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[slot]);
                     kst = stk;
