@@ -714,7 +714,8 @@ def run_decode_q(args):
             pairs.append((int(bt[b, pg]), len(pairs)))
             bt[b, pg] = len(pairs) - 1
     qp = kvp.QuantKVPool.like(pool, len(pairs), args.bits)
-    kvp.kvp_quantize_blocks(pool, qp, torch.tensor(pairs, dtype=torch.int32, device=dev))
+    tpairs = torch.tensor(pairs, dtype=torch.int32, device=dev)
+    kvp.kvp_quantize_blocks(pool, qp, tpairs)
     torch.cuda.synchronize()
     tq = torch.from_numpy(qpages).to(dev)
     tbt = torch.from_numpy(bt).to(dev)
@@ -739,6 +740,8 @@ def run_decode_q(args):
         return sorted(ts)[len(ts) // 2]
 
     mctx = int(ctx.max())
+    # the write-back of the cached pages in quantized form (one call over all pairs)
+    t_quant = timed(lambda: kvp.kvp_quantize_blocks(pool, qp, tpairs, stream=stream))
     t16 = timed(lambda: kvp.kvp_decode_attn(pool, q, ctx_d, bt16, mctx, w.softmax_scale, stream=stream))
     tqz = timed(lambda: kvp.kvp_decode_attn_q(pool, qp, tq, q, ctx_d, tbt, mctx, w.softmax_scale, stream=stream))
     npages = (ctx + bs - 1) // bs
@@ -757,6 +760,8 @@ def run_decode_q(args):
                    "quantized_pages": int(qpages.sum()), "pages_16bit": int((npages - qpages).sum()),
                    "l2": "flushed before every timed call"},
         "decode_16bit_ms": t16 * 1e3, "speedup_vs_16bit": t16 / tqz, "bytes_read": bytesq,
+        "quantize_ms": t_quant * 1e3,
+        "quantize_gbs": len(pairs) * (page16 + pageq) / t_quant / 1e9,  # 16-bit pages read + quantized written
         "bytes_read_16bit": bytes16, "gpu_launches": 1 + (1 if kvp.kvp_decode_num_splits(
             len(ctx), hkv, bs, mctx) > 1 else 0),
         "roofline": {"kernel": "decode_attn_q", "bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",

@@ -39,88 +39,160 @@ __device__ __forceinline__ uint32_t qcode(float x, float s, float z, int levels)
     return static_cast<uint32_t>(min(max(c, 0), levels));
 }
 
-// One CTA per (pair, kv head).  K: thread t handles channels 2t and 2t+1 over
-// the block's tokens; V: warp w handles tokens w, w+4, ..., its lanes the
-// channel pairs of the token.  Codes of a channel pair are stored together:
-// two bytes at 8 bits, one byte (even channel in the low nibble) at 4 bits.
-template <bool kBF16, int BITS>
+// One warp per (pair, kv head) page-head, four per CTA.  Lane l owns the
+// 16-byte unit u = l % SEG (channels 8u .. 8u+7; lanes with u >= D/8 idle)
+// of rows r0 = l / SEG, r0 + R, ... (R = 32 / SEG rows per pass), and issues
+// all its loads of K (then of V) before any arithmetic.  K: per-channel
+// minimum and maximum over the lane's rows, combined across the R lanes that
+// share the unit; V: per-row minimum and maximum over the lane's 8 channels,
+// combined across the row's lanes.  Codes and scales follow the same fp32
+// steps as before, so the result is bit-for-bit the format's.
+template <bool kBF16, int BITS, int D, int BS>
 __global__ void __launch_bounds__(kQThreads) quantize_kernel(const uint16_t* __restrict__ kp,
                                                              const uint16_t* __restrict__ vp, PoolView pool,
-                                                             QPoolView qp, const int32_t* __restrict__ pairs) {
+                                                             QPoolView qp, const int32_t* __restrict__ pairs,
+                                                             int32_t n) {
     constexpr int kLevels = (1 << BITS) - 1;
+    constexpr int U = D / 8;              // 16-byte units per row
+    constexpr int SEG = U > 8 ? 16 : 8;   // lanes per row segment
+    constexpr int R = 32 / SEG;           // rows per pass
+    constexpr int NR = BS / R;            // rows per lane
+    constexpr int CROW = D * BITS / 8;    // code bytes per row
     pdl_trigger();
     pdl_wait();
-    const int i = blockIdx.x, h = blockIdx.y;
+    const int Hkv = pool.num_kv_heads;
+    const int wg = blockIdx.x * (kQThreads / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (wg >= n * Hkv) return;
+    const int i = wg / Hkv, h = wg - (wg / Hkv) * Hkv;
     const int64_t src = __ldg(pairs + 2 * i), dst = __ldg(pairs + 2 * i + 1);
     if (src < 0 || src >= pool.num_blocks || dst < 0 || dst >= qp.num_blocks) {
-        if (threadIdx.x == 0 && h == 0) report(pool.err_word, KVP_DEVERR_BAD_PAIR);
+        if (lane == 0 && h == 0) report(pool.err_word, KVP_DEVERR_BAD_PAIR);
         return;
     }
-    const int BS = pool.block_size, D = pool.head_dim, Hkv = pool.num_kv_heads;
-    const int crow = D * BITS / 8;
     const int64_t ps = src * Hkv + h, pd = dst * Hkv + h;
-    const uint16_t* K = kp + ps * BS * D;
-    const uint16_t* V = vp + ps * BS * D;
-    uint8_t* kc = qp.k_codes + pd * BS * crow;
-    uint8_t* vc = qp.v_codes + pd * BS * crow;
+    const uint4* K = reinterpret_cast<const uint4*>(kp + ps * BS * D);
+    const uint4* V = reinterpret_cast<const uint4*>(vp + ps * BS * D);
+    uint8_t* kc = qp.k_codes + pd * BS * CROW;
+    uint8_t* vc = qp.v_codes + pd * BS * CROW;
     __half* km = qp.k_meta + pd * 2 * D;
     __half* vm = qp.v_meta + pd * BS * 2;
     uint32_t* err = pool.err_word;
+    const int u = lane % SEG, r0 = lane / SEG;
+    const bool act = u < U;
 
-    for (int c2 = threadIdx.x; c2 < D / 2; c2 += kQThreads) {
-        float mn0 = INFINITY, mx0 = -INFINITY, mn1 = INFINITY, mx1 = -INFINITY;
-        for (int t = 0; t < BS; ++t) {
-            const float2 x = unpack2<kBF16>(*reinterpret_cast<const uint32_t*>(K + t * D + 2 * c2));
-            mn0 = fminf(mn0, x.x);
-            mx0 = fmaxf(mx0, x.x);
-            mn1 = fminf(mn1, x.y);
-            mx1 = fmaxf(mx1, x.y);
+    // Eight codes of one unit, stored as 8 bytes (8 bits) or 4 (4 bits, the
+    // even channel in the low nibble).
+    auto store_codes = [&](uint8_t* row, const uint32_t (&c)[8]) {
+        if constexpr (BITS == 8) {
+            *reinterpret_cast<uint2*>(row + 8 * u) =
+                make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24), c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
+        } else {
+            *reinterpret_cast<uint32_t*>(row + 4 * u) = c[0] | (c[1] << 4) | (c[2] << 8) | (c[3] << 12) | (c[4] << 16) |
+                                                        (c[5] << 20) | (c[6] << 24) | (c[7] << 28);
         }
-        __half sh0, zh0, sh1, zh1;
-        float s0, z0, s1, z1;
-        group_params(mn0, mx0, static_cast<float>(kLevels), sh0, zh0, s0, z0, err);
-        group_params(mn1, mx1, static_cast<float>(kLevels), sh1, zh1, s1, z1, err);
-        km[2 * c2] = sh0;
-        km[2 * c2 + 1] = sh1;
-        km[D + 2 * c2] = zh0;
-        km[D + 2 * c2 + 1] = zh1;
-        for (int t = 0; t < BS; ++t) {
-            const float2 x = unpack2<kBF16>(*reinterpret_cast<const uint32_t*>(K + t * D + 2 * c2));
-            const uint32_t a = qcode(x.x, s0, z0, kLevels), b = qcode(x.y, s1, z1, kLevels);
-            if constexpr (BITS == 8)
-                *reinterpret_cast<uint16_t*>(kc + t * crow + 2 * c2) = static_cast<uint16_t>(a | (b << 8));
-            else
-                kc[t * crow + c2] = static_cast<uint8_t>(a | (b << 4));
-        }
-    }
+    };
+    auto unpack8 = [&](uint4 a, float (&x)[8]) {
+        const float2 p0 = unpack2<kBF16>(a.x), p1 = unpack2<kBF16>(a.y), p2 = unpack2<kBF16>(a.z),
+                     p3 = unpack2<kBF16>(a.w);
+        x[0] = p0.x; x[1] = p0.y; x[2] = p1.x; x[3] = p1.y; x[4] = p2.x; x[5] = p2.y; x[6] = p3.x; x[7] = p3.y;
+    };
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int t = warp; t < BS; t += kQThreads / 32) {
-        float mn = INFINITY, mx = -INFINITY;
-        for (int c2 = lane; c2 < D / 2; c2 += 32) {
-            const float2 x = unpack2<kBF16>(*reinterpret_cast<const uint32_t*>(V + t * D + 2 * c2));
-            mn = fminf(mn, fminf(x.x, x.y));
-            mx = fmaxf(mx, fmaxf(x.x, x.y));
+    // ---- K: per channel over the page's tokens ----
+    {
+        uint4 w[NR];
+#pragma unroll
+        for (int k = 0; k < NR; ++k) w[k] = act ? __ldg(K + (r0 + R * k) * U + u) : make_uint4(0, 0, 0, 0);
+        float mn[8], mx[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            mn[c] = INFINITY;
+            mx[c] = -INFINITY;
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        for (int k = 0; k < NR; ++k) {
+            float x[8];
+            unpack8(w[k], x);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                mn[c] = fminf(mn[c], x[c]);
+                mx[c] = fmaxf(mx[c], x[c]);
+            }
         }
-        __half sh, zh;
-        float s, z;
-        group_params(mn, mx, static_cast<float>(kLevels), sh, zh, s, z, lane == 0 ? err : nullptr);
-        if (lane == 0) {
-            vm[2 * t] = sh;
-            vm[2 * t + 1] = zh;
+#pragma unroll
+        for (int o = SEG; o < 32; o <<= 1) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                mn[c] = fminf(mn[c], __shfl_xor_sync(0xffffffffu, mn[c], o));
+                mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], o));
+            }
         }
-        for (int c2 = lane; c2 < D / 2; c2 += 32) {
-            const float2 x = unpack2<kBF16>(*reinterpret_cast<const uint32_t*>(V + t * D + 2 * c2));
-            const uint32_t a = qcode(x.x, s, z, kLevels), b = qcode(x.y, s, z, kLevels);
-            if constexpr (BITS == 8)
-                *reinterpret_cast<uint16_t*>(vc + t * crow + 2 * c2) = static_cast<uint16_t>(a | (b << 8));
-            else
-                vc[t * crow + c2] = static_cast<uint8_t>(a | (b << 4));
+        if (act) {
+            float s[8], z[8];
+            __half sh[8], zh[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                group_params(mn[c], mx[c], static_cast<float>(kLevels), sh[c], zh[c], s[c], z[c],
+                             r0 == 0 ? err : nullptr);
+            if (r0 == 0) {
+                auto pack_h = [](const __half (&a)[8]) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        w[j] = static_cast<uint32_t>(__half_as_ushort(a[2 * j])) |
+                               (static_cast<uint32_t>(__half_as_ushort(a[2 * j + 1])) << 16);
+                    return make_uint4(w[0], w[1], w[2], w[3]);
+                };
+                *reinterpret_cast<uint4*>(km + 8 * u) = pack_h(sh);
+                *reinterpret_cast<uint4*>(km + D + 8 * u) = pack_h(zh);
+            }
+#pragma unroll
+            for (int k = 0; k < NR; ++k) {
+                float x[8];
+                unpack8(w[k], x);
+                uint32_t c8[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) c8[c] = qcode(x[c], s[c], z[c], kLevels);
+                store_codes(kc + (r0 + R * k) * CROW, c8);
+            }
+        }
+    }
+    // ---- V: per token over the channels ----
+    {
+        uint4 w[NR];
+#pragma unroll
+        for (int k = 0; k < NR; ++k) w[k] = act ? __ldg(V + (r0 + R * k) * U + u) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int k = 0; k < NR; ++k) {
+            float x[8];
+            unpack8(w[k], x);
+            float mn = INFINITY, mx = -INFINITY;
+            if (act) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    mn = fminf(mn, x[c]);
+                    mx = fmaxf(mx, x[c]);
+                }
+            }
+#pragma unroll
+            for (int o = 1; o < SEG; o <<= 1) {
+                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            }
+            const int t = r0 + R * k;
+            __half sh, zh;
+            float s, z;
+            group_params(mn, mx, static_cast<float>(kLevels), sh, zh, s, z, u == 0 ? err : nullptr);
+            if (u == 0) {
+                vm[2 * t] = sh;
+                vm[2 * t + 1] = zh;
+            }
+            if (act) {
+                uint32_t c8[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) c8[c] = qcode(x[c], s, z, kLevels);
+                store_codes(vc + t * CROW, c8);
+            }
         }
     }
 }
@@ -132,20 +204,43 @@ cudaError_t launch_decode_q_d(const DecodeParams& p, const CUtensorMap& tk, cons
                              : launch_decode_kernel<kBF16, D, 16, 4>(p, tk, tv, stream);
 }
 
+template <bool kBF16, int BITS, int D>
+cudaError_t launch_quantize_d(const PoolView& pool, const uint16_t* k, const uint16_t* v, const QPoolView& qpool,
+                              const int32_t* pairs, int32_t n, cudaStream_t stream) {
+    const int64_t warps = static_cast<int64_t>(n) * pool.num_kv_heads;
+    const dim3 grid(static_cast<unsigned>((warps + kQThreads / 32 - 1) / (kQThreads / 32)));
+    switch (pool.block_size) {
+        case 8: return launch_k(quantize_kernel<kBF16, BITS, D, 8>, grid, kQThreads, 0, stream, k, v, pool, qpool, pairs, n);
+        case 16: return launch_k(quantize_kernel<kBF16, BITS, D, 16>, grid, kQThreads, 0, stream, k, v, pool, qpool, pairs, n);
+        case 32: return launch_k(quantize_kernel<kBF16, BITS, D, 32>, grid, kQThreads, 0, stream, k, v, pool, qpool, pairs, n);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <bool kBF16, int BITS>
+cudaError_t launch_quantize_b(const PoolView& pool, const uint16_t* k, const uint16_t* v, const QPoolView& qpool,
+                              const int32_t* pairs, int32_t n, cudaStream_t stream) {
+    switch (pool.head_dim) {
+        case 64: return launch_quantize_d<kBF16, BITS, 64>(pool, k, v, qpool, pairs, n, stream);
+        case 96: return launch_quantize_d<kBF16, BITS, 96>(pool, k, v, qpool, pairs, n, stream);
+        case 128: return launch_quantize_d<kBF16, BITS, 128>(pool, k, v, qpool, pairs, n, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_quantize_blocks(const PoolView& pool, const void* k_pool, const void* v_pool,
                                    const QPoolView& qpool, const int32_t* pairs, int32_t n, cudaStream_t stream) {
     if (n <= 0) return cudaSuccess;
-    const dim3 grid(n, pool.num_kv_heads);
     const uint16_t* k = static_cast<const uint16_t*>(k_pool);
     const uint16_t* v = static_cast<const uint16_t*>(v_pool);
     const bool bf = pool.dtype == KVP_BF16;
     if (qpool.bits == 8)
-        return bf ? launch_k(quantize_kernel<true, 8>, grid, kQThreads, 0, stream, k, v, pool, qpool, pairs)
-                  : launch_k(quantize_kernel<false, 8>, grid, kQThreads, 0, stream, k, v, pool, qpool, pairs);
-    return bf ? launch_k(quantize_kernel<true, 4>, grid, kQThreads, 0, stream, k, v, pool, qpool, pairs)
-              : launch_k(quantize_kernel<false, 4>, grid, kQThreads, 0, stream, k, v, pool, qpool, pairs);
+        return bf ? launch_quantize_b<true, 8>(pool, k, v, qpool, pairs, n, stream)
+                  : launch_quantize_b<false, 8>(pool, k, v, qpool, pairs, n, stream);
+    return bf ? launch_quantize_b<true, 4>(pool, k, v, qpool, pairs, n, stream)
+              : launch_quantize_b<false, 4>(pool, k, v, qpool, pairs, n, stream);
 }
 
 cudaError_t launch_decode_attn_q(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
