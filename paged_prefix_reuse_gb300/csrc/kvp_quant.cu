@@ -33,9 +33,23 @@ __device__ __forceinline__ void group_params(float mn, float mx, float levels, _
 
 // code = clamp(round_half_even((x - z) / s), 0, levels), each step one fp32
 // operation; a zero scale (constant group) gives code 0.
-__device__ __forceinline__ uint32_t qcode(float x, float s, float z, int levels) {
+// Computed without a division in the common case.  With r = 1/s
+// (correctly rounded), q' = (x - z) * r is within |q| * 1.8e-7 of the
+// correctly rounded quotient q = (x - z) / s: within 1e-4 for |q'| < 512.
+// So when q' lies farther than 1e-4 from a half-integer, q and q' round to
+// the same integer; when |q'| >= 512 both lie far outside [0, levels] and
+// clamp alike.  Otherwise (and for a NaN) the exact division decides, so the
+// result always equals that of the division.
+__device__ __forceinline__ uint32_t qcode_fast(float x, float s, float z, float r, int levels) {
     if (!(s > 0.f)) return 0u;
-    const int c = __float2int_rn(__fdiv_rn(__fsub_rn(x, z), s));
+    const float d = __fsub_rn(x, z);
+    const float q = __fmul_rn(d, r);
+    const float f = fabsf(q - rintf(q));
+    int c;
+    if (f < 0.4999f || fabsf(q) >= 512.f)
+        c = __float2int_rn(q);
+    else
+        c = __float2int_rn(__fdiv_rn(d, s));
     return static_cast<uint32_t>(min(max(c, 0), levels));
 }
 
@@ -146,13 +160,16 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const uint16_t* __r
                 *reinterpret_cast<uint4*>(km + 8 * u) = pack_h(sh);
                 *reinterpret_cast<uint4*>(km + D + 8 * u) = pack_h(zh);
             }
+            float rs[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) rs[c] = s[c] > 0.f ? __frcp_rn(s[c]) : 0.f;
 #pragma unroll
             for (int k = 0; k < NR; ++k) {
                 float x[8];
                 unpack8(w[k], x);
                 uint32_t c8[8];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) c8[c] = qcode(x[c], s[c], z[c], kLevels);
+                for (int c = 0; c < 8; ++c) c8[c] = qcode_fast(x[c], s[c], z[c], rs[c], kLevels);
                 store_codes(kc + (r0 + R * k) * CROW, c8);
             }
         }
@@ -188,9 +205,10 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const uint16_t* __r
                 vm[2 * t + 1] = zh;
             }
             if (act) {
+                const float r = s > 0.f ? __frcp_rn(s) : 0.f;
                 uint32_t c8[8];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) c8[c] = qcode(x[c], s, z, kLevels);
+                for (int c = 0; c < 8; ++c) c8[c] = qcode_fast(x[c], s, z, r, kLevels);
                 store_codes(vc + t * CROW, c8);
             }
         }

@@ -320,3 +320,40 @@ def test_quantized_prefill_bad_quantized_block_is_flagged():
                                      torch.from_numpy(bt).cuda(), st.max_q_pf, st.max_ctx_pf, w.softmax_scale)
     torch.cuda.synchronize()
     assert st.pool.errors() & kvp.DEVERR["bad_block"]
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quantize_codes_at_half_step_boundaries_match_oracle(bits):
+    """Values placed half a quantization step apart, so that (x - z) / s lands
+    within rounding distance of half-integers: the kernel's division-free
+    code must still equal the correctly rounded division of the format."""
+    import paged_prefix_reuse_gb300 as kvp
+
+    rng = np.random.default_rng(300 + bits)
+    nb, Hkv, bs, d = 24, 2, 16, 128
+    levels = (1 << bits) - 1
+    lo = rng.uniform(-3, 0, size=(nb, Hkv, 1, d)).astype(np.float32)
+    step = rng.uniform(0.001, 0.05, size=(nb, Hkv, 1, d)).astype(np.float32)
+    k = rng.integers(0, levels, size=(nb, Hkv, bs, d)).astype(np.float32)
+    K = lo + (k + 0.5) * step
+    K[:, :, 0] = lo[:, :, 0]                 # the group's minimum
+    K[:, :, 1] = lo[:, :, 0] + levels * step[:, :, 0]  # and maximum
+    Vlo = rng.uniform(-2, 0, size=(nb, Hkv, bs, 1)).astype(np.float32)
+    Vst = rng.uniform(0.001, 0.05, size=(nb, Hkv, bs, 1)).astype(np.float32)
+    V = Vlo + (rng.integers(0, levels, size=(nb, Hkv, bs, d)) + 0.5) * Vst
+    V[..., 0:1] = Vlo
+    V[..., 1:2] = Vlo + levels * Vst
+    for dtype in ("f16", "bf16"):
+        kb, vb = wl.round_to_bits(K, dtype), wl.round_to_bits(V.astype(np.float32), dtype)
+        tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+        pool = kvp.PagedKVPool(torch.from_numpy(kb.view(np.int16)).view(tdt).cuda(),
+                               torch.from_numpy(vb.view(np.int16)).view(tdt).cuda())
+        qp = kvp.QuantKVPool.like(pool, nb, bits)
+        pairs = np.stack([np.arange(nb), rng.permutation(nb)], 1).astype(np.int32)
+        kvp.kvp_quantize_blocks(pool, qp, torch.from_numpy(pairs).cuda())
+        torch.cuda.synchronize()
+        assert pool.errors() == 0
+        want, _ = quant.quantize_blocks(dtype, kb, vb, quant.empty_qpool(nb, Hkv, bs, d, bits), bits, pairs)
+        got = _qarrays(qp)
+        for a, b in zip(got, want):
+            np.testing.assert_array_equal(a.astype(np.float32), b.astype(np.float32))
