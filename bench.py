@@ -116,9 +116,12 @@ def _peak_value(peaks, *keys):
 # (own block tables, Q and O), so its traffic is four times B=1's.
 TRAFFIC_PROXY = {"long_context_prefix": ("long_context_prefix_b1", 4.0)}
 # The source files a kernel's code comes from (besides kvp_internal.cuh).
-KERNEL_SOURCES = {"prefix": ["kvp_prefix.cu"], "decode": ["kvp_decode.cu", "kvp_decode_impl.cuh"],
-                  "decode_q_int8": ["kvp_quant.cu", "kvp_decode_impl.cuh"], "deviation": ["kvp_cacheblend.cu"],
-                  "block_swap": ["kvp_cache.cu"]}
+KERNEL_SOURCES = {"prefix": ["kvp_prefix.cu", "kvp_prefix_impl.cuh"], "decode": ["kvp_decode.cu", "kvp_decode_impl.cuh"],
+                  "decode_q_int8": ["kvp_quant.cu", "kvp_decode_impl.cuh"],
+                  "decode_q_int4": ["kvp_quant.cu", "kvp_decode_impl.cuh"],
+                  "prefix_q_int8": ["kvp_prefix_q.cu", "kvp_prefix_impl.cuh"],
+                  "prefix_q_int4": ["kvp_prefix_q.cu", "kvp_prefix_impl.cuh"], "deviation": ["kvp_cacheblend.cu"],
+                  "block_swap": ["kvp_cache.cu"], "append": ["kvp_cache.cu"]}
 
 
 def committed_traffic(kernel: str, workload: str):
@@ -766,8 +769,8 @@ def run_decode_q(args):
             len(ctx), hkv, bs, mctx) > 1 else 0),
         "roofline": {"kernel": "decode_attn_q", "bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
                      "frac": gbs / hbm, "peak_source": f"{peak_src} HBM copy",
-                     "traffic": committed_traffic("decode_q_int8", "continuous_batching_step_int8_prefix")
-                     if args.bits == 8 else None},
+                     "traffic": committed_traffic(f"decode_q_int{args.bits}",
+                                                  f"continuous_batching_step_int{args.bits}_prefix")},
     }
     print(json.dumps(line), flush=True)
     return 0
