@@ -123,6 +123,21 @@ struct PrefixCfg {
     static_assert(256 + 2 * D <= (int)kTmemCols, "tensor memory");
 };
 
+// Named barrier `id` over the 128 threads of a warpgroup that also returns,
+// to every one of them, whether v held in all of them (bar.red.and).
+__device__ __forceinline__ bool warpgroup_all(int id, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id)
+        : "memory");
+    return r != 0;
+}
+
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     const uint32_t a = smem_u32(p);
     return p + (((a + 1023u) & ~1023u) - a);
@@ -485,6 +500,10 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
 
             // ------------------------------ epilogue ------------------------------
             if (ok) ok = mbar_wait(&o_done[wg], 0, abort_flag, err, p.wait_limit_ns);
+            // Make the outcome uniform over the warpgroup before its named
+            // barrier below (which cannot time out): every warp passes this one,
+            // which returns the AND over the warpgroup of "no wait gave up".
+            ok = warpgroup_all(wg + 1, ok && !*abort_flag);
             if (ok) {
                 tc_fence_after();
                 const float inv = l > 0.f ? 1.f / l : 0.f;
