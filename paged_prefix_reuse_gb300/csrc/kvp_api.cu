@@ -302,6 +302,7 @@ static kvp_status prefix_common(const kvp_pool* pool, const kvp_qpool* qpool, co
     p.total_q = total_q;
     p.num_q_heads = num_q_heads;
     p.group = g;
+    p.group_mul = ((uint64_t(1) << 32) + g - 1) / g;
     p.q_tiles = static_cast<int32_t>(q_tiles);
     p.num_splits = splits;
     p.wait_limit_ns = wait_limit_ns();

@@ -69,7 +69,8 @@ struct PrefixParams {
     const int32_t* context_lens;
     const int32_t* block_tables;
     int32_t max_blocks, B, total_q, num_q_heads, group;  // group = Hq / Hkv
-    int32_t q_tiles;                                    // CTA row tiles per (sequence, kv head)
+    uint64_t group_mul;  // ceil(2^32 / group): n / group = (n * group_mul) >> 32 for n < 2^24
+    int32_t q_tiles;     // CTA row tiles per (sequence, kv head)
     int32_t num_splits;
     float scale_log2;  // softmax_scale * log2(e)
     float* ws_o;       // [total_q * Hq][num_splits][head_dim] fp32 (splits > 1)

@@ -187,6 +187,28 @@ __device__ __forceinline__ void tmem_ld16_sync(uint32_t taddr, uint32_t (&r)[16]
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Row rg of a (sequence, kv head) problem is (token rg / g, query head h g +
+// rg % g); the quotient by multiply-shift, exact for rg < 2^24 (checked).
+__device__ __forceinline__ int64_t out_row(const PrefixParams& p, int cu0, int h, int rg) {
+    const int t = static_cast<int>((static_cast<uint64_t>(static_cast<uint32_t>(rg)) * p.group_mul) >> 32);
+    return static_cast<int64_t>(cu0 + t) * p.num_q_heads + h * p.group + (rg - t * p.group);
+}
+
 // Eight bf16 values -> eight fp16 values (round to nearest).
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 a) {
     const float2 x = unpack2<true>(a.x), y = unpack2<true>(a.y), z = unpack2<true>(a.z), w = unpack2<true>(a.w);
@@ -298,11 +320,17 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
     pdl_trigger();
     const int split = blockIdx.x % p.num_splits;
     const int ct = p.q_tiles - 1 - static_cast<int>(blockIdx.x) / p.num_splits;  // heavy tiles first
-    const int h = blockIdx.y, s = blockIdx.z;
+    // Head-major order: the CTAs of all sequences of one kv head run together,
+    // so K/V blocks that several sequences share are re-read from L2.
+    const int s = blockIdx.y, h = blockIdx.z;
     const int g = p.group, BS = p.pool.block_size, Hkv = p.pool.num_kv_heads;
     uint32_t* err = p.pool.err_word;
 
-    // All three metadata loads before the first branch: one memory round trip.
+    // The metadata loads, and the producer's first 32 block-table entries
+    // (the key range of split 0 starts at page 0), in one memory round trip.
+    const int pre_blk = (warp == kProducerWarp && split == 0)
+                            ? __ldg(p.block_tables + static_cast<int64_t>(s) * p.max_blocks + min(lane, p.max_blocks - 1))
+                            : 0;
     const int cu0 = __ldg(p.cu_seqlens_q + s);
     const int cu1 = __ldg(p.cu_seqlens_q + s + 1);
     const int L = __ldg(p.context_lens + s);
@@ -317,7 +345,7 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
     const int P = L - N;
     const int npages = (L + BS - 1) / BS;
     const int qp = min(max(qp_raw, 0), npages);  // pages read from the quantized pool
-    if (P < 0 || npages > p.max_blocks) {
+    if (P < 0 || npages > p.max_blocks || rows_total >= (1 << 24)) {
         if (tid == 0 && split == 0) report(err, KVP_DEVERR_BAD_LEN);
         pdl_wait();
         return;
@@ -340,6 +368,25 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
             for (int c = 0; c < D; ++c) p.ws_o[(wrow * p.num_splits + split) * D + c] = 0.f;
         }
         return;
+    }
+
+    // Softmax warps: issue the global loads of their Q tile now, so their
+    // latency overlaps the barrier initialisation and the TMEM allocation.
+    constexpr int V16 = D / 8;
+    const int wg = warp >> 2;
+    const int row = tid & (kBM - 1);
+    const bool q_mine = warp < kSoftmaxWarps && (wg == 0 || has1);
+    uint4 qv[V16];
+    if (q_mine) {
+        const uint4* q4 = static_cast<const uint4*>(p.q);
+#pragma unroll
+        for (int k = 0; k < V16; ++k) {
+            const int e = row + k * kBM;
+            const int rr = e / V16, c16 = e % V16;
+            const int rgl = r0 + wg * kBM + rr;
+            qv[k] = make_uint4(0, 0, 0, 0);
+            if (rgl < rows_total) qv[k] = __ldg(q4 + out_row(p, cu0, h, rgl) * V16 + c16);
+        }
     }
 
     if (tid == 0) {
@@ -373,41 +420,24 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
 
     if (warp < kSoftmaxWarps) {
         // =========================== softmax warpgroups ===========================
-        const int wg = warp >> 2;
-        if (wg == 0 || has1) {
-            const int row = tid & (kBM - 1);
+        if (q_mine) {
             const int rg = r0 + wg * kBM + row;
             const bool valid = rg < rows_total;
-            const int token = valid ? rg / g : 0;
-            const int head = h * g + (valid ? rg % g : 0);
+            const int tq = static_cast<int>((static_cast<uint64_t>(static_cast<uint32_t>(rg)) * p.group_mul) >> 32);
+            const int token = valid ? tq : 0;
+            const int head = h * g + (valid ? rg - tq * g : 0);
             const int qpos = valid ? P + token : L - 1;
 
-            {  // Q tile wg -> swizzled shared memory (K-major A operand)
-                // All of this thread's 16-byte loads are issued before any store,
-                // so their latencies overlap instead of adding up.
-                constexpr int V16 = D / 8;
-                const uint4* q4 = static_cast<const uint4*>(p.q);
+            {  // Q tile wg (loaded above) -> swizzled shared memory (K-major A operand)
                 uint8_t* qt = smem + C::OFF_Q + wg * C::TILE_BYTES;
-                uint4 qv[V16];
-#pragma unroll
-                for (int k = 0; k < V16; ++k) {
-                    const int e = row + k * kBM;
-                    const int rr = e / V16, c16 = e % V16;
-                    const int rgl = r0 + wg * kBM + rr;
-                    qv[k] = make_uint4(0, 0, 0, 0);
-                    if (rgl < rows_total) {
-                        const int64_t qrow =
-                            static_cast<int64_t>(cu0 + rgl / g) * p.num_q_heads + h * g + rgl % g;
-                        qv[k] = __ldg(q4 + qrow * V16 + c16);
-                        if constexpr (kMma != kBF16) qv[k] = bf16x8_to_f16x8(qv[k]);
-                    }
-                }
 #pragma unroll
                 for (int k = 0; k < V16; ++k) {
                     const int e = row + k * kBM;
                     const int rr = e / V16, c16 = e % V16;
                     const int ch = c16 / (C::CW / 8), ci = c16 % (C::CW / 8);
-                    *reinterpret_cast<uint4*>(qt + ch * C::CHUNK_BYTES + swz_offset(rr, ci, C::ROWB)) = qv[k];
+                    uint4 v = qv[k];
+                    if constexpr (kMma != kBF16) v = bf16x8_to_f16x8(v);
+                    *reinterpret_cast<uint4*>(qt + ch * C::CHUNK_BYTES + swz_offset(rr, ci, C::ROWB)) = v;
                 }
 #pragma unroll
                 for (int c16 = V16; c16 < DP / 8; ++c16) {  // padded columns of this thread's row: zeros
@@ -514,23 +544,20 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
                     // last S_wg that read it has completed), then write whole rows
                     // with coalesced 16-byte stores.  Row rr's 16-byte chunk c
                     // sits at chunk position (c + rr) % (d/8) to spread banks.
-                    constexpr int V16 = D / 8;
                     uint4* stg = reinterpret_cast<uint4*>(smem + C::OFF_Q + wg * C::TILE_BYTES);
 #pragma unroll 1
-                    for (int cb = 0; cb < D / 16; ++cb) {
-                        uint32_t r[16];
-                        tmem_ld16_sync(lane_base + ocol + 16 * cb, r);
-                        uint4 a0, a1;
-                        a0.x = pack2<kBF16>(__uint_as_float(r[0]) * inv, __uint_as_float(r[1]) * inv);
-                        a0.y = pack2<kBF16>(__uint_as_float(r[2]) * inv, __uint_as_float(r[3]) * inv);
-                        a0.z = pack2<kBF16>(__uint_as_float(r[4]) * inv, __uint_as_float(r[5]) * inv);
-                        a0.w = pack2<kBF16>(__uint_as_float(r[6]) * inv, __uint_as_float(r[7]) * inv);
-                        a1.x = pack2<kBF16>(__uint_as_float(r[8]) * inv, __uint_as_float(r[9]) * inv);
-                        a1.y = pack2<kBF16>(__uint_as_float(r[10]) * inv, __uint_as_float(r[11]) * inv);
-                        a1.z = pack2<kBF16>(__uint_as_float(r[12]) * inv, __uint_as_float(r[13]) * inv);
-                        a1.w = pack2<kBF16>(__uint_as_float(r[14]) * inv, __uint_as_float(r[15]) * inv);
-                        stg[row * V16 + (2 * cb + row) % V16] = a0;
-                        stg[row * V16 + (2 * cb + 1 + row) % V16] = a1;
+                    for (int cb = 0; cb < D / 32; ++cb) {
+                        uint32_t r[32];
+                        tmem_ld32_sync(lane_base + ocol + 32 * cb, r);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            uint4 a;
+                            a.x = pack2<kBF16>(__uint_as_float(r[8 * u]) * inv, __uint_as_float(r[8 * u + 1]) * inv);
+                            a.y = pack2<kBF16>(__uint_as_float(r[8 * u + 2]) * inv, __uint_as_float(r[8 * u + 3]) * inv);
+                            a.z = pack2<kBF16>(__uint_as_float(r[8 * u + 4]) * inv, __uint_as_float(r[8 * u + 5]) * inv);
+                            a.w = pack2<kBF16>(__uint_as_float(r[8 * u + 6]) * inv, __uint_as_float(r[8 * u + 7]) * inv);
+                            stg[row * V16 + (4 * cb + u + row) % V16] = a;
+                        }
                     }
                     if (valid && p.lse)
                         p.lse[static_cast<int64_t>(head) * p.total_q + cu0 + token] = lse2 * 0.69314718055994531f;
@@ -539,16 +566,15 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
                         asm volatile("bar.sync 1, 128;" ::: "memory");
                     else
                         asm volatile("bar.sync 2, 128;" ::: "memory");
-                    uint8_t* out_b = static_cast<uint8_t*>(p.out);
-#pragma unroll 1
+                    // Thread i writes 16-byte chunk (e % (d/8)) of row e / (d/8) for
+                    // e = i + 128 k; unrolled by five so that several chunks are
+                    // in flight at once.
+                    uint4* out4 = static_cast<uint4*>(p.out);
+#pragma unroll 5
                     for (int e = row; e < kBM * V16; e += kBM) {
                         const int rr = e / V16, c = e % V16;
                         const int rgl = r0 + wg * kBM + rr;
-                        if (rgl < rows_total) {
-                            const int64_t grow =
-                                static_cast<int64_t>(cu0 + rgl / g) * p.num_q_heads + h * g + rgl % g;
-                            reinterpret_cast<uint4*>(out_b + grow * D * 2)[c] = stg[rr * V16 + (c + rr) % V16];
-                        }
+                        if (rgl < rows_total) out4[out_row(p, cu0, h, rgl) * V16 + c] = stg[rr * V16 + (c + rr) % V16];
                     }
                 } else {
                     float* dst = p.ws_o + (orow * p.num_splits + split) * D;
@@ -577,13 +603,16 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
         const int pages_per_tile = kBN / BS;  // 4, 8 or 16: a tile never straddles a 32-page batch
         const int page_first = j_begin * pages_per_tile;
         const int32_t* table = p.block_tables + static_cast<int64_t>(s) * p.max_blocks;
+        const int32_t pool_rows = static_cast<int32_t>(p.pool.num_blocks) * Hkv * BS;  // < 2^31 (host check)
         // Lane i holds the block id of page (batch * 32 + i); the next batch is
         // requested 32 pages ahead so its latency hides behind the tiles in flight.
         auto load_batch = [&](int batch) -> int {
             const int pg = min(page_first + batch * 32 + lane, npages - 1);
             return __ldg(table + pg);
         };
-        int blk_cur = load_batch(0);
+        // Split 0's first batch was loaded with the metadata; clamp it the
+        // same way (pages past the context repeat the last page).
+        int blk_cur = page_first == 0 ? __shfl_sync(0xffffffffu, pre_blk, min(lane, npages - 1)) : load_batch(0);
         int blk_nxt = load_batch(1);
         pdl_wait();  // pool contents from the kernel before (the append) are read from here on
         int loads = 0;   // ring loads issued: K_j is load 2j, V_j is load 2j+1
@@ -606,7 +635,9 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
             // One lane per physical page issues that page's boxes: TMA issue from
             // a single thread is serial, so spread it over the pages of the tile.
             const int blk_q = __shfl_sync(0xffffffffu, my_blk, ((rel & 31) + lane) & 31);
-            const int32_t y = (blk_q * Hkv + h) * BS;
+            // A page past the context is fetched as a box below the last row of
+            // the pool tensor: TMA fills it with zeros and reads no memory.
+            const int32_t y = page_first + rel + lane < npages ? (blk_q * Hkv + h) * BS : pool_rows;
             // Quantized pages of this tile: its first nq pages (BITS > 0: 16-token pages).
             const int nq = BITS ? min(max(qp - (page_first + rel), 0), pages_per_tile) : 0;
             for (int kv = 0; kv < 2; ++kv) {
@@ -741,19 +772,16 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
             const bool more = jj + 1 < n_local;
             if (!wait_slot(gv)) { ok = false; break; }
             const int nvalid = L - (j_begin + jj) * kBN;
-            if (nvalid < kBN) {
-                // Rows past the context may hold any bytes (even NaN); P is 0
-                // there, but 0 * NaN is NaN, so clear those V rows.
+            if (nvalid < kBN && nvalid % BS != 0) {
+                // Rows of the last page past the context may hold any bytes
+                // (even NaN); P is 0 there, but 0 * NaN is NaN, so clear those V
+                // rows.  Whole pages past the context arrived as zeros.
                 uint8_t* vt = smem + C::OFF_RING + (gv % C::NSLOT) * C::TILE_BYTES;
-                const int first = max(nvalid, 0);
-                const int per_row = C::ROWB / 16;
-                const int nvec = (kBN - first) * per_row * C::NCH;
-                for (int e = lane; e < nvec; e += 32) {
-                    const int c = e / ((kBN - first) * per_row);
-                    const int rem = e - c * (kBN - first) * per_row;
-                    *reinterpret_cast<uint4*>(vt + c * C::CHUNK_BYTES + (first + rem / per_row) * C::ROWB +
-                                              (rem % per_row) * 16) = make_uint4(0, 0, 0, 0);
-                }
+                const int first = nvalid;
+                const int nbytes = (BS - nvalid % BS) * C::ROWB;  // contiguous in each chunk column
+                for (int c = 0; c < C::NCH; ++c)
+                    for (int o = 16 * lane; o < nbytes; o += 16 * 32)
+                        *reinterpret_cast<uint4*>(vt + c * C::CHUNK_BYTES + first * C::ROWB + o) = make_uint4(0, 0, 0, 0);
                 fence_proxy_async_smem();
                 __syncwarp();
             }
@@ -837,7 +865,7 @@ cudaError_t launch_prefix_t(const PrefixParams& p, const CUtensorMap& tk, const 
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    dim3 grid(p.q_tiles * p.num_splits, p.pool.num_kv_heads, p.B);
+    dim3 grid(p.q_tiles * p.num_splits, p.B, p.pool.num_kv_heads);
     return launch_k(prefix_kernel<kBF16, D, BITS>, grid, prefix_threads(BITS), C::SMEM_BYTES, stream, tk, tv, p);
 }
 
