@@ -184,9 +184,10 @@ cudaError_t launch_cache_append(const PoolView& pool, void* k_pool, void* v_pool
     const int32_t vpt = pool.num_kv_heads * (pool.head_dim / 8);
     const int32_t tpb = vpt >= kThreads ? 1 : kThreads / vpt;
     const int64_t steps = (static_cast<int64_t>(T) + tpb - 1) / tpb;
-    // One step per block when there are few; a block loops (kUnroll steps per
-    // pass) only once the steps outnumber the blocks the GPU holds.
-    return launch_k(append_kernel, grid_for(steps, 1), kThreads, 0, stream, pool, static_cast<uint4*>(k_pool),
+    // kUnroll steps per block, so that every thread has kUnroll tokens' rows
+    // in flight; a block loops only once the steps outnumber the blocks the
+    // GPU holds.
+    return launch_k(append_kernel, grid_for(steps, kUnroll), kThreads, 0, stream, pool, static_cast<uint4*>(k_pool),
                     static_cast<uint4*>(v_pool), static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
                     slot_mapping, T, vpt, tpb);
 }

@@ -7,14 +7,17 @@
 // byte (g = query heads per kv head), so it is HBM-bound.  Design:
 //  * one CTA per (key range, kv head, sequence); the g query heads of the
 //    group share each loaded page;
-//  * a producer warp streams 32-key stages (K and V page-heads of one or more
-//    physical blocks, addressed through the block table) with 2-D TMA loads
-//    into a ring of 96 KB of shared memory, swizzled so that the consumers'
-//    ldmatrix reads are conflict-free;
-//  * four consumer warps take stages round-robin and run q.K^T and P.V as
+//  * a producer warp streams stages of 16 keys (32 for 32-token blocks): the
+//    K and V page-heads of the stage's physical blocks, addressed through the
+//    block table, with 2-D TMA loads into a ring of four stage slots (32 KB at
+//    head_dim 128), swizzled so that the consumers' ldmatrix reads are
+//    conflict-free;
+//  * two consumer warps take stages round-robin and run q.K^T and P.V as
 //    m16n8k16 tensor-core MMAs (the group padded to 16 rows) with an fp32
 //    online softmax; the warps' partial states are merged through shared
-//    memory at the end;
+//    memory at the end (or written as two partials per split);
+//  * 96 threads and 128 registers: five CTAs share an SM, so that about
+//    160 KB of loads can be in flight per SM;
 //  * with more than one split, each CTA writes a normalised partial (O, lse)
 //    and merge_kernel combines them: lse = log2 sum_i 2^lse_i,
 //    O = sum_i 2^(lse_i - lse) O_i.

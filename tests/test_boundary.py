@@ -329,3 +329,22 @@ def test_binding_rejects_wrong_dtype_and_layout():
         kvp.kvp_block_copy(pool, i32(1, 3))
     with pytest.raises(ValueError, match="deviation has dtype"):
         kvp.kvp_select_recompute(torch.zeros(4, dtype=torch.float64), torch.zeros(4, dtype=torch.int64), i32(2))
+
+
+def test_group_division_by_multiply_shift_is_exact():
+    """The prefix kernel maps row rg of a (sequence, kv head) problem to
+    (token rg // g, head offset rg % g) as (rg * ceil(2^32 / g)) >> 32, with
+    ceil(2^32 / g) computed on the host; it refuses rows >= 2^24.  The error
+    of the multiplier is e = M g - 2^32 < g, so the quotient is exact while
+    rg * e < 2^32; checked here exhaustively near the bound, for every
+    g the kernel can see up to 256."""
+    import numpy as np
+
+    lim = 1 << 24
+    for g in range(1, 257):
+        m = ((1 << 32) + g - 1) // g
+        n = np.concatenate([np.arange(0, 4096, dtype=np.uint64),
+                            np.arange(lim - 4096, lim, dtype=np.uint64),
+                            np.random.default_rng(g).integers(0, lim, 4096, dtype=np.uint64)])
+        q = (n * np.uint64(m)) >> np.uint64(32)
+        assert np.array_equal(q, n // np.uint64(g)), g
