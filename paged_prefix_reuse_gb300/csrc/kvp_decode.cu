@@ -28,19 +28,27 @@ namespace {
 
 // One warp per output row: merge `splits` partials (normalised O, log2 lse):
 //   lse = log2 sum_i 2^lse_i,  O = sum_i 2^(lse_i - lse) O_i.
-// Lane i computes the weight of split i (32 at a time); the weights are
-// broadcast by shuffle while each lane accumulates four adjacent columns with
-// 16-byte loads, so one split's partial is one coalesced 4*D-byte read.
+// Lane i holds lse of partials i, i + 32, ... (the first 128 in registers);
+// each lane owns four adjacent columns of O.  The row's lse loads and the O
+// rows of its first kChunk partials are issued together, before any of them
+// is used, so a row with up to kChunk partials costs one memory round trip;
+// later chunks of O rows are loaded kChunk at a time.  The weights reach the
+// lanes by shuffle (past the first 128 partials, from a broadcast load).
 template <bool kBF16, int D>
-__global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
+__global__ void __launch_bounds__(256) merge_kernel(const float* ws_o, const float* ws_lse,
                                                     int32_t rows, int32_t Hq, int32_t max_splits,
                                                     void* __restrict__ out, float* __restrict__ lse,
                                                     int32_t lse_stride, const int32_t* __restrict__ ctx,
                                                     int32_t block_size, int32_t pages_per_split,
                                                     int32_t parts_per_split) {
+    constexpr int V4 = D / 4;     // float4 columns per row: 16, 24 or 32
+    constexpr int kChunk = 16;    // O rows loaded at once
+    constexpr int kMaxParts = 128;
     pdl_trigger();
-    pdl_wait();  // the partials come from the kernel before
-    constexpr int V4 = D / 4;  // float4 columns per row: 16, 24 or 32
+    // The partials come from the kernel before: nothing is read before this
+    // wait, and they are read through L2 (ld.global.cg), not the
+    // non-coherent path, so no load can be taken ahead of it.
+    pdl_wait();
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (warp >= rows) return;
@@ -53,58 +61,68 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ ws
         const int np = (L + block_size - 1) / block_size;
         splits = max(0, min(max_splits, (np + pages_per_split - 1) / pages_per_split));
     }
-    splits *= parts_per_split;
-    max_splits *= parts_per_split;
-    const float* lrow = ws_lse + row * max_splits;
+    const int nparts = splits * parts_per_split;
+    const int stride = max_splits * parts_per_split;
+    const float* lrow = ws_lse + row * stride;
+    const float4* orow = reinterpret_cast<const float4*>(ws_o + row * stride * D);
+
+    float lv[kMaxParts / 32];
+#pragma unroll
+    for (int k = 0; k < kMaxParts / 32; ++k) lv[k] = lane + 32 * k < nparts ? __ldcg(lrow + lane + 32 * k) : -INFINITY;
+    float4 ov[kChunk];
+#pragma unroll
+    for (int u = 0; u < kChunk; ++u)
+        ov[u] = (u < nparts && lane < V4) ? __ldcg(orow + static_cast<int64_t>(u) * V4 + lane)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+
     float M = -INFINITY;
-    for (int i = lane; i < splits; i += 32) M = fmaxf(M, __ldg(lrow + i));
+#pragma unroll
+    for (int k = 0; k < kMaxParts / 32; ++k) M = fmaxf(M, lv[k]);
+    for (int i = kMaxParts + lane; i < nparts; i += 32) M = fmaxf(M, __ldcg(lrow + i));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float sum = 0.f;
-    for (int i = lane; i < splits; i += 32) {
-        const float li = __ldg(lrow + i);
+#pragma unroll
+    for (int k = 0; k < kMaxParts / 32; ++k) sum += (lv[k] == -INFINITY) ? 0.f : fast_exp2(lv[k] - M);
+    for (int i = kMaxParts + lane; i < nparts; i += 32) {
+        const float li = __ldcg(lrow + i);
         sum += (li == -INFINITY) ? 0.f : fast_exp2(li - M);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     const float tot = (M == -INFINITY || sum <= 0.f) ? -INFINITY : M + __log2f(sum);
+    float wv[kMaxParts / 32];  // lane i: weight of partials i, i + 32, ...
+#pragma unroll
+    for (int k = 0; k < kMaxParts / 32; ++k)
+        wv[k] = (tot == -INFINITY || lv[k] == -INFINITY) ? 0.f : fast_exp2(lv[k] - tot);
 
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float4* orow = reinterpret_cast<const float4*>(ws_o + row * max_splits * D);
-    if (tot != -INFINITY) {
-        for (int base = 0; base < splits; base += 32) {
-            const int i = base + lane;
-            const float li = i < splits ? __ldg(lrow + i) : -INFINITY;
-            const float wi = (li == -INFINITY) ? 0.f : fast_exp2(li - tot);
-            const int n = min(32, splits - base);
-            int k = 0;
-            for (; k + 4 <= n; k += 4) {
-                float w[4];
-                float4 v[4];
+    for (int base = 0; base < nparts; base += kChunk) {
+        if (base > 0) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    w[u] = __shfl_sync(0xffffffffu, wi, k + u);
-                    v[u] = lane < V4 ? __ldg(orow + static_cast<int64_t>(base + k + u) * V4 + lane)
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+            for (int u = 0; u < kChunk; ++u)
+                ov[u] = (base + u < nparts && lane < V4)
+                            ? __ldcg(orow + static_cast<int64_t>(base + u) * V4 + lane)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        // A chunk lies within one group of 32 partials: its weights sit in
+        // wv[base / 32] of lanes base % 32 .. base % 32 + kChunk - 1.
+        const int kq = base >> 5;
+        float wsrc = 0.f;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    acc.x = fmaf(w[u], v[u].x, acc.x);
-                    acc.y = fmaf(w[u], v[u].y, acc.y);
-                    acc.z = fmaf(w[u], v[u].z, acc.z);
-                    acc.w = fmaf(w[u], v[u].w, acc.w);
-                }
+        for (int k = 0; k < kMaxParts / 32; ++k) wsrc = kq == k ? wv[k] : wsrc;
+#pragma unroll
+        for (int u = 0; u < kChunk; ++u) {
+            const int i = base + u;
+            float w = __shfl_sync(0xffffffffu, wsrc, i & 31);
+            if (i >= kMaxParts && i < nparts) {
+                const float li = __ldcg(lrow + i);
+                w = (tot == -INFINITY || li == -INFINITY) ? 0.f : fast_exp2(li - tot);
             }
-            for (; k < n; ++k) {
-                const float w0 = __shfl_sync(0xffffffffu, wi, k);
-                if (lane < V4) {
-                    const float4 v0 = __ldg(orow + static_cast<int64_t>(base + k) * V4 + lane);
-                    acc.x = fmaf(w0, v0.x, acc.x);
-                    acc.y = fmaf(w0, v0.y, acc.y);
-                    acc.z = fmaf(w0, v0.z, acc.z);
-                    acc.w = fmaf(w0, v0.w, acc.w);
-                }
-            }
+            acc.x = fmaf(w, ov[u].x, acc.x);
+            acc.y = fmaf(w, ov[u].y, acc.y);
+            acc.z = fmaf(w, ov[u].z, acc.z);
+            acc.w = fmaf(w, ov[u].w, acc.w);
         }
     }
     if (lane < V4) {

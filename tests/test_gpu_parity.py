@@ -145,6 +145,13 @@ def test_decode_split_counts(splits):
     _check_step(w, decode_splits=splits)
 
 
+def test_decode_merge_of_more_than_128_partials():
+    """100 key ranges of two partials each for the longest context: the merge
+    takes the weights of partials past the first 128 from broadcast loads."""
+    w = wl.make_random(54, [3300, 31, 1500, 0], [1, 1, 1, 1], Hq=8, Hkv=2, d=128, dtype="bf16", num_decode=4)
+    _check_step(w, decode_splits=100)
+
+
 @pytest.mark.parametrize("d,dtype,bs", [(64, "f16", 16), (96, "bf16", 8), (128, "f16", 32), (96, "f16", 16)])
 def test_decode_head_dims_and_blocks(d, dtype, bs):
     w = wl.make_random(53, [3, 77, 400, 1023], [1, 1, 1, 1], Hq=4, Hkv=1, d=d, dtype=dtype, bs=bs, num_decode=4)
