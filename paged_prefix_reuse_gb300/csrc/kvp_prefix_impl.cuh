@@ -37,8 +37,13 @@
 //    grew by more than 2^8 (exact: the final 1/l uses the same reference);
 //  * the commit that signals S_i(j+1) also covers PV_i(j), so when a
 //    warpgroup sees S it may touch O_i and overwrite the P columns freely;
-//  * key tiles past the last query's position are never loaded; V rows past
-//    the context are zeroed in shared memory before P.V (0 * NaN = NaN).
+//  * key tiles past the last query's position are never loaded; pages of a
+//    loaded tile that lie past the context arrive as out-of-bounds TMA boxes
+//    (zeros, no memory read), and the rows of the last page past the context
+//    are zeroed in shared memory before P.V (0 * NaN = NaN);
+//  * the grid is (query-tile pairs x splits, sequences, kv heads), so the CTAs
+//    of all sequences of one kv head run together and blocks that several
+//    sequences share are re-read from L2.
 //
 // TMEM columns: S_0/P_0 [0,128), S_1/P_1 [128,256), O_0 [256,256+d),
 // O_1 [256+d, 256+2d) -- 512 columns, one CTA per SM.
