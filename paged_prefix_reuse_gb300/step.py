@@ -249,14 +249,22 @@ class HostStep:
         ready = torch.cuda.Event()
         ready.record(s0)
         done = []
+        landed = None  # the previous group's host-to-device copies
         for g, s in zip(self.groups, self.streams):
             t0, t1 = g["t0"], g["t1"]
             s.wait_event(fork)
             with torch.cuda.stream(s):
-                # The group's tokens need no table: their copies start at once.
+                # The group's tokens need no table, so their copies start at
+                # once -- but after the previous group's: the copies share one
+                # host link, and in group order the first group's kernels start
+                # after its own share of the bytes instead of after all of them.
+                if landed is not None:
+                    s.wait_event(landed)
                 st.q[t0:t1].copy_(self.h_q[t0:t1], non_blocking=True)
                 st.k_new[t0:t1].copy_(self.h_k[t0:t1], non_blocking=True)
                 st.v_new[t0:t1].copy_(self.h_v[t0:t1], non_blocking=True)
+                landed = torch.cuda.Event()
+                landed.record(s)
                 s.wait_event(ready)
                 kvp_slot_mapping(st.pool, g["d_cu"], g["d_ctx"], g["d_bt"], t1 - t0, out=st.slots[t0:t1], stream=s)
                 kvp_cache_append(st.pool, st.k_new[t0:t1], st.v_new[t0:t1], st.slots[t0:t1], stream=s)
