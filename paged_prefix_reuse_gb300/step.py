@@ -152,7 +152,7 @@ class HostStep:
         Hq, d = w.num_q_heads, w.head_dim
         if groups <= 0:
             groups = self.auto_groups(w, st.npf)
-        ranges = self.partition(cu, st.npf, st.ndec, groups)
+        plan = self.plan(cu, st.npf, st.ndec, groups)
 
         parts, off = [], 0
 
@@ -166,10 +166,17 @@ class HostStep:
             return start, a.size
 
         self.groups = []
-        for kind, a, b in ranges:
-            g = {"kind": kind, "n": b - a, "t0": int(cu[a]), "t1": int(cu[b]),
-                 "cu": put(cu[a : b + 1] - cu[a]), "ctx": put(ctx[a:b]), "bt": put(bt[a:b]),
-                 "max_q": int(np.diff(cu[a : b + 1]).max()), "max_ctx": int(ctx[a:b].max())}
+        for kind, a, b, c0, c1 in plan:
+            if c0 is None:  # whole sequences [a, b)
+                g = {"kind": kind, "n": b - a, "t0": int(cu[a]), "t1": int(cu[b]), "chunk": False,
+                     "cu": put(cu[a : b + 1] - cu[a]), "ctx": put(ctx[a:b]), "bt": put(bt[a:b]),
+                     "max_q": int(np.diff(cu[a : b + 1]).max()), "max_ctx": int(ctx[a:b].max())}
+            else:  # new tokens [c0, c1) of sequence a: its keys end at P + c1
+                n_new = int(cu[a + 1] - cu[a])
+                cend = int(ctx[a]) - (n_new - c1)
+                g = {"kind": kind, "n": 1, "t0": int(cu[a]) + c0, "t1": int(cu[a]) + c1, "chunk": c0 > 0,
+                     "cu": put([0, c1 - c0]), "ctx": put([cend]), "bt": put(bt[a : a + 1]),
+                     "max_q": c1 - c0, "max_ctx": cend}
             self.groups.append(g)
         meta = np.concatenate(parts) if parts else np.zeros(4, dtype=np.int32)
         self.h_meta = torch.from_numpy(meta).pin_memory()
@@ -201,6 +208,34 @@ class HostStep:
             g["lse_host"].numel() * 4 for g in self.groups)
 
     @staticmethod
+    def plan(cu_seqlens_q, npf: int, ndec: int, groups: int, align: int = 256):
+        """[(kind, a, b, c0, c1)]: with no more groups than prefill sequences
+        that have new tokens, ``partition``'s ranges of whole sequences [a, b)
+        (c0 = c1 = None); with more, each such sequence a's new tokens cut into
+        ceil(groups / sequences) chunks [c0, c1) of about equal length, in
+        multiples of ``align`` tokens (one group each), then the decode batch.
+        A chunk's queries see the keys up to its own end, so its call needs
+        the earlier chunks' K/V appended first."""
+        cu = np.asarray(cu_seqlens_q, dtype=np.int64)
+        live = [s for s in range(npf) if cu[s + 1] > cu[s]]
+        if groups <= len(live):
+            return [(k, a, b, None, None) for k, a, b in HostStep.partition(cu, npf, ndec, groups)]
+        per = -(-groups // len(live))
+        out = []
+        for s in live:
+            n = int(cu[s + 1] - cu[s])
+            chunk = -(-n // per)  # ceil(n / per)
+            step = max(align, -(-chunk // align) * align)  # rounded up to whole multiples of align
+            c0 = 0
+            while c0 < n:
+                c1 = min(n, c0 + step)
+                out.append(("prefill", s, s + 1, c0, c1))
+                c0 = c1
+        if ndec:
+            out.append(("decode", npf, npf + ndec, None, None))
+        return out
+
+    @staticmethod
     def partition(cu_seqlens_q, npf: int, ndec: int, groups: int):
         """[(kind, first sequence, end sequence)]: the prefill sequences [0, npf)
         cut into at most ``groups`` contiguous ranges of about equal token
@@ -220,7 +255,7 @@ class HostStep:
         return ranges
 
     @staticmethod
-    def auto_groups(w, npf: int, sms: int = 152, rows_per_cta: int = 256, most: int = 4) -> int:
+    def auto_groups(w, npf: int, sms: int = 152, rows_per_cta: int = 256, most: int = 8) -> int:
         """One group per GPU's worth of prefix-attention CTAs (at most
         ``most``): a group that leaves SMs idle gains nothing from starting
         early, and each group adds its own launches and copies."""
@@ -250,6 +285,7 @@ class HostStep:
         ready.record(s0)
         done = []
         landed = None  # the previous group's host-to-device copies
+        appended = []  # each earlier group's appends
         for g, s in zip(self.groups, self.streams):
             t0, t1 = g["t0"], g["t1"]
             s.wait_event(fork)
@@ -268,6 +304,14 @@ class HostStep:
                 s.wait_event(ready)
                 kvp_slot_mapping(st.pool, g["d_cu"], g["d_ctx"], g["d_bt"], t1 - t0, out=st.slots[t0:t1], stream=s)
                 kvp_cache_append(st.pool, st.k_new[t0:t1], st.v_new[t0:t1], st.slots[t0:t1], stream=s)
+                if g["chunk"]:
+                    # A later chunk of a sequence attends to the K/V the
+                    # earlier chunks' groups append.
+                    for e in appended:
+                        s.wait_event(e)
+                ea = torch.cuda.Event()
+                ea.record(s)
+                appended.append(ea)
                 if g["kind"] == "prefill":
                     out = st.out_pf[t0:t1]
                     kvp_prefix_attn(st.pool, st.q[t0:t1], g["d_cu"], g["d_ctx"], g["d_bt"], g["max_q"], g["max_ctx"],

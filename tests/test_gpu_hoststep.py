@@ -76,3 +76,37 @@ def test_host_step_matches_device_step(name, groups, graph):
     lse = torch.cat(hs.lse_host, dim=1)
     assert torch.equal(lse, lse_ref)
     assert hs.h2d_bytes > 0 and hs.d2h_bytes == out.numel() * 2 + lse.numel() * 4
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_host_step_with_chunked_sequences_matches_device_step(graph):
+    """More groups than sequences: each sequence's new tokens are cut into
+    chunks whose queries see the keys up to the chunk's end, and a chunk
+    follows the earlier chunks' appends.  With one key range per CTA the
+    results are bit-identical to the one-stream step."""
+    from paged_prefix_reuse_gb300.step import DeviceStep, HostStep
+
+    w = wl.make_random(49, [900, 200], [600, 300], Hq=8, Hkv=2, d=128, dtype="bf16")
+    ref = DeviceStep(w, prefix_splits=1)
+    ref.run()
+    torch.cuda.synchronize()
+    st = DeviceStep(w, prefix_splits=1)
+    hs = HostStep(st, groups=4)
+    assert [g["t1"] - g["t0"] for g in hs.groups] == [512, 88, 256, 44]
+    st.q.fill_(float("nan"))
+    st.k_new.zero_()
+    st.v_new.zero_()
+    stream = torch.cuda.Stream()
+    if graph:
+        g = hs.capture(stream)
+        st.q.fill_(float("nan"))
+        g.replay()
+    else:
+        with torch.cuda.stream(stream):
+            hs.run(stream)
+    stream.synchronize()
+    assert st.pool.errors() == 0
+    assert torch.equal(st.slots[: st.T], ref.slots[: ref.T])
+    assert torch.equal(st.pool.k, ref.pool.k) and torch.equal(st.pool.v, ref.pool.v)
+    assert torch.equal(hs.out_host, ref.out_pf.cpu())
+    assert torch.equal(torch.cat([l for l in hs.lse_host], dim=1), ref.lse_pf.cpu())

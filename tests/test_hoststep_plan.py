@@ -33,11 +33,37 @@ def test_partition_without_prefill_or_decode():
     assert HostStep.partition([0, 0, 0], 2, 0, 2) == []
 
 
+def test_plan_keeps_whole_sequences_while_groups_do_not_outnumber_them():
+    cu = [0, 50, 120, 121, 122]
+    assert HostStep.plan(cu, 2, 2, 2) == [(k, a, b, None, None) for k, a, b in HostStep.partition(cu, 2, 2, 2)]
+
+
+@pytest.mark.parametrize("groups", [5, 8, 9])
+def test_plan_cuts_long_sequences_into_aligned_chunks(groups):
+    lens = [2048, 0, 600, 1300]
+    cu = np.concatenate([[0], np.cumsum(lens), [sum(lens) + 1, sum(lens) + 2]])  # + 2 decode tokens
+    plan = HostStep.plan(cu, 4, 2, groups)
+    assert plan[-1] == ("decode", 4, 6, None, None)
+    pre = plan[:-1]
+    # every new token of every prefill sequence in exactly one chunk, in order
+    seen = []
+    for kind, a, b, c0, c1 in pre:
+        assert kind == "prefill" and b == a + 1 and c0 < c1
+        assert c0 % 256 == 0 and (c1 % 256 == 0 or c1 == lens[a])
+        seen += [(a, t) for t in range(c0, c1)]
+    assert seen == [(s, t) for s in range(4) for t in range(lens[s])]
+    per = -(-groups // 3)  # three sequences have new tokens
+    for s in (0, 2, 3):
+        assert len([1 for _, a, _, _, _ in pre if a == s]) <= per
+
+
 def test_auto_groups_follow_the_prefix_cta_count():
-    # one group per 152 prefix-attention CTAs, at most four
+    # one group per 152 prefix-attention CTAs, at most eight
     assert HostStep.auto_groups(wl.make_config(2), wl.make_config(2).num_prefill) == 1  # 128 CTAs
     w4 = wl.make_config(4)
     assert HostStep.auto_groups(w4, w4.num_prefill) == 2  # 320 CTAs
     w3 = wl.make_config(3)
     assert HostStep.auto_groups(w3, w3.num_prefill) == 4
     assert HostStep.auto_groups(w3, 0) == 1
+    w5 = wl.make_config(5)
+    assert HostStep.auto_groups(w5, w5.num_prefill) == 8  # 2048 CTAs: four sequences in two chunks each
