@@ -255,7 +255,7 @@ class HostStep:
         return ranges
 
     @staticmethod
-    def auto_groups(w, npf: int, sms: int = 152, rows_per_cta: int = 256, most: int = 8) -> int:
+    def auto_groups(w, npf: int, sms: int = 152, rows_per_cta: int = 256, most: int = 16) -> int:
         """One group per GPU's worth of prefix-attention CTAs (at most
         ``most``): a group that leaves SMs idle gains nothing from starting
         early, and each group adds its own launches and copies."""

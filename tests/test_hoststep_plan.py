@@ -58,7 +58,7 @@ def test_plan_cuts_long_sequences_into_aligned_chunks(groups):
 
 
 def test_auto_groups_follow_the_prefix_cta_count():
-    # one group per 152 prefix-attention CTAs, at most eight
+    # one group per 152 prefix-attention CTAs, at most sixteen
     assert HostStep.auto_groups(wl.make_config(2), wl.make_config(2).num_prefill) == 1  # 128 CTAs
     w4 = wl.make_config(4)
     assert HostStep.auto_groups(w4, w4.num_prefill) == 2  # 320 CTAs
@@ -66,4 +66,6 @@ def test_auto_groups_follow_the_prefix_cta_count():
     assert HostStep.auto_groups(w3, w3.num_prefill) == 4
     assert HostStep.auto_groups(w3, 0) == 1
     w5 = wl.make_config(5)
-    assert HostStep.auto_groups(w5, w5.num_prefill) == 8  # 2048 CTAs: four sequences in two chunks each
+    assert HostStep.auto_groups(w5, w5.num_prefill) == 13  # 2048 CTAs
+    cu5 = np.asarray(w5.cu_seqlens_q)
+    assert len(HostStep.plan(cu5, w5.num_prefill, 0, 13)) == 16  # four sequences in four chunks of 512
