@@ -49,18 +49,22 @@
 // O_1 [256+d, 256+2d) -- 512 columns, one CTA per SM.
 //
 // Over a quantized cached prefix (BITS 8 or 4; kvboost "Optional: KV
-// quantization": cached K per channel, V per token, 8 or 4 bits), two more
-// warps (10 and 11) turn codes into the fp16 tiles tcgen05 reads:
+// quantization": cached K per channel, V per token, 8 or 4 bits), four more
+// warps (10 to 13) turn codes into the fp16 tiles tcgen05 reads:
 //  * for a K or V half-tile holding quantized pages, the producer first
 //    stages those pages' codes and scales (bulk copies, a few hundred bytes
 //    to 2 KB each) in a ring of its own, then TMA-loads the half-tile's
 //    16-bit pages (the live suffix) straight into the K/V ring slot;
-//  * each dequantizing warp owns half the rows of the slot: quantized pages
+//  * each dequantizing warp owns a quarter of the slot's rows: quantized pages
 //    become code * s + z in fp16 (one fused multiply-add per pair), written
 //    in the same 128B-swizzled layout TMA gives; a bf16 pool's 16-bit pages
 //    are converted to fp16 in place; then the slot goes to the MMA warp;
 //  * the products run in fp16 whatever the pool dtype (Q is converted when
 //    it is staged, P is written as fp16), as in the quantized decode.
+//  * fourteen warps leave 128 registers a thread (registers are allocated per
+//    SM sub-partition, and two of them hold four warps), so this kernel's
+//    softmax reads S in two halves of 64 columns, twice each.
+
 #pragma once
 #include "kvp_internal.cuh"
 
@@ -71,8 +75,8 @@ constexpr int kSoftmaxWarps = 8;                    // two warpgroups, one per q
 constexpr int kProducerWarp = kSoftmaxWarps;        // warp 8
 constexpr int kMmaWarp = kSoftmaxWarps + 1;         // warp 9
 constexpr int kThreads = (kSoftmaxWarps + 2) * 32;  // 320
-constexpr int kDequantWarp0 = kSoftmaxWarps + 2;    // warps 10, 11 (quantized prefix only)
-constexpr int kDequantWarps = 2;
+constexpr int kDequantWarp0 = kSoftmaxWarps + 2;    // warps 10-13 (quantized prefix only)
+constexpr int kDequantWarps = 4;
 __host__ __device__ constexpr int prefix_threads(int bits) { return kThreads + (bits ? kDequantWarps * 32 : 0); }
 constexpr int kBM = 128;                            // rows per query tile (TMEM lanes)
 constexpr int kRowsPerCta = 2 * kBM;
@@ -214,6 +218,37 @@ __device__ __forceinline__ int64_t out_row(const PrefixParams& p, int cu0, int h
     return static_cast<int64_t>(cu0 + t) * p.num_q_heads + h * p.group + (rg - t * p.group);
 }
 
+__device__ __forceinline__ void tmem_ld64_sync(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,"
+        "%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,"
+        "%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]),
+          "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]),
+          "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]),
+          "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]),
+          "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,"
+        "%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
 // Eight bf16 values -> eight fp16 values (round to nearest).
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 a) {
     const float2 x = unpack2<true>(a.x), y = unpack2<true>(a.y), z = unpack2<true>(a.z), w = unpack2<true>(a.w);
@@ -244,8 +279,9 @@ __device__ __forceinline__ void prefix_fill_rows(uint32_t stage, uint32_t dst, i
     const bool has = u < UD;
     const int uc = u % (L::CW / 8);
     const uint32_t ubase = dst + (u / (L::CW / 8)) * L::CHUNK_BYTES;
-    const int i0 = 4 * dw;
-    const int nmine = min(max(nq - i0, 0), 4);  // quantized pages among this warp's four
+    constexpr int kPagesPerWarp = QC::PAGES / kDequantWarps;
+    const int i0 = kPagesPerWarp * dw;
+    const int nmine = min(max(nq - i0, 0), kPagesPerWarp);  // quantized pages among this warp's
 #pragma unroll 1
     for (int pg = 0; pg < nmine; ++pg) {
         const int i = i0 + pg;
@@ -285,7 +321,7 @@ __device__ __forceinline__ void prefix_fill_rows(uint32_t stage, uint32_t dst, i
     if constexpr (kBF16) {
         // This warp's 16-bit pages (the live suffix): bf16 -> fp16 in place.
 #pragma unroll 1
-        for (int pg = nmine; pg < 4; ++pg) {
+        for (int pg = nmine; pg < kPagesPerWarp; ++pg) {
             uint4 a[IT];
 #pragma unroll
             for (int it = 0; it < IT; ++it) a[it] = lds128(ubase + swz_offset(16 * (i0 + pg) + it * RPP + r_in, uc, L::ROWB));
@@ -464,69 +500,149 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
                 const int j = j_begin + jj;
                 if (!mbar_wait(&s_full[wg], jj & 1, abort_flag, err, p.wait_limit_ns)) { ok = false; break; }
                 tc_fence_after();
-                float x[kBN];
-                {
-                    uint32_t r[kBN];
-                    tmem_ld128_sync(lane_base + scol, r);
+                if constexpr (BITS == 0) {
+                    float x[kBN];
+                    {
+                        uint32_t r[kBN];
+                        tmem_ld128_sync(lane_base + scol, r);
 #pragma unroll
-                    for (int i = 0; i < kBN; ++i) x[i] = __uint_as_float(r[i]);
-                }
-                const int lim = qpos - j * kBN;  // last visible column of this tile
-                if (lim < kBN - 1) {
-#pragma unroll
-                    for (int c = 0; c < kBN; ++c)
-                        if (c > lim) x[c] = -INFINITY;
-                }
-                // Row maximum: 3-input max in eight independent chains.
-                float mx8[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mx8[i] = x[i];
-#pragma unroll
-                for (int c = 8; c < kBN - 8; c += 16) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], x[c + i], x[c + 8 + i]);
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], x[kBN - 8 + i]);
-                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                                       fmaxf(mx8[6], mx8[7]));
-                const float m_new = fmaxf(m, mx * sl2);
-                const bool need = m_new > m + 8.0f;
-                float alpha = 1.f;
-                if (need) {
-                    alpha = fast_exp2(m - m_new);
-                    m = m_new;
-                    l *= alpha;
-                }
-                const float mref = (m == -INFINITY) ? 0.f : m;
-                // p = 2^(x * scale * log2 e - m), pairs on the packed fp32 pipe.
-                const float2 sc = make_float2(sl2, sl2), nb = make_float2(-mref, -mref);
-                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                                 make_float2(0.f, 0.f)};
-                uint32_t pk[kBN / 2];
-#pragma unroll
-                for (int c = 0; c < kBN; c += 2) {
-                    const float2 t = ffma2(make_float2(x[c], x[c + 1]), sc, nb);
-                    const float2 e = make_float2(fast_exp2(t.x), fast_exp2(t.y));
-                    acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], e);
-                    pk[c >> 1] = pack2<kMma>(e.x, e.y);
-                }
-                const float2 a = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
-                l += a.x + a.y;
-
-                if (jj > 0 && __any_sync(0xffffffffu, need)) {
-                    // O_wg holds PV_0 .. PV_{jj-1} (the commit that signalled S
-                    // covered them) at the old reference maximum: rescale it.
-#pragma unroll
-                    for (int cb = 0; cb < D / 16; ++cb) {
-                        uint32_t r[16];
-                        tmem_ld16_sync(lane_base + ocol + 16 * cb, r);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st16(lane_base + ocol + 16 * cb, r);
+                        for (int i = 0; i < kBN; ++i) x[i] = __uint_as_float(r[i]);
                     }
+                    const int lim = qpos - j * kBN;  // last visible column of this tile
+                    if (lim < kBN - 1) {
+#pragma unroll
+                        for (int c = 0; c < kBN; ++c)
+                            if (c > lim) x[c] = -INFINITY;
+                    }
+                    // Row maximum: 3-input max in eight independent chains.
+                    float mx8[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx8[i] = x[i];
+#pragma unroll
+                    for (int c = 8; c < kBN - 8; c += 16) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], x[c + i], x[c + 8 + i]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], x[kBN - 8 + i]);
+                    const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                           fmaxf(mx8[6], mx8[7]));
+                    const float m_new = fmaxf(m, mx * sl2);
+                    const bool need = m_new > m + 8.0f;
+                    float alpha = 1.f;
+                    if (need) {
+                        alpha = fast_exp2(m - m_new);
+                        m = m_new;
+                        l *= alpha;
+                    }
+                    const float mref = (m == -INFINITY) ? 0.f : m;
+                    // p = 2^(x * scale * log2 e - m), pairs on the packed fp32 pipe.
+                    const float2 sc = make_float2(sl2, sl2), nb = make_float2(-mref, -mref);
+                    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                     make_float2(0.f, 0.f)};
+                    uint32_t pk[kBN / 2];
+#pragma unroll
+                    for (int c = 0; c < kBN; c += 2) {
+                        const float2 t = ffma2(make_float2(x[c], x[c + 1]), sc, nb);
+                        const float2 e = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+                        acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], e);
+                        pk[c >> 1] = pack2<kMma>(e.x, e.y);
+                    }
+                    const float2 a = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+                    l += a.x + a.y;
+
+                    if (jj > 0 && __any_sync(0xffffffffu, need)) {
+                        // O_wg holds PV_0 .. PV_{jj-1} (the commit that signalled S
+                        // covered them) at the old reference maximum: rescale it.
+#pragma unroll
+                        for (int cb = 0; cb < D / 16; ++cb) {
+                            uint32_t r[16];
+                            tmem_ld16_sync(lane_base + ocol + 16 * cb, r);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                            tmem_st16(lane_base + ocol + 16 * cb, r);
+                        }
+                    }
+                    tmem_st64(lane_base + scol, pk);  // P over the first 64 columns of S
+                } else {
+                    // Fourteen warps leave 128 registers: S is read in two halves
+                    // of 64 columns, twice -- for the row maximum, then for the
+                    // exponentials -- and P is stored per half (the half-0 P goes
+                    // over S columns already read; half 1's S lies beyond it).
+                    const int lim = qpos - j * kBN;  // last visible column of this tile
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t r[kBN / 2];
+                        tmem_ld64_sync(lane_base + scol + half * (kBN / 2), r);
+                        float xh[kBN / 2];
+#pragma unroll
+                        for (int c = 0; c < kBN / 2; ++c) xh[c] = __uint_as_float(r[c]);
+                        if (lim < kBN - 1) {
+#pragma unroll
+                            for (int c = 0; c < kBN / 2; ++c)
+                                if (half * (kBN / 2) + c > lim) xh[c] = -INFINITY;
+                        }
+                        float mx4[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) mx4[i] = xh[i];
+#pragma unroll
+                        for (int c = 4; c < kBN / 2 - 4; c += 8) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) mx4[i] = fmax3(mx4[i], xh[c + i], xh[c + 4 + i]);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) mx4[i] = fmaxf(mx4[i], xh[kBN / 2 - 4 + i]);
+                        mx = fmaxf(mx, fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])));
+                    }
+                    const float m_new = fmaxf(m, mx * sl2);
+                    const bool need = m_new > m + 8.0f;
+                    float alpha = 1.f;
+                    if (need) {
+                        alpha = fast_exp2(m - m_new);
+                        m = m_new;
+                        l *= alpha;
+                    }
+                    const float mref = (m == -INFINITY) ? 0.f : m;
+                    if (jj > 0 && __any_sync(0xffffffffu, need)) {
+                        // Rescale O (as above) before this tile's P.V adds to it.
+#pragma unroll
+                        for (int cb = 0; cb < D / 16; ++cb) {
+                            uint32_t r[16];
+                            tmem_ld16_sync(lane_base + ocol + 16 * cb, r);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                            tmem_st16(lane_base + ocol + 16 * cb, r);
+                        }
+                    }
+                    const float2 sc = make_float2(sl2, sl2), nb = make_float2(-mref, -mref);
+                    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                     make_float2(0.f, 0.f)};
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t r[kBN / 2];
+                        tmem_ld64_sync(lane_base + scol + half * (kBN / 2), r);
+                        float xh[kBN / 2];
+#pragma unroll
+                        for (int c = 0; c < kBN / 2; ++c) xh[c] = __uint_as_float(r[c]);
+                        if (lim < kBN - 1) {
+#pragma unroll
+                            for (int c = 0; c < kBN / 2; ++c)
+                                if (half * (kBN / 2) + c > lim) xh[c] = -INFINITY;
+                        }
+                        uint32_t pk[kBN / 4];
+#pragma unroll
+                        for (int c = 0; c < kBN / 2; c += 2) {
+                            const float2 t = ffma2(make_float2(xh[c], xh[c + 1]), sc, nb);
+                            const float2 e = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+                            acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], e);
+                            pk[c >> 1] = pack2<kMma>(e.x, e.y);
+                        }
+                        tmem_st32(lane_base + scol + half * (kBN / 4), pk);
+                    }
+                    const float2 a = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+                    l += a.x + a.y;
                 }
-                tmem_st64(lane_base + scol, pk);  // P over the first 64 columns of S
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
