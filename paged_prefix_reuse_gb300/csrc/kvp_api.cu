@@ -39,15 +39,18 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // The pool viewed as a 2-D tensor of rows (block, kv head, slot) x head_dim;
 // one TMA box is one block of one kv head, `chunk_elems` columns wide.
-kvp_status make_pool_map(CUtensorMap* map, void* base, const kvp_pool* pool, int CW = 0) {
+// Boxes of CW columns (0: the head dim's chunk) by box_rows rows (0: one
+// block); a box wider than the row reads zeros past it.
+kvp_status make_pool_map(CUtensorMap* map, void* base, const kvp_pool* pool, int CW = 0, int box_rows = 0) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return KVP_ERR_CUDA;
     const int D = pool->head_dim;
-    if (CW == 0) CW = chunk_elems(D);  // else a box wider than the row reads zeros past it
+    if (CW == 0) CW = chunk_elems(D);
+    if (box_rows == 0) box_rows = pool->block_size;
     const cuuint64_t rows = static_cast<cuuint64_t>(pool->num_blocks) * pool->num_kv_heads * pool->block_size;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), rows};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(CW), static_cast<cuuint32_t>(pool->block_size)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(CW), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
     const CUtensorMapDataType dt =
         pool->dtype == KVP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -455,19 +458,24 @@ static kvp_status decode_common(const kvp_pool* pool, const kvp_qpool* qpool, co
     if (p.max_splits > 1) {
         const size_t need = kvp_workspace_size(1, B, num_q_heads, pool->head_dim, p.max_splits);
         if (!workspace || workspace_bytes < need || !aligned16(workspace)) return KVP_ERR_WORKSPACE;
-        const size_t r = static_cast<size_t>(B) * num_q_heads * p.max_splits * decode_parts_per_split();
+        // The 16-bit kernel writes a partial per consumer warp and split, the
+        // quantized-prefix kernel one per split; the workspace fits either.
+        const size_t r = static_cast<size_t>(B) * num_q_heads * p.max_splits * (qpool ? 1 : decode_parts_per_split());
         p.ws_o = static_cast<float*>(workspace);
         p.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(r * pool->head_dim * 4));
     }
+    // The quantized-prefix kernel takes its 16-bit pages in halves of 8 rows.
     CUtensorMap tk, tv;
-    if ((st = make_pool_map(&tk, pool->k_pool, pool)) != KVP_OK) return st;
-    if ((st = make_pool_map(&tv, pool->v_pool, pool)) != KVP_OK) return st;
+    const int rows = qpool ? kDecodeQHalfRows : 0;
+    if ((st = make_pool_map(&tk, pool->k_pool, pool, 0, rows)) != KVP_OK) return st;
+    if ((st = make_pool_map(&tv, pool->v_pool, pool, 0, rows)) != KVP_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = qpool ? launch_decode_attn_q(p, tk, tv, s) : launch_decode_attn(p, tk, tv, s);
     if (e != cudaSuccess) return KVP_ERR_CUDA;
     if (p.max_splits > 1)
         e = launch_merge(p.ws_o, p.ws_lse, B * num_q_heads, num_q_heads, pool->head_dim, p.max_splits, pool->dtype,
-                         out, lse, B, context_lens, pool->block_size, p.pages_per_split, decode_parts_per_split(), s);
+                         out, lse, B, context_lens, pool->block_size, p.pages_per_split,
+                         qpool ? 1 : decode_parts_per_split(), s);
     return from_cuda(e);
 }
 

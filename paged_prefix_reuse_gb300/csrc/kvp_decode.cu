@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* ws_o, const flo
 template <bool kBF16, int D, int SK>
 cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                             cudaStream_t stream) {
-    return launch_decode_kernel<kBF16, D, SK, 0>(p, tk, tv, stream);
+    return launch_decode_kernel<kBF16, D, SK>(p, tk, tv, stream);
 }
 
 template <bool kBF16, int D>

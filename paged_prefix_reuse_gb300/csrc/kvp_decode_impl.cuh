@@ -1,7 +1,7 @@
-// kvp_decode_impl.cuh -- the decode-attention kernel template, shared by
-// the 16-bit decode (kvp_decode.cu) and the decode over a quantized cached
-// prefix (kvp_quant.cu), each translation unit instantiating its own
-// variants.  See kvp_decode.cu for the design.
+// kvp_decode_impl.cuh -- the 16-bit decode-attention kernel template
+// (instantiated by kvp_decode.cu; see there for the design) and the ring
+// constants that the decode over a quantized cached prefix (kvp_quant.cu)
+// shares with it.
 #pragma once
 #include "kvp_internal.cuh"
 
@@ -13,10 +13,8 @@ constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
 constexpr int kRingSlots = 2 * kConsumerWarps;  // two slots per consumer warp: one computing, one loading
 
 // SK keys per stage: 16 (one 16-token block) when blocks hold <= 16 tokens,
-// else 32 (one 32-token block).  BITS 8 or 4: stages of the quantized cached
-// prefix arrive as codes and scales (one 16-token block per stage) and each
-// consumer warp dequantizes its stage into a private 16-bit tile.
-template <int D, int SK, int BITS = 0>
+// else 32 (one 32-token block).
+template <int D, int SK>
 struct DecodeCfg {
     static constexpr int CW = chunk_elems(D);
     static constexpr int ROWB = CW * 2;
@@ -32,110 +30,9 @@ struct DecodeCfg {
     static_assert(NS % kConsumerWarps == 0, "ring depth");
     static constexpr int RED_BYTES = (D / 8) * 32 * 16 + 32 * 8;  // one warp's fragments + row stats
     static constexpr int RING_BYTES = NS * STAGE_BYTES > RED_BYTES ? NS * STAGE_BYTES : RED_BYTES;
-    // Quantized stage inside a slot: K codes, V codes, K meta (scale row, min
-    // row, fp16), V meta ((scale, min) per token, fp16).
-    static constexpr int QCODE = SK * D * BITS / 8;
-    static constexpr int QOFF_V = QCODE, QOFF_KM = 2 * QCODE, QOFF_VM = 2 * QCODE + 4 * D;
-    static constexpr int QSTAGE = 2 * QCODE + 4 * D + 4 * SK;
-    static_assert(BITS == 0 || QSTAGE <= STAGE_BYTES, "quantized stage fits a slot");
-    static constexpr int STG_BYTES = BITS ? STAGE_BYTES : 0;  // per consumer warp: dequantized K and V
-    static constexpr int OFF_STG = RING_BYTES;
-    static constexpr int OFF_BAR = RING_BYTES + kConsumerWarps * STG_BYTES;
+    static constexpr int OFF_BAR = RING_BYTES;
     static constexpr int SMEM_BYTES = OFF_BAR + (2 * NS + 1) * 8 + 16 + 1024;
 };
-
-// Dequantize one quantized stage (SK keys of one kv head) into the warp's
-// fp16 K and V tiles, in the chunked, swizzled layout the TMA path gives.
-// K scale/min are per channel (a lane's channels are fixed across its keys
-// when 32 is a multiple of the units per row), V's per token.  Keys at or
-// past nvalid become zeros.  All addresses are shared-memory addresses; the
-// accesses are explicit shared loads and stores, and each half of the
-// lane's units has all its code and scale loads issued before its
-// arithmetic and stores.
-template <int D, int SK, int BITS>
-__device__ __forceinline__ void dequant_stage(uint32_t qs, uint32_t stk, uint32_t stv, int nvalid, int lane) {
-    using C = DecodeCfg<D, SK, BITS>;
-    constexpr int U = D / 8;            // 16-byte output units per row
-    constexpr int CROW = D * BITS / 8;  // code bytes per row
-    constexpr int IT = SK * U / 32;     // units per lane
-    constexpr int H = IT % 2 == 0 ? IT / 2 : IT;  // units per batch of loads
-    static_assert((SK * U) % 32 == 0, "whole units per lane");
-    const uint32_t kc = qs, vc = qs + C::QOFF_V, km = qs + C::QOFF_KM, vm = qs + C::QOFF_VM;
-    constexpr bool kFixedUnit = (32 % U) == 0;
-    uint32_t ks[4], kz[4];
-    auto load_kmeta = [&](int u) {
-        const uint4 a = lds128(km + u * 16);
-        const uint4 b = lds128(km + 2 * D + u * 16);
-        ks[0] = a.x; ks[1] = a.y; ks[2] = a.z; ks[3] = a.w;
-        kz[0] = b.x; kz[1] = b.y; kz[2] = b.z; kz[3] = b.w;
-    };
-    if constexpr (kFixedUnit) load_kmeta(lane % U);
-#pragma unroll
-    for (int h0 = 0; h0 < IT; h0 += H) {
-        uint2 kw[H], vw[H];
-        uint32_t sz[H];
-#pragma unroll
-        for (int k = 0; k < H; ++k) {
-            const int e = lane + 32 * (h0 + k);
-            const int key = e / U, u = e - (e / U) * U;
-            const uint32_t off = key * CROW + u * BITS;
-            if constexpr (BITS == 8) {
-                kw[k] = lds64(kc + off);
-                vw[k] = lds64(vc + off);
-            } else {
-                kw[k] = make_uint2(lds32(kc + off), 0u);
-                vw[k] = make_uint2(lds32(vc + off), 0u);
-            }
-            sz[k] = lds32(vm + 4 * key);  // (scale, min) of this token
-        }
-#pragma unroll
-        for (int k = 0; k < H; ++k) {
-            const int e = lane + 32 * (h0 + k);
-            const int key = e / U, u = e - (e / U) * U;
-            if constexpr (!kFixedUnit) load_kmeta(u);
-            uint4 ko = make_uint4(0, 0, 0, 0), vo = make_uint4(0, 0, 0, 0);
-            if (key < nvalid) {
-                ko = dequant_words<BITS>(kw[k], ks, kz);
-                const uint32_t s1 = __byte_perm(sz[k], 0, 0x1010), z1 = __byte_perm(sz[k], 0, 0x3232);
-                const uint32_t vs[4] = {s1, s1, s1, s1}, vz[4] = {z1, z1, z1, z1};
-                vo = dequant_words<BITS>(vw[k], vs, vz);
-            }
-            const uint32_t off = (u / (C::CW / 8)) * C::REGION + swz_offset(key, u % (C::CW / 8), C::ROWB);
-            sts128(stk + off, ko);
-            sts128(stv + off, vo);
-        }
-    }
-}
-
-// A 16-bit bf16 stage (the live suffix of a bf16 pool) converted to fp16 for
-// the fp16 products of the quantized-prefix kernel; keys at or past nvalid
-// become zeros.  Same swizzled layout in and out; shared-memory addresses.
-template <int D, int SK, int BITS>
-__device__ __forceinline__ void bf16_stage_to_f16(uint32_t kin, uint32_t vin, uint32_t stk, uint32_t stv,
-                                                  int nvalid, int lane) {
-    using C = DecodeCfg<D, SK, BITS>;
-    constexpr int U = D / 8;
-#pragma unroll
-    for (int it = 0; it < SK * U / 32; ++it) {
-        const int e = lane + 32 * it;
-        const int key = e / U, u = e - (e / U) * U;
-        const uint32_t off = (u / (C::CW / 8)) * C::REGION + swz_offset(key, u % (C::CW / 8), C::ROWB);
-        uint4 ko = make_uint4(0, 0, 0, 0), vo = make_uint4(0, 0, 0, 0);
-        if (key < nvalid) {
-            const uint4 a = lds128(kin + off), b = lds128(vin + off);
-            ko = make_uint4(pack2<false>(unpack2<true>(a.x).x, unpack2<true>(a.x).y),
-                            pack2<false>(unpack2<true>(a.y).x, unpack2<true>(a.y).y),
-                            pack2<false>(unpack2<true>(a.z).x, unpack2<true>(a.z).y),
-                            pack2<false>(unpack2<true>(a.w).x, unpack2<true>(a.w).y));
-            vo = make_uint4(pack2<false>(unpack2<true>(b.x).x, unpack2<true>(b.x).y),
-                            pack2<false>(unpack2<true>(b.y).x, unpack2<true>(b.y).y),
-                            pack2<false>(unpack2<true>(b.z).x, unpack2<true>(b.z).y),
-                            pack2<false>(unpack2<true>(b.w).x, unpack2<true>(b.w).y));
-        }
-        sts128(stk + off, ko);
-        sts128(stv + off, vo);
-    }
-}
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -170,16 +67,11 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return p + (((a + 1023u) & ~1023u) - a);
 }
 
-template <bool kBF16, int D, int SK, int BITS>
-__global__ void __launch_bounds__(kDecodeThreads, BITS ? 4 : 5)
+template <bool kBF16, int D, int SK>
+__global__ void __launch_bounds__(kDecodeThreads, 5)
     decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                   const DecodeParams p) {
-    using C = DecodeCfg<D, SK, BITS>;
-    static_assert(BITS == 0 || BITS == 4 || BITS == 8, "bits");
-    // The quantized-prefix kernel runs its tensor-core products in fp16
-    // whatever the pool dtype (fp16 holds the dequantized values and a bf16
-    // pool's values more closely than bf16); the output keeps the pool dtype.
-    constexpr bool kMma = BITS ? false : kBF16;
+    using C = DecodeCfg<D, SK>;
     constexpr int kStageKeys = SK;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
@@ -213,9 +105,6 @@ __global__ void __launch_bounds__(kDecodeThreads, BITS ? 4 : 5)
     const int key1 = min(L, page1 * BS);
     const int nstages = (key1 - key0 + kStageKeys - 1) / kStageKeys;
     const int pps = kStageKeys / BS;  // physical pages per stage
-    // Pages [0, qp) of this sequence are quantized blocks (one page per stage
-    // then: the quantized path runs with block_size == SK == 16).
-    const int qp = (BITS > 0 && p.qpages) ? min(max(__ldg(p.qpages + b), 0), npages) : 0;
 
     if (tid == 0) {
         for (int i = 0; i < C::NS; ++i) {
@@ -253,8 +142,7 @@ __global__ void __launch_bounds__(kDecodeThreads, BITS ? 4 : 5)
             if (rel == 0) {
                 int pg = min(page0 + i * pps + lane, npages - 1);
                 int blk = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks + pg);
-                const int64_t nblk = (BITS > 0 && pg < qp) ? p.qpool.num_blocks : p.pool.num_blocks;
-                if (blk < 0 || blk >= nblk) {
+                if (blk < 0 || blk >= p.pool.num_blocks) {
                     report(err, KVP_DEVERR_BAD_BLOCK);
                     blk = 0;
                 }
@@ -265,27 +153,12 @@ __global__ void __launch_bounds__(kDecodeThreads, BITS ? 4 : 5)
                 ok = mbar_wait(&empty[slot], ((i / C::NS) - 1) & 1, abort_flag, err, p.wait_limit_ns);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
-            const bool qst = BITS > 0 && page0 + i < qp;
-            if (lane == 0) mbar_expect_tx(&full[slot], qst ? C::QSTAGE : C::STAGE_BYTES);
+            if (lane == 0) mbar_expect_tx(&full[slot], C::STAGE_BYTES);
             __syncwarp();
             // One lane per physical page of the stage issues that page's boxes.
             const int blk = __shfl_sync(0xffffffffu, my_blk, (rel + lane) & 31);
             uint8_t* kst = smem + slot * C::STAGE_BYTES;
             uint8_t* vst = kst + C::KBYTES;
-            if constexpr (BITS > 0) {
-                if (qst) {
-                    // A quantized page: codes and scales, four contiguous pieces.
-                    if (lane == 0) {
-                        const int64_t ph = static_cast<int64_t>(blk) * Hkv + h;
-                        bulk_load(kst, p.qpool.k_codes + ph * C::QCODE, C::QCODE, &full[slot]);
-                        bulk_load(kst + C::QOFF_V, p.qpool.v_codes + ph * C::QCODE, C::QCODE, &full[slot]);
-                        bulk_load(kst + C::QOFF_KM, p.qpool.k_meta + ph * 2 * D, 4 * D, &full[slot]);
-                        bulk_load(kst + C::QOFF_VM, p.qpool.v_meta + ph * 2 * SK, 4 * SK, &full[slot]);
-                    }
-                    issued = i + 1;
-                    continue;
-                }
-            }
             if (lane < pps) {
                 const int32_t y = (blk * Hkv + h) * BS;
 #pragma unroll
@@ -317,13 +190,6 @@ __global__ void __launch_bounds__(kDecodeThreads, BITS ? 4 : 5)
             qa[ks][1] = r1 < g ? __ldg(q32 + (qrow1 + ks * 16 + cq) / 2) : 0u;
             qa[ks][2] = r0 < g ? __ldg(q32 + (qrow0 + ks * 16 + cq + 8) / 2) : 0u;
             qa[ks][3] = r1 < g ? __ldg(q32 + (qrow1 + ks * 16 + cq + 8) / 2) : 0u;
-            if constexpr (kMma != kBF16) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float2 f = unpack2<kBF16>(qa[ks][j]);
-                    qa[ks][j] = pack2<kMma>(f.x, f.y);
-                }
-            }
         }
         const float sl2 = p.scale_log2;
 
@@ -334,26 +200,7 @@ __global__ void __launch_bounds__(kDecodeThreads, BITS ? 4 : 5)
             uint8_t* vst = kst + C::KBYTES;
             const int kbeg = key0 + i * kStageKeys;
             const int nvalid = min(kStageKeys, key1 - kbeg);
-            const bool qst = BITS > 0 && page0 + i < qp;
-            // Staged: dequantized (or converted to fp16) into this warp's own
-            // tile, after which the slot goes back at once.
-            const bool staged = BITS > 0 && (qst || kBF16);
-            if constexpr (BITS > 0) {
-                if (staged) {
-                    uint8_t* stk = smem + C::OFF_STG + warp * C::STG_BYTES;
-                    const uint32_t stk_a = smem_u32(stk);
-                    if (qst)
-                        dequant_stage<D, SK, BITS>(smem_u32(kst), stk_a, stk_a + C::KBYTES, nvalid, lane);
-                    else
-                        bf16_stage_to_f16<D, SK, BITS>(smem_u32(kst), smem_u32(vst), stk_a, stk_a + C::KBYTES, nvalid,
-                                                       lane);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[slot]);
-                    kst = stk;
-                    vst = stk + C::KBYTES;
-                }
-            }
-            if (!staged && nvalid < kStageKeys) {
+            if (nvalid < kStageKeys) {
                 // Rows past the context may hold any bytes (even NaN); P is 0
                 // there, but 0 * NaN is NaN, so clear those V rows.
                 const int vecs_per_row = C::ROWB / 16;
@@ -385,8 +232,8 @@ __global__ void __launch_bounds__(kDecodeThreads, BITS ? 4 : 5)
                                           swz_offset(key, c16 % (C::CW / 8), C::ROWB);
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4(addr, b0, b1, b2, b3);
-                    mma16816<kMma>(s[2 * np], qa[ks], b0, b1);
-                    mma16816<kMma>(s[2 * np + 1], qa[ks], b2, b3);
+                    mma16816<kBF16>(s[2 * np], qa[ks], b0, b1);
+                    mma16816<kBF16>(s[2 * np + 1], qa[ks], b2, b3);
                 }
             }
             if (nvalid < kStageKeys) {
@@ -448,10 +295,10 @@ __global__ void __launch_bounds__(kDecodeThreads, BITS ? 4 : 5)
             uint32_t pa[SK / 16][4];
 #pragma unroll
             for (int kk = 0; kk < SK / 16; ++kk) {
-                pa[kk][0] = pack2<kMma>(s[2 * kk][0], s[2 * kk][1]);
-                pa[kk][1] = pack2<kMma>(s[2 * kk][2], s[2 * kk][3]);
-                pa[kk][2] = pack2<kMma>(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-                pa[kk][3] = pack2<kMma>(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+                pa[kk][0] = pack2<kBF16>(s[2 * kk][0], s[2 * kk][1]);
+                pa[kk][1] = pack2<kBF16>(s[2 * kk][2], s[2 * kk][3]);
+                pa[kk][2] = pack2<kBF16>(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+                pa[kk][3] = pack2<kBF16>(s[2 * kk + 1][2], s[2 * kk + 1][3]);
             }
             // O += P V: V is [key][dim] in shared memory, loaded transposed.
 #pragma unroll
@@ -464,17 +311,13 @@ __global__ void __launch_bounds__(kDecodeThreads, BITS ? 4 : 5)
                                           swz_offset(key, c16 % (C::CW / 8), C::ROWB);
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4_t(addr, b0, b1, b2, b3);
-                    mma16816<kMma>(o[2 * nd2], pa[kk], b0, b1);
-                    mma16816<kMma>(o[2 * nd2 + 1], pa[kk], b2, b3);
+                    mma16816<kBF16>(o[2 * nd2], pa[kk], b0, b1);
+                    mma16816<kBF16>(o[2 * nd2 + 1], pa[kk], b2, b3);
                 }
             }
-            if (!staged) {
-                if (nvalid < kStageKeys) fence_proxy_async_smem();  // generic zeroing before the next TMA write
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[slot]);
-            } else {
-                __syncwarp();  // the tile is rewritten by the next stage's dequantization
-            }
+            if (nvalid < kStageKeys) fence_proxy_async_smem();  // generic zeroing before the next TMA write
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
         }
         // Row sums were accumulated per thread over its own columns.
         l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], 1);
@@ -554,19 +397,19 @@ __global__ void __launch_bounds__(kDecodeThreads, BITS ? 4 : 5)
     }
 }
 
-template <bool kBF16, int D, int SK, int BITS>
+template <bool kBF16, int D, int SK>
 cudaError_t launch_decode_kernel(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                  cudaStream_t stream) {
-    using C = DecodeCfg<D, SK, BITS>;
+    using C = DecodeCfg<D, SK>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<kBF16, D, SK, BITS>,
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<kBF16, D, SK>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     dim3 grid(p.max_splits, p.pool.num_kv_heads, p.B);
-    return launch_k(decode_kernel<kBF16, D, SK, BITS>, grid, kDecodeThreads, C::SMEM_BYTES, stream, tk, tv, p);
+    return launch_k(decode_kernel<kBF16, D, SK>, grid, kDecodeThreads, C::SMEM_BYTES, stream, tk, tv, p);
 }
 
 }  // namespace

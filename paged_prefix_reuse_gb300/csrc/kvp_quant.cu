@@ -8,11 +8,13 @@
 // channels -- asymmetric min/max codes with an fp16 scale rounded up and an
 // fp16 min rounded down, codes computed in fp32 against those stored values.
 //
-// Decode over the quantized prefix uses the decode kernel of
-// kvp_decode_impl.cuh with BITS = 8 or 4: a quantized page arrives as four
-// bulk copies (codes and scales, ~57% / ~32% of its 16-bit bytes at d=128)
-// and the consumer warp dequantizes it into a 16-bit tile before the same
-// tensor-core products; the live suffix's pages take the 16-bit TMA path.
+// Decode over the quantized prefix (decode_q_kernel below) keeps the 16-bit
+// decode's pipeline -- one producer warp, a 4-slot ring, two consumer warps,
+// split partials merged by merge_kernel -- but a quantized page arrives as
+// four bulk copies (codes and scales, ~57% / ~32% of its 16-bit bytes at
+// d=128) and its codes enter transposed tensor-core products straight from
+// registers, the scales folded into q and P; the live suffix's pages take the
+// 16-bit TMA path.
 #include "kvp_decode_impl.cuh"
 
 namespace kvp {
@@ -215,11 +217,646 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const uint16_t* __r
     }
 }
 
+// ---------------------------------------------------------------------------
+// Decode over a quantized cached prefix.
+//
+// The products run transposed: S^T = K q^T (keys as the MMA's M dimension,
+// the query heads of the group as N = 8) and O^T = V^T P^T (channels as M),
+// so a lane's O accumulators are 32 floats at d = 128 instead of 64, and the
+// codes enter the tensor core straight from registers, with no dequantized
+// tile in shared memory:
+//  * K (per-channel scale s_c and min z_c over the page's tokens):
+//      q.k_t = sum_c q_c s_c code_tc + sum_c q_c z_c.
+//    The codes become fp16 subnormals (code * 2^-24, exact: the code is the
+//    mantissa) by one byte permute per pair; q_c s_c is formed once per page
+//    as an unevaluated sum hi + lo of two fp16 values (hi = q s rounded,
+//    lo = q s - hi by one fused multiply-add, so the pair carries ~20 bits),
+//    each multiplied by the codes; a third product with every key row equal
+//    to z gives the sum q.z.  S = 2^24 * (first + second) + (third).
+//  * V (per-token scale sv_t and min zv_t):
+//      sum_t P_t v_tc = sum_t (P_t sv_t) code_tc + sum_t P_t zv_t.
+//    The codes become fp16 1024 + code (one byte permute per pair, exact);
+//    P' = P sv is rounded to fp16 for the product, and the row's scalar
+//    sum_t (P_t zv_t - 1024 P'_t) is accumulated beside O and added at the end.
+//  * The live suffix's 16-bit pages use the same products with s = 1, z = 0
+//    and no offset (fp16 operands, a bf16 pool's values converted).
+// K's contraction runs over the channels in any order, so each lane takes
+// whole runs of channels (8 bits: pairs (c, c+1); 4 bits: pairs (c, c+4),
+// which a mask of the code word yields directly); q, s and z are paired
+// alike.  The row maximum is exact (no lazy threshold), so P <= 1 and P sv
+// stays in fp16 range for any stored scale.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 16-bit matrix held as one row per four lanes (lane l:
+// row l / 4, columns 2 (l % 4) and 2 (l % 4) + 1), returned in the same layout.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
+    return v;
+}
+
+// NB bytes from the shared address a (a multiple of AL) into words, with the
+// widest accesses that AL allows.
+template <int NB, int AL>
+__device__ __forceinline__ void lds_bytes(uint32_t a, uint32_t (&w)[(NB + 3) / 4]) {
+    if constexpr (AL >= 16 && NB % 16 == 0) {
+#pragma unroll
+        for (int i = 0; i < NB / 16; ++i) {
+            const uint4 v = lds128(a + 16 * i);
+            w[4 * i] = v.x;
+            w[4 * i + 1] = v.y;
+            w[4 * i + 2] = v.z;
+            w[4 * i + 3] = v.w;
+        }
+    } else if constexpr (AL >= 8 && NB % 8 == 0) {
+#pragma unroll
+        for (int i = 0; i < NB / 8; ++i) {
+            const uint2 v = lds64(a + 8 * i);
+            w[2 * i] = v.x;
+            w[2 * i + 1] = v.y;
+        }
+    } else if constexpr (AL >= 4 && NB % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < NB / 4; ++i) w[i] = lds32(a + 4 * i);
+    } else {
+        static_assert(NB % 2 == 0, "whole 16-bit pieces");
+#pragma unroll
+        for (int i = 0; i < (NB + 3) / 4; ++i) w[i] = 0u;
+#pragma unroll
+        for (int i = 0; i < NB / 2; ++i) w[i / 2] |= lds16(a + 2 * i) << (16 * (i % 2));
+    }
+}
+
+constexpr int lowest_align(int n) { return (n & -n) >= 16 ? 16 : (n & -n); }
+
+// Two consumer warps and a producer per CTA, five CTAs per SM (registers
+// allow no more).  Measured on the mixed batch's decode: four consumer warps
+// at three CTAs per SM ran 1.3x slower.
+constexpr int kDecodeQConsumers = 2;
+constexpr int kDecodeQCtasPerSm = 5;
+
+template <int D, int BITS>
+struct QDec {
+    static constexpr int SK = 16;         // keys per stage: one 16-token page
+    static constexpr int KS = D / 16;     // k-steps of S^T, m-tiles of O^T
+    static constexpr int KCH = D / 4;     // K channels of a lane (quarter lane % 4)
+    static constexpr int VCH = D / 8;     // V channels of a lane (eighth lane / 4)
+    static constexpr int CROW = D * BITS / 8;
+    static constexpr int KCB = KCH * BITS / 8;  // code bytes of a lane's K channels, per key
+    static constexpr int VCB = VCH * BITS / 8;  // the same for V
+    static constexpr int KAL = lowest_align(KCB), VAL = lowest_align(VCB);
+    // A 16-bit stage is half a page (HK keys): K then V, each in the swizzled
+    // TMA layout of the 16-bit decode kernel (chunk columns of CW channels).
+    static constexpr int HK = kDecodeQHalfRows;
+    static constexpr int CW = chunk_elems(D), ROWB = 2 * CW, NCH = D / CW, HREGION = HK * ROWB;
+    static constexpr int HKBYTES = HK * D * 2;
+    // A quantized stage is one page: K codes, V codes, K meta (scale row, min
+    // row), V meta ((scale, min) per token), all meta fp16.
+    static constexpr int QCODE = SK * CROW;
+    static constexpr int QOFF_V = QCODE, QOFF_KM = 2 * QCODE, QOFF_VM = 2 * QCODE + 4 * D;
+    static constexpr int QSTAGE = 2 * QCODE + 4 * D + 4 * SK;
+    // Slots hold either kind of stage and start on 1024-byte boundaries (the
+    // swizzled TMA tiles need it).
+    static constexpr int SLOT = ((QSTAGE > 2 * HKBYTES ? QSTAGE : 2 * HKBYTES) + 1023) / 1024 * 1024;
+    // Eight slots, four per consumer warp: a stage's copies are in flight for
+    // a microsecond or more, so a consumer needs several stages ahead.
+    static constexpr int NS = 8;
+    static constexpr int QC = kDecodeQConsumers;  // consumer warps; warp QC is the producer
+    static constexpr int THREADS = (QC + 1) * 32;
+    static_assert(NS % QC == 0, "every slot has one owner warp");
+    static constexpr int RED_FLOATS = 4 * KS + 6;  // per lane: O^T, then (m, l, bias) of its two rows
+    static_assert(32 * RED_FLOATS * 4 * (QC - 1) <= NS * SLOT, "the combine fits the ring");
+    static constexpr int RING_BYTES = NS * SLOT;
+    static constexpr int OFF_BAR = RING_BYTES;
+    static constexpr int SMEM_BYTES = OFF_BAR + (2 * NS + 1) * 8 + 16 + 1024;
+};
+
+// Pairs of the contraction for the 8 consecutive K channels in w[0..3]
+// (16-bit values, two per word): o[e][0] and o[e][1] feed k-step 2u + e as
+// the pairs of MMA rows (2t, 2t+1) and (2t+8, 2t+9).  8 bits pair (c, c+1),
+// 4 bits pair (c, c+4) (channels relative to the run).
+template <int BITS>
+__device__ __forceinline__ void pair_words(const uint32_t (&w)[4], uint32_t (&o)[2][2]) {
+    if constexpr (BITS == 8) {
+        o[0][0] = w[0];
+        o[0][1] = w[1];
+        o[1][0] = w[2];
+        o[1][1] = w[3];
+    } else {
+        o[0][0] = __byte_perm(w[0], w[2], 0x5410);
+        o[0][1] = __byte_perm(w[0], w[2], 0x7632);
+        o[1][0] = __byte_perm(w[1], w[3], 0x5410);
+        o[1][1] = __byte_perm(w[1], w[3], 0x7632);
+    }
+}
+
+// The same pairs from codes, as fp16 subnormals code * 2^-24: 8 bits, the
+// two code words of the run; 4 bits, its one word of eight nibbles (the even
+// channel of a byte in the low nibble).
+template <int BITS>
+__device__ __forceinline__ void code_pairs(const uint32_t* c, uint32_t (&o)[2][2]) {
+    if constexpr (BITS == 8) {
+        o[0][0] = __byte_perm(c[0], 0u, 0x4140);
+        o[0][1] = __byte_perm(c[0], 0u, 0x4342);
+        o[1][0] = __byte_perm(c[1], 0u, 0x4140);
+        o[1][1] = __byte_perm(c[1], 0u, 0x4342);
+    } else {
+        constexpr uint32_t M = 0x000F000Fu;
+        o[0][0] = c[0] & M;
+        o[0][1] = (c[0] >> 4) & M;
+        o[1][0] = (c[0] >> 8) & M;
+        o[1][1] = (c[0] >> 12) & M;
+    }
+}
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    const float2 f = unpack2<true>(w);
+    return pack2<false>(f.x, f.y);
+}
+
+// V^T operand pairs for m-tile mt of keys (A, B) = (2t, 2t+1) or (2t+8, 2t+9):
+// (1024 + code_A, 1024 + code_B) at the lane's channels 2 mt and 2 mt + 1.
+template <int BITS>
+__device__ __forceinline__ void v_code_pairs(const uint32_t* wa, const uint32_t* wb, int mt, uint32_t& lo,
+                                             uint32_t& hi) {
+    if constexpr (BITS == 8) {
+        const int j = mt >> 1;
+        const uint32_t t = (mt & 1) ? __byte_perm(wa[j], wb[j], 0x7362) : __byte_perm(wa[j], wb[j], 0x5140);
+        lo = magic_pair(t, 0x4140);
+        hi = magic_pair(t, 0x4342);
+    } else {
+        const int j = mt >> 2, i = mt & 3;
+        const uint32_t sel = i | (i << 4) | ((4 + i) << 8) | ((4 + i) << 12);
+        const uint32_t x = __byte_perm(wa[j], wb[j], sel);
+        lo = (x & 0x000F000Fu) | 0x64006400u;
+        hi = ((x >> 4) & 0x000F000Fu) | 0x64006400u;
+    }
+}
+
+template <bool kBF16, int D, int BITS>
+__global__ void __launch_bounds__(QDec<D, BITS>::THREADS, kDecodeQCtasPerSm)
+    decode_q_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                    const DecodeParams p) {
+    using C = QDec<D, BITS>;
+    static_assert(BITS == 4 || BITS == 8, "bits");
+    constexpr int KS = C::KS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* empty = full + C::NS;
+    uint64_t* stall = empty + C::NS;  // nothing arrives on it (KVP_LAUNCH_STALL_TEST)
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(stall + 1);
+
+    // blockIdx.x = split * ngrp + row block (8 query heads of the group each).
+    const int g = p.group;
+    const int ngrp = (g + 7) >> 3;
+    const int sp = blockIdx.x / ngrp, r_base = 8 * (blockIdx.x - sp * ngrp);
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_trigger();
+    const int Hkv = p.pool.num_kv_heads;
+    uint32_t* err = p.pool.err_word;
+
+    const int L = __ldg(p.context_lens + b);
+    const int npages = (L + C::SK - 1) / C::SK;
+    if (L < 1 || npages > p.max_blocks) {
+        if (sp == 0 && r_base == 0 && tid == 0) report(err, KVP_DEVERR_BAD_LEN);
+        pdl_wait();  // every CTA waits, so the grid completes after the one before
+        return;
+    }
+    const int page0 = sp * p.pages_per_split;
+    if (page0 >= npages) {
+        pdl_wait();
+        return;
+    }
+    const int page1 = min(npages, page0 + p.pages_per_split);
+    const int key1 = min(L, page1 * C::SK);
+    // Pages [0, qp) of this sequence are quantized blocks.  Stages: one per
+    // quantized page of the split ([page0, qend)), then one per half of each
+    // 16-bit page that holds keys of the context.
+    const int qp = p.qpages ? min(max(__ldg(p.qpages + b), 0), npages) : 0;
+    const int qend = min(page1, max(page0, qp));
+    const int nq = qend - page0;
+    const int nstages = nq + max(0, (key1 - qend * C::SK + C::HK - 1) / C::HK);
+
+    if (tid == 0) {
+        for (int i = 0; i < C::NS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(stall, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // Lane roles: t = lane % 4 picks the rows 2t, 2t+1 of S^T / O^T (query
+    // heads r_base + 2t, + 1), the K channel quarter and the keys 2t, 2t+1,
+    // 2t+8, 2t+9 of the V operand; u = lane / 4 picks the keys u, u+8 of the
+    // K operand, the query head r_base + u of the q operand and the V channel
+    // eighth.
+    const int u = lane >> 2, t = lane & 3;
+    float o[KS][4];
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_run[2] = {0.f, 0.f};
+    float bias[2] = {0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+    if (warp == C::QC) {
+        // ------------------------------ producer ------------------------------
+        if (lane == 0) {
+            prefetch_tmap(&tmap_k);
+            prefetch_tmap(&tmap_v);
+        }
+        pdl_wait();  // pool contents from the kernel before are read from here on
+        const bool stalled = p.stall_test && !stall_wait(stall, abort_flag, err, p.wait_limit_ns);
+        int my_blk = 0;
+        int issued = 0;
+        for (int i = 0; i < nstages && !stalled; ++i) {
+            const int slot = i % C::NS;
+            if ((i & 31) == 0) {
+                // Block ids of the pages of the next 32 stages, one per lane.
+                const int si = i + lane;
+                const int pg = min(si < nq ? page0 + si : qend + (si - nq) / 2, npages - 1);
+                int blk = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks + pg);
+                const int64_t nblk = pg < qp ? p.qpool.num_blocks : p.pool.num_blocks;
+                if (blk < 0 || blk >= nblk) {
+                    report(err, KVP_DEVERR_BAD_BLOCK);
+                    blk = 0;
+                }
+                my_blk = blk;
+            }
+            int ok = 1;
+            if (lane == 0 && i >= C::NS)
+                ok = mbar_wait(&empty[slot], ((i / C::NS) - 1) & 1, abort_flag, err, p.wait_limit_ns);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            const int blk = __shfl_sync(0xffffffffu, my_blk, i & 31);
+            if (lane == 0) {
+                uint8_t* st = smem + slot * C::SLOT;
+                if (i < nq) {
+                    // A quantized page: codes and scales, four contiguous pieces.
+                    const int64_t ph = static_cast<int64_t>(blk) * Hkv + h;
+                    mbar_expect_tx(&full[slot], C::QSTAGE);
+                    bulk_load(st, p.qpool.k_codes + ph * C::QCODE, C::QCODE, &full[slot]);
+                    bulk_load(st + C::QOFF_V, p.qpool.v_codes + ph * C::QCODE, C::QCODE, &full[slot]);
+                    bulk_load(st + C::QOFF_KM, p.qpool.k_meta + ph * 2 * D, 4 * D, &full[slot]);
+                    bulk_load(st + C::QOFF_VM, p.qpool.v_meta + ph * 2 * C::SK, 4 * C::SK, &full[slot]);
+                } else {
+                    // Half (i - nq) % 2 of a 16-bit page: rows of HK keys.
+                    const int32_t y = (blk * Hkv + h) * C::SK + ((i - nq) & 1) * C::HK;
+                    mbar_expect_tx(&full[slot], 2 * C::HKBYTES);
+#pragma unroll
+                    for (int c = 0; c < C::NCH; ++c) {
+                        tma_load_2d(st + c * C::HREGION, &tmap_k, c * C::CW, y, &full[slot]);
+                        tma_load_2d(st + C::HKBYTES + c * C::HREGION, &tmap_v, c * C::CW, y, &full[slot]);
+                    }
+                }
+            }
+            issued = i + 1;
+        }
+        // Do not leave while copies may still land in shared memory.
+        if (lane == 0) {
+            for (int i = max(0, issued - C::NS); i < issued; ++i) {
+                volatile int no_abort = 0;
+                mbar_wait(&full[i % C::NS], (i / C::NS) & 1, &no_abort, err);
+            }
+        }
+    } else {
+        // ------------------------------ consumers ------------------------------
+        // q operand: query head r_base + u (zero past the group), the lane's
+        // K channel quarter, paired as the codes are; fp16 whatever the pool.
+        uint32_t qb[KS][2];
+        {
+            const int r = r_base + u;
+            const bool live = r < g;
+            const uint4* qrow = reinterpret_cast<const uint4*>(
+                static_cast<const uint8_t*>(p.q) +
+                ((static_cast<int64_t>(b) * p.num_q_heads + h * g + (live ? r : 0)) * D + t * C::KCH) * 2);
+#pragma unroll
+            for (int k = 0; k < C::KCH / 8; ++k) {
+                const uint4 v = live ? __ldg(qrow + k) : make_uint4(0u, 0u, 0u, 0u);
+                uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                if constexpr (kBF16) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) w[j] = bf16x2_to_f16x2(w[j]);
+                }
+                uint32_t pr[2][2];
+                pair_words<BITS>(w, pr);
+                qb[2 * k][0] = pr[0][0];
+                qb[2 * k][1] = pr[0][1];
+                qb[2 * k + 1][0] = pr[1][0];
+                qb[2 * k + 1][1] = pr[1][1];
+            }
+        }
+        const float sl2 = p.scale_log2;
+
+        for (int i = warp; i < nstages; i += C::QC) {
+            const int slot = i % C::NS;
+            if (!mbar_wait(&full[slot], (i / C::NS) & 1, abort_flag, err, p.wait_limit_ns)) break;
+            const uint32_t sb = smem_u32(smem + slot * C::SLOT);
+            const bool qst = i < nq;
+            const int kb = qst ? (page0 + i) * C::SK : qend * C::SK + (i - nq) * C::HK;  // first key
+            const int nvalid = min(qst ? C::SK : C::HK, key1 - kb);  // >= 1
+
+            // ---- S^T = K q^T (rows: keys u, u+8; columns: query heads 2t, 2t+1) ----
+            float s[4] = {0.f, 0.f, 0.f, 0.f};
+            if (qst) {
+                constexpr int KW = (C::KCB + 3) / 4;
+                uint32_t c0[KW], c1[KW];
+                lds_bytes<C::KCB, C::KAL>(sb + u * C::CROW + t * C::KCB, c0);
+                lds_bytes<C::KCB, C::KAL>(sb + (u + 8) * C::CROW + t * C::KCB, c1);
+                uint32_t sw[C::KCH / 2], zw[C::KCH / 2];
+                lds_bytes<C::KCH * 2, 16>(sb + C::QOFF_KM + t * C::KCH * 2, sw);
+                lds_bytes<C::KCH * 2, 16>(sb + C::QOFF_KM + 2 * D + t * C::KCH * 2, zw);
+                float sl[4] = {0.f, 0.f, 0.f, 0.f}, sz[4] = {0.f, 0.f, 0.f, 0.f};
+                constexpr int CWU = BITS == 8 ? 2 : 1;  // code words per 8-channel run
+#pragma unroll
+                for (int k = 0; k < C::KCH / 8; ++k) {
+                    uint32_t a0[2][2], a1[2][2], sp2[2][2], zp2[2][2];
+                    code_pairs<BITS>(c0 + CWU * k, a0);
+                    code_pairs<BITS>(c1 + CWU * k, a1);
+                    const uint32_t s4[4] = {sw[4 * k], sw[4 * k + 1], sw[4 * k + 2], sw[4 * k + 3]};
+                    const uint32_t z4[4] = {zw[4 * k], zw[4 * k + 1], zw[4 * k + 2], zw[4 * k + 3]};
+                    pair_words<BITS>(s4, sp2);
+                    pair_words<BITS>(z4, zp2);
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int ks = 2 * k + e;
+                        const __half2 x0 = *reinterpret_cast<const __half2*>(&qb[ks][0]);
+                        const __half2 x1 = *reinterpret_cast<const __half2*>(&qb[ks][1]);
+                        const __half2 y0 = *reinterpret_cast<const __half2*>(&sp2[e][0]);
+                        const __half2 y1 = *reinterpret_cast<const __half2*>(&sp2[e][1]);
+                        const __half2 h0 = __hmul2(x0, y0), h1 = __hmul2(x1, y1);
+                        const __half2 l0 = __hfma2(x0, y0, __hneg2(h0)), l1 = __hfma2(x1, y1, __hneg2(h1));
+                        mma_f16(s, a0[e][0], a1[e][0], a0[e][1], a1[e][1], *reinterpret_cast<const uint32_t*>(&h0),
+                                *reinterpret_cast<const uint32_t*>(&h1));
+                        mma_f16(sl, a0[e][0], a1[e][0], a0[e][1], a1[e][1], *reinterpret_cast<const uint32_t*>(&l0),
+                                *reinterpret_cast<const uint32_t*>(&l1));
+                        mma_f16(sz, zp2[e][0], zp2[e][0], zp2[e][1], zp2[e][1], qb[ks][0], qb[ks][1]);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[e] = fmaf(s[e] + sl[e], 16777216.f, sz[e]);
+            } else {
+                // Keys u of the half page; MMA rows u + 8 stay zero (masked below).
+#pragma unroll
+                for (int k = 0; k < C::KCH / 8; ++k) {
+                    const int c = t * C::KCH + 8 * k;  // first channel of the run
+                    const uint4 x0 = lds128(sb + (c / C::CW) * C::HREGION + swz_offset(u, (c % C::CW) / 8, C::ROWB));
+                    uint32_t w0[4] = {x0.x, x0.y, x0.z, x0.w};
+                    if constexpr (kBF16) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) w0[j] = bf16x2_to_f16x2(w0[j]);
+                    }
+                    uint32_t a0[2][2];
+                    pair_words<BITS>(w0, a0);
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        mma_f16(s, a0[e][0], 0u, a0[e][1], 0u, qb[2 * k + e][0], qb[2 * k + e][1]);
+                }
+            }
+
+            // ---- V operand loads (issued before the softmax) ----
+            constexpr int VW = (C::VCB + 3) / 4;
+            uint32_t va[VW], vb[VW], vc[VW], vd[VW];  // keys 2t, 2t+1, 2t+8, 2t+9
+            uint32_t vm0 = 0u, vm1 = 0u;              // (scale, min) of keys u, u+8
+            if (qst) {
+                const uint32_t vbase = sb + C::QOFF_V + u * C::VCB;
+                lds_bytes<C::VCB, C::VAL>(vbase + (2 * t) * C::CROW, va);
+                lds_bytes<C::VCB, C::VAL>(vbase + (2 * t + 1) * C::CROW, vb);
+                lds_bytes<C::VCB, C::VAL>(vbase + (2 * t + 8) * C::CROW, vc);
+                lds_bytes<C::VCB, C::VAL>(vbase + (2 * t + 9) * C::CROW, vd);
+                vm0 = lds32(sb + C::QOFF_VM + 4 * u);
+                vm1 = lds32(sb + C::QOFF_VM + 4 * (u + 8));
+            }
+
+            // ---- online softmax over the stage's keys (log2 domain) ----
+            if (u >= nvalid) s[0] = s[1] = -INFINITY;
+            if (u + 8 >= nvalid) s[2] = s[3] = -INFINITY;
+            float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+            for (int x = 4; x < 32; x <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, x));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, x));
+            }
+            const float mx0s = mx0 * sl2, mx1s = mx1 * sl2;
+            float a0 = 1.f, a1 = 1.f;
+            if (mx0s > m_run[0]) {
+                a0 = fast_exp2(m_run[0] - mx0s);
+                m_run[0] = mx0s;
+            }
+            if (mx1s > m_run[1]) {
+                a1 = fast_exp2(m_run[1] - mx1s);
+                m_run[1] = mx1s;
+            }
+            if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    o[mt][0] *= a0;
+                    o[mt][2] *= a0;
+                    o[mt][1] *= a1;
+                    o[mt][3] *= a1;
+                }
+                l_run[0] *= a0;
+                l_run[1] *= a1;
+                bias[0] *= a0;
+                bias[1] *= a1;
+            }
+            const float pr0 = fast_exp2(fmaf(s[0], sl2, -m_run[0]));
+            const float pr1 = fast_exp2(fmaf(s[1], sl2, -m_run[1]));
+            const float pr2 = fast_exp2(fmaf(s[2], sl2, -m_run[0]));
+            const float pr3 = fast_exp2(fmaf(s[3], sl2, -m_run[1]));
+            l_run[0] += pr0 + pr2;
+            l_run[1] += pr1 + pr3;
+
+            // ---- O^T += V^T P^T ----
+            uint32_t pk0, pk1;  // (key u | u+8; query heads 2t, 2t+1)
+            if (qst) {
+                float2 m0 = unpack2<false>(vm0), m1 = unpack2<false>(vm1);  // (scale, min)
+                if (u >= nvalid) m0 = make_float2(0.f, 0.f);  // meta past the context is never used
+                if (u + 8 >= nvalid) m1 = make_float2(0.f, 0.f);
+                pk0 = pack2<false>(pr0 * m0.x, pr1 * m0.x);
+                pk1 = pack2<false>(pr2 * m1.x, pr3 * m1.x);
+                const float2 r0 = unpack2<false>(pk0), r1 = unpack2<false>(pk1);
+                bias[0] += fmaf(pr0, m0.y, pr2 * m1.y) - 1024.f * (r0.x + r1.x);
+                bias[1] += fmaf(pr1, m0.y, pr3 * m1.y) - 1024.f * (r0.y + r1.y);
+            } else {
+                pk0 = pack2<false>(pr0, pr1);
+                pk1 = pack2<false>(pr2, pr3);
+            }
+            const uint32_t pb0 = movmatrix_t(pk0), pb1 = movmatrix_t(pk1);  // P'^T: keys 2t.. / 2t+8..; head u
+            if (qst) {
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    uint32_t x0, x1, x2, x3;
+                    v_code_pairs<BITS>(va, vb, mt, x0, x1);
+                    v_code_pairs<BITS>(vc, vd, mt, x2, x3);
+                    mma_f16(o[mt], x0, x1, x2, x3, pb0, pb1);
+                }
+            } else {
+                // The lane's V channels of keys 2t, 2t+1 of the half page, four
+                // at a time; keys past the context (any bytes, even NaN) read as
+                // 0, and keys 2t+8, 2t+9 (past the half) are 0.
+#pragma unroll
+                for (int k = 0; k < C::VCH / 4; ++k) {
+                    const int c = u * C::VCH + 4 * k;
+                    const uint32_t a = sb + C::HKBYTES + (c / C::CW) * C::HREGION + ((c / 4) & 1) * 8;
+                    uint32_t w[2][2];
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        uint2 x = lds64(a + swz_offset(2 * t + j, (c % C::CW) / 8, C::ROWB));
+                        if (2 * t + j >= nvalid) x = make_uint2(0u, 0u);
+                        if constexpr (kBF16) {
+                            x.x = bf16x2_to_f16x2(x.x);
+                            x.y = bf16x2_to_f16x2(x.y);
+                        }
+                        w[j][0] = x.x;
+                        w[j][1] = x.y;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        mma_f16(o[2 * k + e], __byte_perm(w[0][e], w[1][e], 0x5410),
+                                __byte_perm(w[0][e], w[1][e], 0x7632), 0u, 0u, pb0, pb1);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+        // Row sums and offsets were accumulated per lane over its keys.
+#pragma unroll
+        for (int x = 4; x < 32; x <<= 1) {
+            l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], x);
+            l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], x);
+            bias[0] += __shfl_xor_sync(0xffffffffu, bias[0], x);
+            bias[1] += __shfl_xor_sync(0xffffffffu, bias[1], x);
+        }
+    }
+
+    if (warp == C::QC) return;
+
+    // ------------------------------ epilogue ------------------------------
+    // Lane: query heads r_base + 2t + j (j = 0, 1); channels u*VCH + 2 mt and
+    // + 1 in o[mt][j] and o[mt][j + 2].  The consumer warps combine through
+    // shared memory (all stages are consumed once every consumer passes the
+    // first barrier, so the ring is free); warp 0 writes the CTA's result:
+    // the output rows, or with splits one normalised partial (O, log2 lse).
+    float* red = reinterpret_cast<float*>(smem);  // [QC - 1][RED_FLOATS][32 lanes]
+    asm volatile("bar.sync 1, %0;" ::"r"(C::QC * 32) : "memory");
+    if (warp > 0) {
+        float* w = red + (warp - 1) * C::RED_FLOATS * 32 + lane;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w[(4 * mt + e) * 32] = o[mt][e];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            w[(4 * KS + 3 * j) * 32] = m_run[j];
+            w[(4 * KS + 3 * j + 1) * 32] = l_run[j];
+            w[(4 * KS + 3 * j + 2) * 32] = bias[j];
+        }
+    }
+    // Every consumer warp always reaches both barriers (even after a
+    // timed-out wait), so none can be left waiting for another.
+    asm volatile("bar.sync 1, %0;" ::"r"(C::QC * 32) : "memory");
+    if (warp != 0 || *abort_flag) return;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int r = r_base + 2 * t + j;
+        if (r >= g) continue;
+        float M = m_run[j];
+#pragma unroll
+        for (int w = 1; w < C::QC; ++w) M = fmaxf(M, red[((w - 1) * C::RED_FLOATS + 4 * KS + 3 * j) * 32 + lane]);
+        float f[C::QC];
+        float lsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < C::QC; ++w) {
+            const float mw = w == 0 ? m_run[j] : red[((w - 1) * C::RED_FLOATS + 4 * KS + 3 * j) * 32 + lane];
+            const float lw = w == 0 ? l_run[j] : red[((w - 1) * C::RED_FLOATS + 4 * KS + 3 * j + 1) * 32 + lane];
+            f[w] = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
+            lsum = fmaf(lw, f[w], lsum);
+        }
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        const float lse2 = lsum > 0.f ? M + __log2f(lsum) : -INFINITY;
+        float x[KS][2];
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            x[mt][0] = (o[mt][j] + bias[j]) * f[0];
+            x[mt][1] = (o[mt][j + 2] + bias[j]) * f[0];
+        }
+#pragma unroll
+        for (int w = 1; w < C::QC; ++w) {
+            const float* rw = red + (w - 1) * C::RED_FLOATS * 32 + lane;
+            const float bw = rw[(4 * KS + 3 * j + 2) * 32];
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                x[mt][0] = fmaf(rw[(4 * mt + j) * 32] + bw, f[w], x[mt][0]);
+                x[mt][1] = fmaf(rw[(4 * mt + j + 2) * 32] + bw, f[w], x[mt][1]);
+            }
+        }
+        const int64_t row = static_cast<int64_t>(b) * p.num_q_heads + h * g + r;
+        if (p.max_splits > 1) {
+            float4* dst = reinterpret_cast<float4*>(p.ws_o + (row * p.max_splits + sp) * D + u * C::VCH);
+#pragma unroll
+            for (int k = 0; k < KS / 2; ++k)
+                dst[k] = make_float4(x[2 * k][0] * inv, x[2 * k][1] * inv, x[2 * k + 1][0] * inv,
+                                     x[2 * k + 1][1] * inv);
+            if (u == 0) p.ws_lse[row * p.max_splits + sp] = lse2;
+            continue;
+        }
+        uint32_t wv[KS];
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) wv[mt] = pack2<kBF16>(x[mt][0] * inv, x[mt][1] * inv);
+        uint8_t* dst = static_cast<uint8_t*>(p.out) + (row * D + u * C::VCH) * 2;
+        if constexpr (KS % 4 == 0) {
+#pragma unroll
+            for (int k = 0; k < KS / 4; ++k)
+                reinterpret_cast<uint4*>(dst)[k] = make_uint4(wv[4 * k], wv[4 * k + 1], wv[4 * k + 2], wv[4 * k + 3]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < KS / 2; ++k) reinterpret_cast<uint2*>(dst)[k] = make_uint2(wv[2 * k], wv[2 * k + 1]);
+        }
+        if (u == 0 && p.lse) p.lse[static_cast<int64_t>(h * g + r) * p.B + b] = lse2 * 0.69314718055994531f;
+    }
+}
+
+template <bool kBF16, int D, int BITS>
+cudaError_t launch_decode_q(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                            cudaStream_t stream) {
+    using C = QDec<D, BITS>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(decode_q_kernel<kBF16, D, BITS>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int ngrp = (p.group + 7) / 8;
+    dim3 grid(p.max_splits * ngrp, p.pool.num_kv_heads, p.B);
+    return launch_k(decode_q_kernel<kBF16, D, BITS>, grid, C::THREADS, C::SMEM_BYTES, stream, tk, tv, p);
+}
+
 template <bool kBF16, int D>
 cudaError_t launch_decode_q_d(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                               cudaStream_t stream) {
-    return p.qpool.bits == 8 ? launch_decode_kernel<kBF16, D, 16, 8>(p, tk, tv, stream)
-                             : launch_decode_kernel<kBF16, D, 16, 4>(p, tk, tv, stream);
+    return p.qpool.bits == 8 ? launch_decode_q<kBF16, D, 8>(p, tk, tv, stream)
+                             : launch_decode_q<kBF16, D, 4>(p, tk, tv, stream);
 }
 
 template <bool kBF16, int BITS, int D>
