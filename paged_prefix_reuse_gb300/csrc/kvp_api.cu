@@ -60,6 +60,28 @@ kvp_status make_pool_map(CUtensorMap* map, void* base, const kvp_pool* pool, int
     return r == CUDA_SUCCESS ? KVP_OK : KVP_ERR_CUDA;
 }
 
+// A code array of a quantized pool as a 2-D tensor of one row of codes per
+// token (head_dim * bits / 8 bytes), boxes of one page-head.  Rows of 128 or
+// 64 bytes land with the matching swizzle, other widths unswizzled.
+kvp_status make_code_map(CUtensorMap* map, void* base, const kvp_qpool* qp) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return KVP_ERR_CUDA;
+    const int crow = qp->head_dim * qp->bits / 8;
+    const cuuint64_t rows = static_cast<cuuint64_t>(qp->num_blocks) * qp->num_kv_heads * qp->block_size;
+    if (rows >= (cuuint64_t(1) << 31)) return KVP_ERR_INVALID_ARG;  // TMA row coordinates are int32
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(crow), rows};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(crow)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(crow), static_cast<cuuint32_t>(qp->block_size)};
+    cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapSwizzle swz = crow == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : crow == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                : CU_TENSOR_MAP_SWIZZLE_NONE;
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? KVP_OK : KVP_ERR_CUDA;
+}
+
 kvp_status check_pool(const kvp_pool* pool) {
     if (!pool || !pool->k_pool || !pool->v_pool) return KVP_ERR_INVALID_ARG;
     if (!aligned16(pool->k_pool) || !aligned16(pool->v_pool)) return KVP_ERR_INVALID_ARG;
@@ -469,8 +491,13 @@ static kvp_status decode_common(const kvp_pool* pool, const kvp_qpool* qpool, co
     const int rows = qpool ? kDecodeQHalfRows : 0;
     if ((st = make_pool_map(&tk, pool->k_pool, pool, 0, rows)) != KVP_OK) return st;
     if ((st = make_pool_map(&tv, pool->v_pool, pool, 0, rows)) != KVP_OK) return st;
+    CUtensorMap tkc, tvc;
+    if (qpool) {
+        if ((st = make_code_map(&tkc, qpool->k_codes, qpool)) != KVP_OK) return st;
+        if ((st = make_code_map(&tvc, qpool->v_codes, qpool)) != KVP_OK) return st;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = qpool ? launch_decode_attn_q(p, tk, tv, s) : launch_decode_attn(p, tk, tv, s);
+    cudaError_t e = qpool ? launch_decode_attn_q(p, tk, tv, tkc, tvc, s) : launch_decode_attn(p, tk, tv, s);
     if (e != cudaSuccess) return KVP_ERR_CUDA;
     if (p.max_splits > 1)
         e = launch_merge(p.ws_o, p.ws_lse, B * num_q_heads, num_q_heads, pool->head_dim, p.max_splits, pool->dtype,

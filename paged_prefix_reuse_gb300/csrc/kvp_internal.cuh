@@ -110,9 +110,11 @@ cudaError_t launch_block_copy(const PoolView& pool, void* k_pool, void* v_pool, 
                               cudaStream_t stream);
 cudaError_t launch_quantize_blocks(const PoolView& pool, const void* k_pool, const void* v_pool,
                                    const QPoolView& qpool, const int32_t* pairs, int32_t n, cudaStream_t stream);
-// tk, tv: boxes of kDecodeQHalfRows rows (half a 16-token block).
+// tk, tv: boxes of kDecodeQHalfRows rows (half a 16-token block) of the
+// 16-bit pool; tkc, tvc: the quantized pool's code arrays, boxes of one
+// page-head of code rows.
 cudaError_t launch_decode_attn_q(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                                 cudaStream_t stream);
+                                 const CUtensorMap& tkc, const CUtensorMap& tvc, cudaStream_t stream);
 constexpr int kDecodeQHalfRows = 8;
 cudaError_t launch_kv_deviation(const PoolView& pool, const void* k_pool, const void* v_pool, const void* k_fresh,
                                 const void* v_fresh, const int64_t* slots, int32_t T, float* dev, cudaStream_t stream);

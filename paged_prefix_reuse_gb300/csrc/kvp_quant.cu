@@ -270,14 +270,29 @@ __device__ __forceinline__ uint32_t lds16(uint32_t a) {
     return v;
 }
 
-// NB bytes from the shared address a (a multiple of AL) into words, with the
-// widest accesses that AL allows.
-template <int NB, int AL>
-__device__ __forceinline__ void lds_bytes(uint32_t a, uint32_t (&w)[(NB + 3) / 4]) {
+// Byte offset of byte x of code row r in a tile of code rows written by TMA:
+// rows of 128 or 64 bytes carry the matching swizzle (the 16-byte chunks of a
+// row permuted), other widths none.
+template <int CROW>
+__device__ __forceinline__ uint32_t code_off(uint32_t r, uint32_t x) {
+    if constexpr (CROW == 128) {
+        return r * 128u + ((((x >> 4) ^ (r & 7u)) << 4) | (x & 15u));
+    } else if constexpr (CROW == 64) {
+        return r * 64u + ((((x >> 4) ^ ((r >> 1) & 3u)) << 4) | (x & 15u));
+    } else {
+        return r * CROW + x;
+    }
+}
+
+// NB bytes of code row r from byte x (x a multiple of AL) of the tile at
+// shared address a into words, with the widest accesses that AL allows; no
+// access crosses a 16-byte chunk.
+template <int NB, int AL, int CROW>
+__device__ __forceinline__ void lds_code(uint32_t a, int r, int x, uint32_t (&w)[(NB + 3) / 4]) {
     if constexpr (AL >= 16 && NB % 16 == 0) {
 #pragma unroll
         for (int i = 0; i < NB / 16; ++i) {
-            const uint4 v = lds128(a + 16 * i);
+            const uint4 v = lds128(a + code_off<CROW>(r, x + 16 * i));
             w[4 * i] = v.x;
             w[4 * i + 1] = v.y;
             w[4 * i + 2] = v.z;
@@ -286,19 +301,19 @@ __device__ __forceinline__ void lds_bytes(uint32_t a, uint32_t (&w)[(NB + 3) / 4
     } else if constexpr (AL >= 8 && NB % 8 == 0) {
 #pragma unroll
         for (int i = 0; i < NB / 8; ++i) {
-            const uint2 v = lds64(a + 8 * i);
+            const uint2 v = lds64(a + code_off<CROW>(r, x + 8 * i));
             w[2 * i] = v.x;
             w[2 * i + 1] = v.y;
         }
     } else if constexpr (AL >= 4 && NB % 4 == 0) {
 #pragma unroll
-        for (int i = 0; i < NB / 4; ++i) w[i] = lds32(a + 4 * i);
+        for (int i = 0; i < NB / 4; ++i) w[i] = lds32(a + code_off<CROW>(r, x + 4 * i));
     } else {
         static_assert(NB % 2 == 0, "whole 16-bit pieces");
 #pragma unroll
         for (int i = 0; i < (NB + 3) / 4; ++i) w[i] = 0u;
 #pragma unroll
-        for (int i = 0; i < NB / 2; ++i) w[i / 2] |= lds16(a + 2 * i) << (16 * (i % 2));
+        for (int i = 0; i < NB / 2; ++i) w[i / 2] |= lds16(a + code_off<CROW>(r, x + 2 * i)) << (16 * (i % 2));
     }
 }
 
@@ -411,6 +426,7 @@ __device__ __forceinline__ void v_code_pairs(const uint32_t* wa, const uint32_t*
 template <bool kBF16, int D, int BITS>
 __global__ void __launch_bounds__(QDec<D, BITS>::THREADS, kDecodeQCtasPerSm)
     decode_q_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                    const __grid_constant__ CUtensorMap tmap_kc, const __grid_constant__ CUtensorMap tmap_vc,
                     const DecodeParams p) {
     using C = QDec<D, BITS>;
     static_assert(BITS == 4 || BITS == 8, "bits");
@@ -483,6 +499,8 @@ __global__ void __launch_bounds__(QDec<D, BITS>::THREADS, kDecodeQCtasPerSm)
         if (lane == 0) {
             prefetch_tmap(&tmap_k);
             prefetch_tmap(&tmap_v);
+            prefetch_tmap(&tmap_kc);
+            prefetch_tmap(&tmap_vc);
         }
         pdl_wait();  // pool contents from the kernel before are read from here on
         const bool stalled = p.stall_test && !stall_wait(stall, abort_flag, err, p.wait_limit_ns);
@@ -511,11 +529,12 @@ __global__ void __launch_bounds__(QDec<D, BITS>::THREADS, kDecodeQCtasPerSm)
             if (lane == 0) {
                 uint8_t* st = smem + slot * C::SLOT;
                 if (i < nq) {
-                    // A quantized page: codes and scales, four contiguous pieces.
+                    // A quantized page: the code tiles by TMA (swizzled), the
+                    // scale and min rows by bulk copies.
                     const int64_t ph = static_cast<int64_t>(blk) * Hkv + h;
                     mbar_expect_tx(&full[slot], C::QSTAGE);
-                    bulk_load(st, p.qpool.k_codes + ph * C::QCODE, C::QCODE, &full[slot]);
-                    bulk_load(st + C::QOFF_V, p.qpool.v_codes + ph * C::QCODE, C::QCODE, &full[slot]);
+                    tma_load_2d(st, &tmap_kc, 0, static_cast<int32_t>(ph) * C::SK, &full[slot]);
+                    tma_load_2d(st + C::QOFF_V, &tmap_vc, 0, static_cast<int32_t>(ph) * C::SK, &full[slot]);
                     bulk_load(st + C::QOFF_KM, p.qpool.k_meta + ph * 2 * D, 4 * D, &full[slot]);
                     bulk_load(st + C::QOFF_VM, p.qpool.v_meta + ph * 2 * C::SK, 4 * C::SK, &full[slot]);
                 } else {
@@ -580,11 +599,11 @@ __global__ void __launch_bounds__(QDec<D, BITS>::THREADS, kDecodeQCtasPerSm)
             if (qst) {
                 constexpr int KW = (C::KCB + 3) / 4;
                 uint32_t c0[KW], c1[KW];
-                lds_bytes<C::KCB, C::KAL>(sb + u * C::CROW + t * C::KCB, c0);
-                lds_bytes<C::KCB, C::KAL>(sb + (u + 8) * C::CROW + t * C::KCB, c1);
-                uint32_t sw[C::KCH / 2], zw[C::KCH / 2];
-                lds_bytes<C::KCH * 2, 16>(sb + C::QOFF_KM + t * C::KCH * 2, sw);
-                lds_bytes<C::KCH * 2, 16>(sb + C::QOFF_KM + 2 * D + t * C::KCH * 2, zw);
+                lds_code<C::KCB, C::KAL, C::CROW>(sb, u, t * C::KCB, c0);
+                lds_code<C::KCB, C::KAL, C::CROW>(sb, u + 8, t * C::KCB, c1);
+                uint32_t sw[C::KCH / 2], zw[C::KCH / 2];  // the fp16 scale and min rows, unswizzled
+                lds_code<C::KCH * 2, 16, 4 * D>(sb + C::QOFF_KM, 0, t * C::KCH * 2, sw);
+                lds_code<C::KCH * 2, 16, 4 * D>(sb + C::QOFF_KM, 0, 2 * D + t * C::KCH * 2, zw);
                 float sl[4] = {0.f, 0.f, 0.f, 0.f}, sz[4] = {0.f, 0.f, 0.f, 0.f};
                 constexpr int CWU = BITS == 8 ? 2 : 1;  // code words per 8-channel run
 #pragma unroll
@@ -638,11 +657,11 @@ __global__ void __launch_bounds__(QDec<D, BITS>::THREADS, kDecodeQCtasPerSm)
             uint32_t va[VW], vb[VW], vc[VW], vd[VW];  // keys 2t, 2t+1, 2t+8, 2t+9
             uint32_t vm0 = 0u, vm1 = 0u;              // (scale, min) of keys u, u+8
             if (qst) {
-                const uint32_t vbase = sb + C::QOFF_V + u * C::VCB;
-                lds_bytes<C::VCB, C::VAL>(vbase + (2 * t) * C::CROW, va);
-                lds_bytes<C::VCB, C::VAL>(vbase + (2 * t + 1) * C::CROW, vb);
-                lds_bytes<C::VCB, C::VAL>(vbase + (2 * t + 8) * C::CROW, vc);
-                lds_bytes<C::VCB, C::VAL>(vbase + (2 * t + 9) * C::CROW, vd);
+                const uint32_t vbase = sb + C::QOFF_V;
+                lds_code<C::VCB, C::VAL, C::CROW>(vbase, 2 * t, u * C::VCB, va);
+                lds_code<C::VCB, C::VAL, C::CROW>(vbase, 2 * t + 1, u * C::VCB, vb);
+                lds_code<C::VCB, C::VAL, C::CROW>(vbase, 2 * t + 8, u * C::VCB, vc);
+                lds_code<C::VCB, C::VAL, C::CROW>(vbase, 2 * t + 9, u * C::VCB, vd);
                 vm0 = lds32(sb + C::QOFF_VM + 4 * u);
                 vm1 = lds32(sb + C::QOFF_VM + 4 * (u + 8));
             }
@@ -838,7 +857,7 @@ __global__ void __launch_bounds__(QDec<D, BITS>::THREADS, kDecodeQCtasPerSm)
 
 template <bool kBF16, int D, int BITS>
 cudaError_t launch_decode_q(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                            cudaStream_t stream) {
+                            const CUtensorMap& tkc, const CUtensorMap& tvc, cudaStream_t stream) {
     using C = QDec<D, BITS>;
     static bool attr_set = false;
     if (!attr_set) {
@@ -849,14 +868,14 @@ cudaError_t launch_decode_q(const DecodeParams& p, const CUtensorMap& tk, const 
     }
     const int ngrp = (p.group + 7) / 8;
     dim3 grid(p.max_splits * ngrp, p.pool.num_kv_heads, p.B);
-    return launch_k(decode_q_kernel<kBF16, D, BITS>, grid, C::THREADS, C::SMEM_BYTES, stream, tk, tv, p);
+    return launch_k(decode_q_kernel<kBF16, D, BITS>, grid, C::THREADS, C::SMEM_BYTES, stream, tk, tv, tkc, tvc, p);
 }
 
 template <bool kBF16, int D>
 cudaError_t launch_decode_q_d(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                              cudaStream_t stream) {
-    return p.qpool.bits == 8 ? launch_decode_q<kBF16, D, 8>(p, tk, tv, stream)
-                             : launch_decode_q<kBF16, D, 4>(p, tk, tv, stream);
+                              const CUtensorMap& tkc, const CUtensorMap& tvc, cudaStream_t stream) {
+    return p.qpool.bits == 8 ? launch_decode_q<kBF16, D, 8>(p, tk, tv, tkc, tvc, stream)
+                             : launch_decode_q<kBF16, D, 4>(p, tk, tv, tkc, tvc, stream);
 }
 
 template <bool kBF16, int BITS, int D>
@@ -899,14 +918,17 @@ cudaError_t launch_quantize_blocks(const PoolView& pool, const void* k_pool, con
 }
 
 cudaError_t launch_decode_attn_q(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                                 cudaStream_t stream) {
+                                 const CUtensorMap& tkc, const CUtensorMap& tvc, cudaStream_t stream) {
     const bool bf = p.pool.dtype == KVP_BF16;
+#define KVP_DQ(DD) \
+    return bf ? launch_decode_q_d<true, DD>(p, tk, tv, tkc, tvc, stream) : launch_decode_q_d<false, DD>(p, tk, tv, tkc, tvc, stream)
     switch (p.pool.head_dim) {
-        case 64: return bf ? launch_decode_q_d<true, 64>(p, tk, tv, stream) : launch_decode_q_d<false, 64>(p, tk, tv, stream);
-        case 96: return bf ? launch_decode_q_d<true, 96>(p, tk, tv, stream) : launch_decode_q_d<false, 96>(p, tk, tv, stream);
-        case 128: return bf ? launch_decode_q_d<true, 128>(p, tk, tv, stream) : launch_decode_q_d<false, 128>(p, tk, tv, stream);
+        case 64: KVP_DQ(64);
+        case 96: KVP_DQ(96);
+        case 128: KVP_DQ(128);
         default: return cudaErrorInvalidValue;
     }
+#undef KVP_DQ
 }
 
 }  // namespace kvp
