@@ -160,15 +160,19 @@ kvp_status kvp_quantize_blocks(const kvp_pool *pool, const kvp_qpool *qpool, con
 
 /* Decode attention over a context whose cached prefix is quantized: as
  * kvp_decode_attn, except that for sequence s the first qpages[s] entries of
- * its block table name blocks of qpool (dequantized on the fly inside the
- * kernel: code * s + z in one fp16 fused multiply-add) and the remaining
- * entries name blocks of the 16-bit pool (the live suffix).  The tensor-core
- * products of this call run in fp16 whatever the pool dtype (q and a bf16
- * pool's suffix pages are converted to fp16; accumulation, softmax, O and
- * LSE in fp32, O written in the pool dtype).  qpages: device int32 [B],
- * 0 <= qpages[s] <= pages of s (a larger value is clamped).  block_size must
- * be 16 (else KVP_ERR_UNSUPPORTED).  Workspace, splits, outputs and errors as
- * kvp_decode_attn (kvp_workspace_size op 1). */
+ * its block table name blocks of qpool and the remaining entries name blocks
+ * of the 16-bit pool (the live suffix).  The codes are dequantized inside the
+ * products: q.k = sum_c (q_c s_c) code_c + q.z with q_c s_c carried as an
+ * fp16 pair hi + lo, and sum_t P_t v_t = sum_t (P_t sv_t) code_t + sum_t P_t
+ * zv_t with P_t sv_t rounded to fp16; the products q_c s_c must lie in fp16
+ * range.  The tensor-core products of this call run in fp16 whatever the pool
+ * dtype (q and a bf16 pool's suffix pages are converted to fp16;
+ * accumulation, softmax, O and LSE in fp32, O written in the pool dtype).
+ * qpages: device int32 [B], 0 <= qpages[s] <= pages of s (a larger value is
+ * clamped).  block_size must be 16 (else KVP_ERR_UNSUPPORTED), and
+ * qpool.num_blocks * num_kv_heads * 16 < 2^31 (else KVP_ERR_INVALID_ARG).
+ * Workspace, splits, outputs and errors as kvp_decode_attn
+ * (kvp_workspace_size op 1 covers it). */
 kvp_status kvp_decode_attn_q(const kvp_pool *pool, const kvp_qpool *qpool, const int32_t *qpages, const void *q,
                              void *out, float *lse, const int32_t *context_lens, const int32_t *block_tables,
                              int32_t max_blocks, int32_t B, int32_t num_q_heads, int32_t max_context_len,
