@@ -8,13 +8,13 @@
 // channels -- asymmetric min/max codes with an fp16 scale rounded up and an
 // fp16 min rounded down, codes computed in fp32 against those stored values.
 //
-// Decode over the quantized prefix (decode_q_kernel below) keeps the 16-bit
-// decode's pipeline -- one producer warp, a 4-slot ring, two consumer warps,
-// split partials merged by merge_kernel -- but a quantized page arrives as
-// four bulk copies (codes and scales, ~57% / ~32% of its 16-bit bytes at
-// d=128) and its codes enter transposed tensor-core products straight from
-// registers, the scales folded into q and P; the live suffix's pages take the
-// 16-bit TMA path.
+// Decode over the quantized prefix (decode_q_kernel below): a quantized page
+// arrives as two TMA code tiles and two bulk copies of scales (~57% / ~32%
+// of its 16-bit bytes at d=128), and its codes enter transposed tensor-core
+// products straight from registers, the scales folded into q and P; the live
+// suffix's pages arrive as 16-bit TMA tiles.  Each warp of a CTA loads and
+// consumes its own stages from a shared ring; split partials are merged by
+// merge_kernel.
 #include "kvp_decode_impl.cuh"
 
 namespace kvp {
@@ -319,10 +319,14 @@ __device__ __forceinline__ void lds_code(uint32_t a, int r, int x, uint32_t (&w)
 
 constexpr int lowest_align(int n) { return (n & -n) >= 16 ? 16 : (n & -n); }
 
-// Two consumer warps and a producer per CTA, five CTAs per SM (registers
-// allow no more).  Measured on the mixed batch's decode: four consumer warps
-// at three CTAs per SM ran 1.3x slower.
-constexpr int kDecodeQConsumers = 2;
+// Two warps per CTA, each loading and consuming its own stages; a ring of as
+// many slots as 40 KB holds (eight at int8, ten at int4, d = 128) and five
+// CTAs per SM.  Measured on the mixed batch's decode (int8 / int4, eight
+// slots): 102 / 111 us; six slots at seven CTAs per SM 111 / 120 us, four
+// slots at eight 113 / 119 us -- the stages a warp has in flight matter more
+// than the number of warps.
+constexpr int kDecodeQWarps = 2;
+constexpr int kDecodeQRingBytes = 40 * 1024;
 constexpr int kDecodeQCtasPerSm = 5;
 
 template <int D, int BITS>
@@ -348,17 +352,18 @@ struct QDec {
     // Slots hold either kind of stage and start on 1024-byte boundaries (the
     // swizzled TMA tiles need it).
     static constexpr int SLOT = ((QSTAGE > 2 * HKBYTES ? QSTAGE : 2 * HKBYTES) + 1023) / 1024 * 1024;
-    // Eight slots, four per consumer warp: a stage's copies are in flight for
-    // a microsecond or more, so a consumer needs several stages ahead.
-    static constexpr int NS = 8;
-    static constexpr int QC = kDecodeQConsumers;  // consumer warps; warp QC is the producer
-    static constexpr int THREADS = (QC + 1) * 32;
+    // Several slots per warp: a stage's copies are in flight for a
+    // microsecond or more, so a warp needs stages ahead.
+    static constexpr int NS = (kDecodeQRingBytes / SLOT) & ~1;
+    static_assert(NS >= 4, "ring depth");
+    static constexpr int QC = kDecodeQWarps;  // warps per CTA, each loading and consuming its own stages
+    static constexpr int THREADS = QC * 32;
     static_assert(NS % QC == 0, "every slot has one owner warp");
     static constexpr int RED_FLOATS = 4 * KS + 6;  // per lane: O^T, then (m, l, bias) of its two rows
     static_assert(32 * RED_FLOATS * 4 * (QC - 1) <= NS * SLOT, "the combine fits the ring");
     static constexpr int RING_BYTES = NS * SLOT;
     static constexpr int OFF_BAR = RING_BYTES;
-    static constexpr int SMEM_BYTES = OFF_BAR + (2 * NS + 1) * 8 + 16 + 1024;
+    static constexpr int SMEM_BYTES = OFF_BAR + (NS + 1) * 8 + 16 + 1024;
 };
 
 // Pairs of the contraction for the 8 consecutive K channels in w[0..3]
@@ -434,8 +439,7 @@ __global__ void __launch_bounds__(QDec<D, BITS>::THREADS, kDecodeQCtasPerSm)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-    uint64_t* empty = full + C::NS;
-    uint64_t* stall = empty + C::NS;  // nothing arrives on it (KVP_LAUNCH_STALL_TEST)
+    uint64_t* stall = full + C::NS;  // nothing arrives on it (KVP_LAUNCH_STALL_TEST)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(stall + 1);
 
     // blockIdx.x = split * ngrp + row block (8 query heads of the group each).
@@ -471,10 +475,7 @@ __global__ void __launch_bounds__(QDec<D, BITS>::THREADS, kDecodeQCtasPerSm)
     const int nstages = nq + max(0, (key1 - qend * C::SK + C::HK - 1) / C::HK);
 
     if (tid == 0) {
-        for (int i = 0; i < C::NS; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
-        }
+        for (int i = 0; i < C::NS; ++i) mbar_init(&full[i], 1);
         mbar_init(stall, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -494,70 +495,68 @@ __global__ void __launch_bounds__(QDec<D, BITS>::THREADS, kDecodeQCtasPerSm)
 #pragma unroll
     for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
-    if (warp == C::QC) {
-        // ------------------------------ producer ------------------------------
-        if (lane == 0) {
-            prefetch_tmap(&tmap_k);
-            prefetch_tmap(&tmap_v);
-            prefetch_tmap(&tmap_kc);
-            prefetch_tmap(&tmap_vc);
+    // Every warp loads its own stages: stage i sits in slot i % NS and belongs
+    // to warp i % QC (NS is a multiple of QC), so the warp that consumes a
+    // slot refills it with its next stage -- no producer warp, no empty
+    // barriers.  Warp w's stages are i = w + QC * j, j = 0 .. nmine - 1.
+    if (lane == 0) {
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_v);
+        prefetch_tmap(&tmap_kc);
+        prefetch_tmap(&tmap_vc);
+    }
+    pdl_wait();  // pool contents from the kernel before are read from here on
+    const int nmine = nstages > warp ? (nstages - warp + C::QC - 1) / C::QC : 0;
+    int win = 0;  // block ids of this warp's stages, lane l: local index (base of the window) + l
+    // Block ids of the local stages [j0, j0 + 32), one per lane.
+    auto load_window = [&](int j0) {
+        const int si = warp + C::QC * (j0 + lane);
+        const int pg = min(si < nq ? page0 + si : qend + (si - nq) / 2, npages - 1);
+        int blk = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks + pg);
+        const int64_t nblk = pg < qp ? p.qpool.num_blocks : p.pool.num_blocks;
+        if (blk < 0 || blk >= nblk) {
+            report(err, KVP_DEVERR_BAD_BLOCK);
+            blk = 0;
         }
-        pdl_wait();  // pool contents from the kernel before are read from here on
-        const bool stalled = p.stall_test && !stall_wait(stall, abort_flag, err, p.wait_limit_ns);
-        int my_blk = 0;
-        int issued = 0;
-        for (int i = 0; i < nstages && !stalled; ++i) {
-            const int slot = i % C::NS;
-            if ((i & 31) == 0) {
-                // Block ids of the pages of the next 32 stages, one per lane.
-                const int si = i + lane;
-                const int pg = min(si < nq ? page0 + si : qend + (si - nq) / 2, npages - 1);
-                int blk = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks + pg);
-                const int64_t nblk = pg < qp ? p.qpool.num_blocks : p.pool.num_blocks;
-                if (blk < 0 || blk >= nblk) {
-                    report(err, KVP_DEVERR_BAD_BLOCK);
-                    blk = 0;
-                }
-                my_blk = blk;
-            }
-            int ok = 1;
-            if (lane == 0 && i >= C::NS)
-                ok = mbar_wait(&empty[slot], ((i / C::NS) - 1) & 1, abort_flag, err, p.wait_limit_ns);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            const int blk = __shfl_sync(0xffffffffu, my_blk, i & 31);
-            if (lane == 0) {
-                uint8_t* st = smem + slot * C::SLOT;
-                if (i < nq) {
-                    // A quantized page: the code tiles by TMA (swizzled), the
-                    // scale and min rows by bulk copies.
-                    const int64_t ph = static_cast<int64_t>(blk) * Hkv + h;
-                    mbar_expect_tx(&full[slot], C::QSTAGE);
-                    tma_load_2d(st, &tmap_kc, 0, static_cast<int32_t>(ph) * C::SK, &full[slot]);
-                    tma_load_2d(st + C::QOFF_V, &tmap_vc, 0, static_cast<int32_t>(ph) * C::SK, &full[slot]);
-                    bulk_load(st + C::QOFF_KM, p.qpool.k_meta + ph * 2 * D, 4 * D, &full[slot]);
-                    bulk_load(st + C::QOFF_VM, p.qpool.v_meta + ph * 2 * C::SK, 4 * C::SK, &full[slot]);
-                } else {
-                    // Half (i - nq) % 2 of a 16-bit page: rows of HK keys.
-                    const int32_t y = (blk * Hkv + h) * C::SK + ((i - nq) & 1) * C::HK;
-                    mbar_expect_tx(&full[slot], 2 * C::HKBYTES);
+        win = blk;
+    };
+    // The copies of local stage jn (all lanes call; lane 0 issues).
+    auto issue = [&](int jn) {
+        if ((jn & 31) == 0) load_window(jn);
+        const int blk = __shfl_sync(0xffffffffu, win, jn & 31);
+        const int i = warp + C::QC * jn;
+        const int slot = i % C::NS;
+        if (lane == 0) {
+            uint8_t* st = smem + slot * C::SLOT;
+            if (i < nq) {
+                // A quantized page: the code tiles by TMA (swizzled), the scale
+                // and min rows by bulk copies.
+                const int64_t ph = static_cast<int64_t>(blk) * Hkv + h;
+                mbar_expect_tx(&full[slot], C::QSTAGE);
+                tma_load_2d(st, &tmap_kc, 0, static_cast<int32_t>(ph) * C::SK, &full[slot]);
+                tma_load_2d(st + C::QOFF_V, &tmap_vc, 0, static_cast<int32_t>(ph) * C::SK, &full[slot]);
+                bulk_load(st + C::QOFF_KM, p.qpool.k_meta + ph * 2 * D, 4 * D, &full[slot]);
+                bulk_load(st + C::QOFF_VM, p.qpool.v_meta + ph * 2 * C::SK, 4 * C::SK, &full[slot]);
+            } else {
+                // Half (i - nq) % 2 of a 16-bit page: rows of HK keys.
+                const int32_t y = (blk * Hkv + h) * C::SK + ((i - nq) & 1) * C::HK;
+                mbar_expect_tx(&full[slot], 2 * C::HKBYTES);
 #pragma unroll
-                    for (int c = 0; c < C::NCH; ++c) {
-                        tma_load_2d(st + c * C::HREGION, &tmap_k, c * C::CW, y, &full[slot]);
-                        tma_load_2d(st + C::HKBYTES + c * C::HREGION, &tmap_v, c * C::CW, y, &full[slot]);
-                    }
+                for (int c = 0; c < C::NCH; ++c) {
+                    tma_load_2d(st + c * C::HREGION, &tmap_k, c * C::CW, y, &full[slot]);
+                    tma_load_2d(st + C::HKBYTES + c * C::HREGION, &tmap_v, c * C::CW, y, &full[slot]);
                 }
             }
-            issued = i + 1;
         }
-        // Do not leave while copies may still land in shared memory.
-        if (lane == 0) {
-            for (int i = max(0, issued - C::NS); i < issued; ++i) {
-                volatile int no_abort = 0;
-                mbar_wait(&full[i % C::NS], (i / C::NS) & 1, &no_abort, err);
-            }
-        }
-    } else {
+    };
+    // Test of the failure path: before any copy is issued, warp 0 waits on a
+    // barrier nothing arrives on until the limit runs out.
+    const bool stalled = p.stall_test && warp == 0 && !stall_wait(stall, abort_flag, err, p.wait_limit_ns);
+    int issued = 0;
+    if (!stalled)
+        for (; issued < min(C::NS / C::QC, nmine); ++issued) issue(issued);
+    int jdone = 0;
+    {
         // ------------------------------ consumers ------------------------------
         // q operand: query head r_base + u (zero past the group), the lane's
         // K channel quarter, paired as the codes are; fp16 whatever the pool.
@@ -586,7 +585,8 @@ __global__ void __launch_bounds__(QDec<D, BITS>::THREADS, kDecodeQCtasPerSm)
         }
         const float sl2 = p.scale_log2;
 
-        for (int i = warp; i < nstages; i += C::QC) {
+        for (; jdone < nmine && !stalled; ++jdone) {
+            const int i = warp + C::QC * jdone;
             const int slot = i % C::NS;
             if (!mbar_wait(&full[slot], (i / C::NS) & 1, abort_flag, err, p.wait_limit_ns)) break;
             const uint32_t sb = smem_u32(smem + slot * C::SLOT);
@@ -755,9 +755,24 @@ __global__ void __launch_bounds__(QDec<D, BITS>::THREADS, kDecodeQCtasPerSm)
                                 __byte_perm(w[0][e], w[1][e], 0x7632), 0u, 0u, pb0, pb1);
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
+            // Refill the slot with this warp's stage NS/QC ahead, once every
+            // lane's reads of it are done (and ordered before the async copy).
+            if (issued < nmine) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                issue(issued);
+                ++issued;
+            }
         }
+        // Do not leave while copies may still land in shared memory.
+        if (lane == 0) {
+            for (int jj = jdone; jj < issued; ++jj) {
+                const int i = warp + C::QC * jj;
+                volatile int no_abort = 0;
+                mbar_wait(&full[i % C::NS], (i / C::NS) & 1, &no_abort, err);
+            }
+        }
+        __syncwarp();
         // Row sums and offsets were accumulated per lane over its keys.
 #pragma unroll
         for (int x = 4; x < 32; x <<= 1) {
@@ -767,8 +782,6 @@ __global__ void __launch_bounds__(QDec<D, BITS>::THREADS, kDecodeQCtasPerSm)
             bias[1] += __shfl_xor_sync(0xffffffffu, bias[1], x);
         }
     }
-
-    if (warp == C::QC) return;
 
     // ------------------------------ epilogue ------------------------------
     // Lane: query heads r_base + 2t + j (j = 0, 1); channels u*VCH + 2 mt and
