@@ -360,3 +360,80 @@ def test_quantize_codes_at_half_step_boundaries_match_oracle(bits):
         got = _qarrays(qp)
         for a, b in zip(got, want):
             np.testing.assert_array_equal(a.astype(np.float32), b.astype(np.float32))
+
+
+@pytest.mark.parametrize("dtype,d,bits,Hq,Hkv,splits", [("bf16", 128, 8, 32, 2, 0), ("f16", 96, 4, 12, 1, 2),
+                                                        ("bf16", 64, 8, 9, 1, 1)])
+def test_quantized_decode_groups_wider_than_eight_heads(dtype, d, bits, Hq, Hkv, splits):
+    """Groups of more than 8 query heads per kv head run as blocks of 8 heads
+    (one CTA each) over the same pages."""
+    import paged_prefix_reuse_gb300 as kvp
+
+    contexts = [300, 17, 1030, 64]
+    w, st, qp, oq, bt, qpages, kb, vb = _decode_case(400 + Hq + bits, contexts, dtype, d, Hq, Hkv, bits,
+                                                     qfrac=[1.0, 0.0, 0.6, 1.0])
+    out, lse = kvp.kvp_decode_attn_q(st.pool, qp, torch.from_numpy(qpages).cuda(), st.q[st.tq:], st.ctx,
+                                     torch.from_numpy(bt).cuda(), st.max_ctx_dec, w.softmax_scale, num_splits=splits)
+    torch.cuda.synchronize()
+    assert st.pool.errors() == 0
+    want, want_lse = quant.decode_attn_q(dtype, oq, bits, kb, vb, w.q[st.tq:], w.context_lens, bt, qpages,
+                                         w.softmax_scale)
+    o = out.float().cpu().numpy().astype(np.float64)
+    assert np.abs(o - want).max() <= TOL[dtype]
+    assert np.abs(lse.cpu().numpy().T.astype(np.float64) - want_lse).max() <= LSE_TOL
+
+
+@pytest.mark.parametrize("op", ["decode", "prefill"])
+def test_quantized_kernels_stalled_wait_times_out_and_context_stays_usable(op):
+    """KVP_LAUNCH_STALL_TEST on the quantized-prefix kernels: one warp of every
+    CTA waits on a barrier nothing arrives on, gives up after the 2 ms limit
+    and reports KVP_DEVERR_TIMEOUT; the same call then runs normally and
+    matches the oracle."""
+    import paged_prefix_reuse_gb300 as kvp
+
+    if op == "decode":
+        w, st, qp, oq, bt, qpages, kb, vb = _decode_case(61, [300, 45, 700], "bf16", 128, 10, 2, 8,
+                                                         qfrac=[1.0, 0.5, 0.9])
+
+        def call(splits):
+            return kvp.kvp_decode_attn_q(st.pool, qp, torch.from_numpy(qpages).cuda(), st.q[st.tq:], st.ctx,
+                                         torch.from_numpy(bt).cuda(), st.max_ctx_dec, w.softmax_scale,
+                                         num_splits=splits)
+
+        def want():
+            return quant.decode_attn_q("bf16", oq, 8, kb, vb, w.q[st.tq:], w.context_lens, bt, qpages,
+                                       w.softmax_scale)
+    else:
+        w = wl.make_random(62, [300, 77], [131, 40], Hq=8, Hkv=2, d=128, dtype="bf16")
+        st, qp, oq, bt, qpages, kb, vb = _prefill_q_case(w, 8, [1.0, 0.5])
+
+        def call(splits):
+            return kvp.kvp_prefix_attn_q(st.pool, qp, torch.from_numpy(qpages).cuda(), st.q[: st.tq],
+                                         st.cu[: st.npf + 1], st.ctx[: st.npf], torch.from_numpy(bt[: st.npf]).cuda(),
+                                         st.max_q_pf, st.max_ctx_pf, w.softmax_scale, num_splits=splits)
+
+        def want():
+            return quant.prefix_attn_q("bf16", oq, 8, kb, vb, w.q, w.cu_seqlens_q, w.context_lens, bt, qpages,
+                                       w.softmax_scale)
+    before = kvp.kvp_get_launch_options()
+    try:
+        kvp.kvp_set_wait_limit_ns(2_000_000)  # 2 ms
+        kvp.kvp_set_launch_options(before | kvp.LAUNCH_STALL_TEST)
+        for splits in (1, 2):
+            call(splits)
+        torch.cuda.synchronize()
+    finally:
+        kvp.kvp_set_launch_options(before)
+        kvp.kvp_set_wait_limit_ns(0)
+    bits = st.pool.errors()
+    assert bits & kvp.DEVERR["timeout"], f"no timeout reported ({bits:#x})"
+    assert not bits & ~kvp.DEVERR["timeout"], f"unexpected error bits {bits:#x}"
+    st.pool.clear_errors()
+    out, lse = call(2)
+    torch.cuda.synchronize()
+    assert st.pool.errors() == 0
+    o_want, l_want = want()
+    o = out.float().cpu().numpy().astype(np.float64).reshape(o_want.shape)
+    assert np.abs(o - o_want).max() <= TOL["bf16"]
+    l = lse.cpu().numpy().astype(np.float64).T.reshape(l_want.shape)
+    assert np.abs(l - l_want).max() <= LSE_TOL
