@@ -58,10 +58,10 @@ def test_plan_cuts_long_sequences_into_aligned_chunks(groups):
 
 
 def test_auto_groups_follow_the_prefix_cta_count():
-    # one group per 152 prefix-attention CTAs, at most sixteen
+    # one group per 152 prefix-attention CTAs, or per sequence of at least 76, at most sixteen
     assert HostStep.auto_groups(wl.make_config(2), wl.make_config(2).num_prefill) == 1  # 128 CTAs
     w4 = wl.make_config(4)
-    assert HostStep.auto_groups(w4, w4.num_prefill) == 2  # 320 CTAs
+    assert HostStep.auto_groups(w4, w4.num_prefill) == 4  # 320 CTAs, four sequences of 80
     w3 = wl.make_config(3)
     assert HostStep.auto_groups(w3, w3.num_prefill) == 4
     assert HostStep.auto_groups(w3, 0) == 1
