@@ -437,3 +437,64 @@ def test_quantized_kernels_stalled_wait_times_out_and_context_stays_usable(op):
     assert np.abs(o - o_want).max() <= TOL["bf16"]
     l = lse.cpu().numpy().astype(np.float64).T.reshape(l_want.shape)
     assert np.abs(l - l_want).max() <= LSE_TOL
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quantized_decode_mixed_batch_at_full_size(bits):
+    """The decode batch of the continuous-batching step at full size, every
+    complete page quantized, in the benchmark's launch configuration
+    (automatic split count).  Eight sequences (the longest, the shortest and
+    six at random) are checked against the oracle, which quantizes their
+    pages itself from the 16-bit pool."""
+    import paged_prefix_reuse_gb300 as kvp
+    from paged_prefix_reuse_gb300.step import DeviceStep
+
+    w = wl.make_config(4)
+    st = DeviceStep(w)
+    st.run_slots()
+    st.run_append()
+    torch.cuda.synchronize()
+    pool, bs = st.pool, w.block_size
+    ctx = st.ctx[st.npf:].cpu().numpy()
+    bt = st.bt[st.npf:].cpu().numpy().copy()
+    qpages = (ctx // bs).astype(np.int32)
+    pairs, bt_q = [], bt.copy()
+    for b in range(len(ctx)):
+        for pg in range(int(qpages[b])):
+            pairs.append((int(bt[b, pg]), len(pairs)))
+            bt_q[b, pg] = len(pairs) - 1
+    qp = kvp.QuantKVPool.like(pool, len(pairs), bits)
+    kvp.kvp_quantize_blocks(pool, qp, torch.tensor(pairs, dtype=torch.int32, device="cuda"))
+    q = st.q[st.tq:]
+    out, lse = kvp.kvp_decode_attn_q(pool, qp, torch.from_numpy(qpages).cuda(), q, st.ctx[st.npf:],
+                                     torch.from_numpy(bt_q).cuda(), int(ctx.max()), w.softmax_scale)
+    torch.cuda.synchronize()
+    assert pool.errors() == 0
+
+    rng = np.random.default_rng(500 + bits)
+    pick = np.unique(np.concatenate([[int(ctx.argmax()), int(ctx.argmin())], rng.choice(len(ctx), 6, replace=False)]))
+    # The oracle's own pools: the picked sequences' blocks, gathered and renumbered.
+    blocks = sorted({int(bt[b, p]) for b in pick for p in range((int(ctx[b]) + bs - 1) // bs)})
+    where = {blk: i for i, blk in enumerate(blocks)}
+    idx = torch.tensor(blocks, dtype=torch.int64, device="cuda")
+    kb, vb = _bits(pool.k.index_select(0, idx)), _bits(pool.v.index_select(0, idx))
+    npg = (ctx[pick] + bs - 1) // bs
+    bt_o = np.zeros((len(pick), int(npg.max())), dtype=np.int64)
+    opairs = []
+    for r, b in enumerate(pick):
+        for p in range(int(npg[r])):
+            blk = where[int(bt[b, p])]
+            if p < int(qpages[b]):
+                opairs.append((blk, len(opairs)))
+                bt_o[r, p] = len(opairs) - 1
+            else:
+                bt_o[r, p] = blk
+    Hkv, d = pool.num_kv_heads, pool.head_dim
+    oq, _ = quant.quantize_blocks(w.dtype, kb, vb, quant.empty_qpool(max(1, len(opairs)), Hkv, bs, d, bits), bits,
+                                  np.array(opairs, dtype=np.int64))
+    want, want_lse = quant.decode_attn_q(w.dtype, oq, bits, kb, vb, w.q[st.tq:][pick], ctx[pick], bt_o,
+                                         qpages[pick], w.softmax_scale)
+    o = out.float().cpu().numpy().astype(np.float64)[pick]
+    assert np.isfinite(o).all()
+    assert np.abs(o - want).max() <= TOL[w.dtype]
+    assert np.abs(lse.cpu().numpy().T.astype(np.float64)[pick] - want_lse).max() <= LSE_TOL
