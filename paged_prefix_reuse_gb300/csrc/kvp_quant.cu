@@ -42,6 +42,11 @@ __device__ __forceinline__ void group_params(float mn, float mx, float levels, _
 // the same integer; when |q'| >= 512 both lie far outside [0, levels] and
 // clamp alike.  Otherwise (and for a NaN) the exact division decides, so the
 // result always equals that of the division.
+// The exact division, out of line: it is rare, and inlined at each of a
+// warp's 128 codes per page-head it made the kernel's code too large for the
+// instruction cache.
+__device__ __noinline__ int qcode_exact(float d, float s) { return __float2int_rn(__fdiv_rn(d, s)); }
+
 __device__ __forceinline__ uint32_t qcode_fast(float x, float s, float z, float r, int levels) {
     if (!(s > 0.f)) return 0u;
     const float d = __fsub_rn(x, z);
@@ -51,7 +56,7 @@ __device__ __forceinline__ uint32_t qcode_fast(float x, float s, float z, float 
     if (f < 0.4999f || fabsf(q) >= 512.f)
         c = __float2int_rn(q);
     else
-        c = __float2int_rn(__fdiv_rn(d, s));
+        c = qcode_exact(d, s);
     return static_cast<uint32_t>(min(max(c, 0), levels));
 }
 
