@@ -569,9 +569,12 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
                     // of 64 columns, twice -- for the row maximum, then for the
                     // exponentials -- and P is stored per half (the half-0 P goes
                     // over S columns already read; half 1's S lies beyond it).
+                    // The half loops are not unrolled: with every warp role of
+                    // this kernel the unrolled code overflowed the instruction
+                    // cache (ncu: 1.5 fetch stalls per issued instruction).
                     const int lim = qpos - j * kBN;  // last visible column of this tile
                     float mx = -INFINITY;
-#pragma unroll
+#pragma unroll 1
                     for (int half = 0; half < 2; ++half) {
                         uint32_t r[kBN / 2];
                         tmem_ld64_sync(lane_base + scol + half * (kBN / 2), r);
@@ -618,7 +621,7 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
                     const float2 sc = make_float2(sl2, sl2), nb = make_float2(-mref, -mref);
                     float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                      make_float2(0.f, 0.f)};
-#pragma unroll
+#pragma unroll 1
                     for (int half = 0; half < 2; ++half) {
                         uint32_t r[kBN / 2];
                         tmem_ld64_sync(lane_base + scol + half * (kBN / 2), r);
