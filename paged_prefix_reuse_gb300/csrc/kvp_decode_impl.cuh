@@ -1,7 +1,7 @@
 // kvp_decode_impl.cuh -- the 16-bit decode-attention kernel template
-// (instantiated by kvp_decode.cu; see there for the design) and the ring
-// constants that the decode over a quantized cached prefix (kvp_quant.cu)
-// shares with it.
+// (instantiated by kvp_decode.cu; see there for the design) and the small
+// shared-memory helpers (align1024) that the decode over a quantized cached
+// prefix (kvp_quant.cu) uses too.
 #pragma once
 #include "kvp_internal.cuh"
 
