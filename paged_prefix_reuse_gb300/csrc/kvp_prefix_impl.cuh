@@ -75,8 +75,11 @@ constexpr int kSoftmaxWarps = 8;                    // two warpgroups, one per q
 constexpr int kProducerWarp = kSoftmaxWarps;        // warp 8
 constexpr int kMmaWarp = kSoftmaxWarps + 1;         // warp 9
 constexpr int kThreads = (kSoftmaxWarps + 2) * 32;  // 320
-constexpr int kDequantWarp0 = kSoftmaxWarps + 2;    // warps 10-13 (quantized prefix only)
-constexpr int kDequantWarps = 4;
+constexpr int kDequantWarp0 = kSoftmaxWarps + 2;    // warps 10-17 (quantized prefix only)
+// One dequantizing warp per page of a 128-key tile.  Measured on the long
+// context: four warps (two pages each) ran int8 at the same speed but int4
+// 12% slower.
+constexpr int kDequantWarps = 8;
 __host__ __device__ constexpr int prefix_threads(int bits) { return kThreads + (bits ? kDequantWarps * 32 : 0); }
 constexpr int kBM = 128;                            // rows per query tile (TMEM lanes)
 constexpr int kRowsPerCta = 2 * kBM;
@@ -255,9 +258,10 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 a) {
     return make_uint4(pack2<false>(x.x, x.y), pack2<false>(y.x, y.y), pack2<false>(z.x, z.y), pack2<false>(w.x, w.y));
 }
 
-// One dequantizing warp's share of a K (kv 0) or V (kv 1) ring slot: rows
-// [64 dw, 64 dw + 64), i.e. pages 4 dw .. 4 dw + 3 of the tile, written as
-// fp16 in the slot's chunked, 128B-swizzled layout.  Pages i < nq come from
+// One dequantizing warp's share of a K (kv 0) or V (kv 1) ring slot: the
+// rows of pages kPagesPerWarp * dw .. kPagesPerWarp * (dw + 1) - 1 of the
+// tile (one page each with eight warps), written as fp16 in the slot's
+// chunked, 128B-swizzled layout.  Pages i < nq come from
 // the staged codes: K[t][c] = code * s_c + z_c (per channel of the page),
 // V[t][c] = code * s_t + z_t (per token), one fp16 fused multiply-add per
 // pair; columns past the head dimension are zeros.  The other pages already
@@ -565,7 +569,7 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
                     }
                     tmem_st64(lane_base + scol, pk);  // P over the first 64 columns of S
                 } else {
-                    // Fourteen warps leave 128 registers: S is read in two halves
+                    // Eighteen warps leave 96 registers: S is read in two halves
                     // of 64 columns, twice -- for the row maximum, then for the
                     // exponentials -- and P is stored per half (the half-0 P goes
                     // over S columns already read; half 1's S lies beyond it).
@@ -942,7 +946,7 @@ __global__ void __launch_bounds__(prefix_threads(BITS), 1)
     } else {
         // ====================== dequantizing warps (BITS > 0) ======================
         if constexpr (BITS > 0) {
-            const int dw = warp - kDequantWarp0;  // owns rows [64 dw, 64 dw + 64) of every slot
+            const int dw = warp - kDequantWarp0;  // owns page dw's rows of every slot
             for (int gl = 0; gl < 2 * n_local; ++gl) {
                 const int slot = gl % C::NSLOT;
                 // The slot is ours once the producer has armed it (after the MMA

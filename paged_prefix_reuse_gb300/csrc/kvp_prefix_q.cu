@@ -1,7 +1,7 @@
 // kvp_prefix_q.cu -- prefix attention over a context whose cached prefix is
 // held in the quantized pool (kvboost 0.6.0, "Optional: KV quantization":
 // cached K per channel and V per token, 8 or 4 bits): the tcgen05 prefix
-// kernel (kvp_prefix_impl.cuh) with its four dequantizing warps, for
+// kernel (kvp_prefix_impl.cuh) with its eight dequantizing warps, for
 // fp16/bf16 pools and head_dim 64/96/128 at block_size 16.
 #include "kvp_prefix_impl.cuh"
 
